@@ -1,0 +1,131 @@
+"""fp64 CPU oracle for the gated delta rule -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline legs of
+``bench.py`` may import this package.  The CUDA library never links, loads or
+calls it, and it shares no code with the CUDA path.
+
+``oracle_fwd`` / ``oracle_bwd`` run the plain per-token recurrence of
+``gdn_oracle.c`` (fp64, OpenMP over independent units).  Inputs are converted
+to fp64 exactly (bf16 and fp32 values are representable in fp64).
+
+Parity status: the forward and backward are pinned by closed forms,
+invariants, an independent chunked formulation, finite differences and
+reverse-mode autodiff (see ``tests/test_oracle_pins.py``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "gdn_oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(extra_flags=(), out_path=None, force=False) -> str:
+    """Compile gdn_oracle.c with gcc (-O2 -fopenmp); returns the .so path."""
+    out = out_path or _LIB_PATH
+    if (not force and os.path.exists(out)
+            and os.path.getmtime(out) >= os.path.getmtime(_SRC) and not extra_flags):
+        return out
+    os.makedirs(os.path.dirname(out), exist_ok=True)
+    tmp = out + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-fopenmp", "-shared", "-fPIC", "-std=c11", *extra_flags, _SRC,
+           "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, out)
+    return out
+
+
+def load(path=None):
+    """Load (building first if needed) the oracle library."""
+    global _lib
+    with _lock:
+        if path is not None:
+            return _declare(ctypes.CDLL(path))
+        if _lib is None:
+            _lib = _declare(ctypes.CDLL(build()))
+        return _lib
+
+
+def _declare(lib):
+    P = ctypes.c_void_p
+    I64 = ctypes.c_int64
+    lib.gdn_oracle_fwd.argtypes = [I64] * 7 + [P] * 6 + [ctypes.c_double, P, P, P, ctypes.c_int]
+    lib.gdn_oracle_fwd.restype = ctypes.c_int
+    lib.gdn_oracle_bwd.argtypes = ([I64] * 7 + [P] * 6 + [ctypes.c_double, P, P, P]
+                                   + [P] * 6 + [ctypes.c_int])
+    lib.gdn_oracle_bwd.restype = ctypes.c_int
+    lib.gdn_oracle_max_threads.restype = ctypes.c_int
+    return lib
+
+
+def _f64(x):
+    if x is None:
+        return None
+    if hasattr(x, "detach"):  # torch tensor: exact upcast on the CPU
+        import torch
+        x = x.detach().to("cpu", torch.float64).numpy()
+    return np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _dims(q, v, cu):
+    B, T, Hq, K = q.shape
+    Hv, V = v.shape[2], v.shape[3]
+    if cu is not None:
+        cu = np.ascontiguousarray(np.asarray(cu, dtype=np.int64))
+        n = len(cu) - 1
+    else:
+        n = B
+    return B, T, Hq, Hv, K, V, n, cu
+
+
+def max_threads(lib=None) -> int:
+    return int((lib or load()).gdn_oracle_max_threads())
+
+
+def oracle_fwd(q, k, v, g, beta, scale=None, initial_state=None, cu_seqlens=None,
+               output_final_state=True, n_threads=0, lib=None):
+    """Returns (o [B,T,Hv,V], final_state [N,Hv,K,V] or None) in fp64."""
+    lib = lib or load()
+    q, k, v, g, beta, h0 = map(_f64, (q, k, v, g, beta, initial_state))
+    B, T, Hq, Hv, K, V, n, cu = _dims(q, v, cu_seqlens)
+    if scale is None:
+        scale = K ** -0.5
+    o = np.zeros((B, T, Hv, V))
+    ht = np.zeros((n, Hv, K, V)) if output_final_state else None
+    rc = lib.gdn_oracle_fwd(B, T, Hq, Hv, K, V, n, _ptr(cu), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
+                            _ptr(beta), float(scale), _ptr(h0), _ptr(o), _ptr(ht), int(n_threads))
+    if rc != 0:
+        raise ValueError(f"oracle_fwd: bad arguments (code {rc})")
+    return o, ht
+
+
+def oracle_bwd(q, k, v, g, beta, do, scale=None, initial_state=None, dht=None,
+               cu_seqlens=None, n_threads=0, lib=None):
+    """Returns (dq, dk, dv, dbeta, dg, dh0 or None) in fp64; dg is w.r.t. the raw g."""
+    lib = lib or load()
+    q, k, v, g, beta, h0, do, dht = map(_f64, (q, k, v, g, beta, initial_state, do, dht))
+    B, T, Hq, Hv, K, V, n, cu = _dims(q, v, cu_seqlens)
+    if scale is None:
+        scale = K ** -0.5
+    dq = np.zeros_like(q); dk = np.zeros_like(k); dv = np.zeros_like(v)
+    db = np.zeros_like(beta); dg = np.zeros_like(g)
+    dh0 = np.zeros((n, Hv, K, V)) if h0 is not None else None
+    rc = lib.gdn_oracle_bwd(B, T, Hq, Hv, K, V, n, _ptr(cu), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
+                            _ptr(beta), float(scale), _ptr(h0), _ptr(do), _ptr(dht), _ptr(dq),
+                            _ptr(dk), _ptr(dv), _ptr(db), _ptr(dg), _ptr(dh0), int(n_threads))
+    if rc != 0:
+        raise ValueError(f"oracle_bwd: bad arguments (code {rc})")
+    return dq, dk, dv, db, dg, dh0
