@@ -1,0 +1,454 @@
+#!/usr/bin/env python3
+"""Benchmark of the gated delta rule chunked prefill, forward + backward, on GB300.
+
+One step = one forward pass (gdn_fwd: gate cumsum, A, state scan, o, final
+state) plus one backward pass (gdn_bwd) over the training-shaped workload
+B=2, T=8192, Hq=16, Hv=64, K=V=128, bf16 io with fp32 gates and states, all
+inputs resident in HBM.  Prints ONE JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the fp64 CPU oracle (the only reference available; it
+is a plain per-token recurrence, not a competitor) on a bounded sample of the
+same workload.  Under torchrun (N > 1) every rank runs its own replica of the
+workload (weak scaling, no collective on the data path); rank 0 prints.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from synth import make_inputs, workload  # noqa: E402
+
+WORKLOAD = "train_b2_t8192_h64"
+METRIC = "GDN chunked-prefill fwd/bwd tokens/s on 1 GB300; % of tensor/HBM roofline"
+L2_FLUSH_BYTES = 512 << 20
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+FFMA_LANES_PER_SM = 128
+N_SMS = 152
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return dict(FALLBACK_PEAKS, sm_max_mhz=2070.0), "fallback"
+
+
+# ---------------------------------------------------------------- algorithmic work
+def algorithmic(w, C=64):
+    """Algorithmic flops / bytes of one forward and one backward pass.
+
+    Per token and value head (d = K = V, e = io element bytes, G = Hv / Hq):
+      fwd flops = 2C(3K + 2V) + 3 * 2KV            (KK^T, QK^T, W, U, P U'; W S, state update, Q S)
+      bwd flops = 16 d^2 + 28 C d + 4 C^2          (recompute + reverse scan + intra-chunk backward)
+      fwd bytes = 2Ke/G + 2Ve + 8 + 4 + Ce         (q, k; v, o; g, beta; g_cum; A)
+      bwd bytes = 4Ke/G + 3Ve + 16 + Ce            (q, k, dq, dk; v, do, dv; g_cum, beta, dbeta, dg; A)
+    plus 4KV bytes per state tensor per (sequence, value head): h0, ht (fwd);
+    h0, dht, dh0 (bwd).
+    """
+    K, V, G = w.K, w.V, w.Hv // w.Hq
+    e = 2 if w.io_dtype == torch.bfloat16 else 4
+    th = w.tokens * w.Hv
+    units = w.n_seqs * w.Hv
+    st = 4 * K * V
+    nst_f = (1 if w.has_h0 else 0) + 1
+    nst_b = (1 if w.has_h0 else 0) * 2 + (1 if w.has_dht else 0)
+    d = K
+    fwd_f = th * (2 * C * (3 * K + 2 * V) + 6 * K * V)
+    bwd_f = th * (16 * d * d + 28 * C * d + 4 * C * C)
+    fwd_b = th * (2 * K * e / G + 2 * V * e + 12 + C * e) + units * st * nst_f
+    bwd_b = th * (4 * K * e / G + 3 * V * e + 16 + C * e) + units * st * nst_b
+    return dict(fwd_flops=fwd_f, bwd_flops=bwd_f, fwd_bytes=fwd_b, bwd_bytes=bwd_b)
+
+
+def kernel_work(name, w, C=64):
+    """(bound, algorithmic flops, algorithmic bytes) of one launch of a kernel
+    over workload ``w``: the share of the pass's algorithmic work that kernel
+    performs (see the design notes' kernel table)."""
+    K, V, G = w.K, w.V, w.Hv // w.Hq
+    e = 2 if w.io_dtype == torch.bfloat16 else 4
+    th = w.tokens * w.Hv
+    d = K
+    table = {
+        # CUDA-core kernels
+        "fwd_prep": ("alu", th * 2 * 2 * C * K, th * (2 * K * e / G + 12 + C * e)),
+        "fwd_scan": ("alu", th * (2 * C * (K + 2 * V) + 6 * K * V), th * (2 * K * e / G + 2 * V * e + 8)),
+        "bwd_prep": ("alu", th * 2 * 2 * C * K, th * (2 * K * e / G + 8)),
+        "bwd_state": ("alu", th * (2 * 2 * C * d + 2 * 2 * d * d), th * (K * e / G + V * e + 8)),
+        "bwd_dscan": ("alu", th * (3 * 2 * d * d + 2 * C * d), th * (2 * K * e / G + V * e + 8)),
+        "bwd_intra": ("alu", th * (4 * d * d + 26 * C * d + 4 * C * C),
+                      th * (4 * K * e / G + 3 * V * e + 16)),
+    }
+    return table.get(name)
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi sampling every 200 ms during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.idx = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.th = threading.Thread(target=self._read, daemon=True)
+            self.th.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if not self.proc:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sms, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sms.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sms:
+            return None
+        sms.sort()
+        return {"sm_mhz": sms[len(sms) // 2], "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sms)}
+
+
+# ---------------------------------------------------------------- our arm
+def kernel_profile(lib):
+    import ctypes
+    n = 32
+    names = ctypes.create_string_buffer(64 * n)
+    counts = (ctypes.c_int * n)()
+    ms = (ctypes.c_double * n)()
+    k = lib.gdn_profile_read(names, 64, counts, ms, n)
+    if k < 0:
+        raise RuntimeError("gdn_profile_read failed")
+    out = {}
+    for i in range(k):
+        nm = names.raw[64 * i:64 * (i + 1)].split(b"\0")[0].decode()
+        out[nm] = (counts[i], ms[i])
+    return out
+
+
+def run_ours(args, rank, world, local_rank):
+    import ctypes
+    import gated_delta_rule_50_gb300 as gdn
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    lib = gdn.load_library()
+    lib.gdn_profile_enable.argtypes = [ctypes.c_int]
+    lib.gdn_profile_read.argtypes = [ctypes.c_char_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
+                                     ctypes.c_int]
+    w = workload(args.workload)
+    x = make_inputs(w)
+    d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
+    cu_cpu = x["cu_seqlens"]
+    ws_f = torch.empty(gdn.workspace_bytes("fwd", d["q"], d["v"], d["cu_seqlens"], cu_cpu), dtype=torch.uint8,
+                       device=dev)
+    ws_b = torch.empty(gdn.workspace_bytes("bwd", d["q"], d["v"], d["cu_seqlens"], cu_cpu), dtype=torch.uint8,
+                       device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def fwd():
+        return gdn.chunk_gated_delta_rule_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], scale=d["scale"],
+                                              initial_state=d["h0"], cu_seqlens=d["cu_seqlens"],
+                                              cu_seqlens_cpu=cu_cpu, output_final_state=True,
+                                              workspace=ws_f)
+
+    def bwd(f):
+        g_cum, A = f[0], f[1]
+        return gdn.chunk_gated_delta_rule_bwd(d["q"], d["k"], d["v"], g_cum, d["beta"], A, d["do"],
+                                              dht=d["dht"], scale=d["scale"], initial_state=d["h0"],
+                                              cu_seqlens=d["cu_seqlens"], cu_seqlens_cpu=cu_cpu,
+                                              workspace=ws_b)
+
+    for _ in range(args.warmup):
+        bwd(fwd())
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    lib.gdn_profile_enable(1)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+            torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)           # write > L2 between timed steps
+        evs[i][0].record(stream)
+        f = fwd()
+        evs[i][1].record(stream)
+        bwd(f)
+        evs[i][2].record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    lib.gdn_profile_enable(0)
+    kprof = kernel_profile(lib)
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop()
+    fwd_ms = sum(a.elapsed_time(b) for a, b, _ in evs) / args.steps
+    bwd_ms = sum(b.elapsed_time(c) for _, b, c in evs) / args.steps
+    step_ms = fwd_ms + bwd_ms
+    if world > 1:
+        t = torch.tensor([step_ms, fwd_ms, bwd_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        step_ms, fwd_ms, bwd_ms = t.tolist()
+
+    peaks, peak_src = load_peaks()
+    alg = algorithmic(w)
+    tokens = w.tokens
+    # dominant kernel
+    launches = sum(c for c, _ in kprof.values())
+    dom = max(kprof.items(), key=lambda kv: kv[1][1]) if kprof else None
+    roof = None
+    if dom:
+        name, (cnt, tot) = dom
+        kw = kernel_work(name, w)
+        avg_s = tot / cnt / 1e3
+        if kw:
+            bound, fl, by = kw
+            if bound == "alu":
+                mhz = peaks.get("sm_max_mhz", 2070.0)
+                peak = N_SMS * FFMA_LANES_PER_SM * 2 * mhz * 1e6 / 1e12
+                ach = fl / avg_s / 1e12
+                roof = {"bound": "alu", "kernel": name, "achieved": round(ach, 3), "peak": round(peak, 1),
+                        "unit": "TFLOP/s", "frac": round(ach / peak, 4), "traffic": None,
+                        "peak_source": f"FP32 FFMA: {N_SMS} SMs x {FFMA_LANES_PER_SM} lanes x 2 x {mhz:.0f} MHz"}
+            elif bound == "hbm":
+                peak = peaks["hbm_gbs"]
+                ach = by / avg_s / 1e9
+                roof = {"bound": "hbm", "kernel": name, "achieved": round(ach, 1), "peak": peak, "unit": "GB/s",
+                        "frac": round(ach / peak, 4), "traffic": None, "peak_source": f"hbm_gbs ({peak_src})"}
+            else:
+                peak = peaks["bf16_tflops"]
+                ach = fl / avg_s / 1e12
+                roof = {"bound": "tensor", "kernel": name, "achieved": round(ach, 2), "peak": peak,
+                        "unit": "TFLOP/s", "frac": round(ach / peak, 4), "traffic": None,
+                        "peak_source": f"bf16_tflops burst ({peak_src})"}
+            roof["avg_launch_us"] = round(avg_s * 1e6, 2)
+            roof["traffic"] = TRAFFIC.get(name)
+    # whole-pass roofline (both passes, measured peaks)
+    bw = peaks["hbm_gbs"] * 1e9
+    tc = peaks["bf16_tflops"] * 1e12
+    t_roof_f = max(alg["fwd_flops"] / tc, alg["fwd_bytes"] / bw)
+    t_roof_b = max(alg["bwd_flops"] / tc, alg["bwd_bytes"] / bw)
+    res = {
+        "metric": METRIC,
+        "value": round(world * tokens / (step_ms / 1e3), 1),
+        "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(step_ms, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if w.io_dtype == torch.bfloat16 else "f32",
+        "data": "synthetic (seeded; q,k unit-norm N(0,1), v N(0,1), g=-softplus(N(0,1)) with 10% "
+                "of heads g=0, beta=sigmoid(N(0,1)), h0/dht 0.1 N(0,1))",
+        "config": {"workload": f"{w.name}: B={w.B} T={w.T} Hq={w.Hq} Hv={w.Hv} K={w.K} V={w.V} chunk=64, "
+                               "fwd+bwd per step", "global_batch": w.B * world, "seq_len": w.T,
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": "512 MB buffer written between timed steps (outside the per-step events)"},
+        "fwd": {"ms": round(fwd_ms, 4), "tokens_per_s": round(world * tokens / (fwd_ms / 1e3), 1),
+                "roofline_frac": round(t_roof_f / (fwd_ms / 1e3), 4)},
+        "bwd": {"ms": round(bwd_ms, 4), "tokens_per_s": round(world * tokens / (bwd_ms / 1e3), 1),
+                "roofline_frac": round(t_roof_b / (bwd_ms / 1e3), 4)},
+        "step_roofline_frac": round((t_roof_f + t_roof_b) / (step_ms / 1e3), 4),
+        "roofline": roof,
+        "kernels": {k: {"launches": c, "ms_total": round(t, 4)} for k, (c, t) in sorted(kprof.items())},
+        "gpu_launches": launches,
+        "clocks": clocks,
+        "wall_s_timed_region": round(wall, 4),
+        "peaks": {"source": peak_src, "hbm_gbs": peaks["hbm_gbs"], "bf16_tflops": peaks["bf16_tflops"]},
+    }
+    if not args.no_e2e:
+        res["e2e"] = run_e2e(args, w, x, dev, gdn, world)
+    if rank == 0 and not args.no_cpu_baseline and world == 1:
+        res["cpu_baseline"] = cpu_baseline(w, x, budget_s=args.cpu_budget)
+    return res
+
+
+def run_e2e(args, w, x, dev, gdn, world):
+    """Same step through the public API with host (pinned) buffers: inputs
+    copied host->device and all outputs copied back inside the timed region."""
+    names_in = ["q", "k", "v", "g", "beta", "h0", "do", "dht"]
+    host = {k: x[k].pin_memory() for k in names_in if x[k] is not None}
+    cu_cpu = x["cu_seqlens"]
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    stream = torch.cuda.current_stream(dev)
+    outs_host = None
+
+    def step():
+        nonlocal outs_host
+        d = {k: t.to(dev, non_blocking=True) for k, t in host.items()}
+        g_cum, A, o, _, ht = gdn.chunk_gated_delta_rule_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"],
+                                                            scale=x["scale"], initial_state=d.get("h0"),
+                                                            output_final_state=True, cu_seqlens_cpu=cu_cpu)
+        grads = gdn.chunk_gated_delta_rule_bwd(d["q"], d["k"], d["v"], g_cum, d["beta"], A, d["do"],
+                                               dht=d.get("dht"), scale=x["scale"], initial_state=d.get("h0"),
+                                               cu_seqlens_cpu=cu_cpu)
+        outs = [o, ht] + [t for t in grads if t is not None]
+        if outs_host is None:
+            outs_host = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
+        for hbuf, t in zip(outs_host, outs):
+            hbuf.copy_(t, non_blocking=True)
+        return sum(t.numel() * t.element_size() for t in outs)
+
+    for _ in range(max(1, args.warmup)):
+        d2h = step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        d2h = step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / args.steps
+    return {"value": round(world * w.tokens / (ms / 1e3), 1), "unit": "tokens/s", "ms_per_step": round(ms, 4),
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+
+# ---------------------------------------------------------------- CPU oracle
+def oracle_sample(w, x, n_groups):
+    """A bounded sample of the workload for the oracle: the first n_groups
+    q/k head groups (each with its G value heads), all sequences, all tokens."""
+    G = w.Hv // w.Hq
+    hv = list(range(n_groups * G))
+    s = dict(x)
+    s["q"], s["k"] = x["q"][:, :, :n_groups], x["k"][:, :, :n_groups]
+    for key in ("v", "g", "beta", "do"):
+        s[key] = x[key][:, :, hv]
+    for key in ("h0", "dht"):
+        if x[key] is not None:
+            s[key] = x[key][:, hv]
+    return s, len(hv)
+
+
+def time_oracle_step(w, s):
+    import oracle
+    t0 = time.perf_counter()
+    oracle.oracle_fwd(s["q"], s["k"], s["v"], s["g"], s["beta"], s["scale"], s["h0"],
+                      cu_seqlens=s["cu_seqlens"])
+    oracle.oracle_bwd(s["q"], s["k"], s["v"], s["g"], s["beta"], s["do"], s["scale"], s["h0"], s["dht"],
+                      cu_seqlens=s["cu_seqlens"])
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(w, x, budget_s=20.0):
+    import oracle
+    lib = oracle.load()
+    cores = oracle.max_threads(lib)
+    G = w.Hv // w.Hq
+    s, nh = oracle_sample(w, x, 1)
+    dt = time_oracle_step(w, s)
+    n_groups = max(1, min(w.Hq, int(budget_s / max(dt, 1e-3))))
+    if n_groups > 1:
+        s, nh = oracle_sample(w, x, n_groups)
+        dt = time_oracle_step(w, s)
+    # tokens/s of the whole workload = tokens processed for the sampled heads,
+    # scaled by the fraction of value heads sampled
+    value = w.tokens * (nh / w.Hv) / dt
+    return {"value": round(value, 1), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"fp64 per-token oracle fwd+bwd on {n_groups} of {w.Hq} q/k head groups "
+                      f"({nh} of {w.Hv} value heads), all {w.tokens} tokens; {dt:.1f} s; value scaled "
+                      f"to the full workload by the head fraction"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    w = workload(args.workload)
+    x = make_inputs(w)
+    import oracle
+    lib = oracle.load()
+    cores = oracle.max_threads(lib)
+    s, nh = oracle_sample(w, x, 1)
+    for _ in range(args.warmup):
+        time_oracle_step(w, s) if False else None
+    times = [time_oracle_step(w, s) for _ in range(args.steps)]
+    dt = sum(times) / len(times)
+    value = w.tokens * (nh / w.Hv) / dt
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 1), "unit": "tokens/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 2),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": f"{w.name}: B={w.B} T={w.T} Hq={w.Hq} Hv={w.Hv} "
+                                                        f"K={w.K} V={w.V}, fwd+bwd per step",
+                                            "global_batch": w.B, "seq_len": w.T},
+            "cpu_baseline": {"value": round(value, 1), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                             "sample": f"fwd+bwd of 1 of {w.Hq} q/k head groups ({nh} value heads), "
+                                       "all tokens, per step; scaled by the head fraction"},
+            "e2e": {"value": round(value, 1), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+TRAFFIC = {}  # kernel -> dram bytes per launch from the committed ncu capture (None until measured)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=WORKLOAD)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    args = ap.parse_args()
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+    local_rank = int(os.environ.get("LOCAL_RANK", 0))
+    if world > 1 and args.impl == "ours":
+        torch.distributed.init_process_group(backend="nccl" if torch.cuda.is_available() else "gloo",
+                                             device_id=torch.device("cuda", local_rank)
+                                             if torch.cuda.is_available() else None)
+    if args.impl == "reference":
+        res = run_reference(args, rank, world)
+    else:
+        res = run_ours(args, rank, world, local_rank)
+    if rank == 0 and res is not None:
+        print(json.dumps(res), flush=True)
+    if world > 1 and args.impl == "ours":
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

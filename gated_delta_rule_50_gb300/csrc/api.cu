@@ -1,0 +1,225 @@
+// api.cu -- the extern "C" entry points of include/gdn.h: host-side validation,
+// workspace layout and the launch sequence.  No device memory is allocated and
+// the stream is never synchronised (except in gdn_workspace_error, which says so).
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+
+#include "common.cuh"
+#include "gdn.h"
+#include "launch.h"
+#include "profile.h"
+
+using namespace gdn;
+
+namespace {
+
+bool aligned16(const void *ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
+bool ok_ptr(const void *ptr) { return ptr != nullptr && aligned16(ptr); }
+bool ok_opt(const void *ptr) { return ptr == nullptr || aligned16(ptr); }
+
+// Validates the problem and fills the host part of the plan.
+gdn_status make_plan(const gdn_problem *pr, Plan *pl) {
+    if (!pr) return GDN_ERR_INVALID_ARG;
+    if (pr->B < 1 || pr->T < 0 || pr->Hq < 1 || pr->Hv < 1 || pr->K < 1 || pr->V < 1)
+        return GDN_ERR_INVALID_ARG;
+    if (pr->Hv % pr->Hq != 0) return GDN_ERR_INVALID_ARG;
+    if (pr->io_dtype != GDN_F32 && pr->io_dtype != GDN_BF16) return GDN_ERR_INVALID_ARG;
+    if (pr->cp_mode < GDN_CP_AUTO || pr->cp_mode > GDN_CP_WARMUP) return GDN_ERR_INVALID_ARG;
+    if (pr->cp_mode == GDN_CP_WARMUP && (pr->warmup_chunks < 1 || pr->warmup_chunks > 64))
+        return GDN_ERR_INVALID_ARG;
+    if ((pr->K != 64 && pr->K != 128) || (pr->V != 64 && pr->V != 128)) return GDN_ERR_UNSUPPORTED;
+    if (pr->B * pr->T > INT32_MAX / 2 || pr->Hv > 65535 || pr->Hq > 65535) return GDN_ERR_UNSUPPORTED;
+    std::memset(pl, 0, sizeof(*pl));
+    pl->B = (int)pr->B; pl->T = (int)pr->T; pl->Hq = (int)pr->Hq; pl->Hv = (int)pr->Hv;
+    pl->K = (int)pr->K; pl->V = (int)pr->V; pl->G = (int)(pr->Hv / pr->Hq);
+    pl->io = pr->io_dtype;
+    pl->scale = pr->scale;
+    if (pr->cu_seqlens) {
+        if (pr->B != 1 || pr->n_seqs < 1 || !pr->cu_seqlens_host) return GDN_ERR_INVALID_ARG;
+        if (pr->n_seqs > INT32_MAX / 4) return GDN_ERR_UNSUPPORTED;
+        const int32_t *cu = pr->cu_seqlens_host;
+        if (cu[0] != 0 || cu[pr->n_seqs] != pr->T) return GDN_ERR_INVALID_ARG;
+        int64_t chunks = 0, mx = 0;
+        for (int64_t s = 0; s < pr->n_seqs; ++s) {
+            if (cu[s + 1] < cu[s]) return GDN_ERR_INVALID_ARG;
+            int64_t c = (cu[s + 1] - cu[s] + C - 1) / C;
+            chunks += c;
+            mx = c > mx ? c : mx;
+        }
+        pl->n_seqs = (int)pr->n_seqs;
+        pl->cu = pr->cu_seqlens;
+        pl->total_chunks = (int)chunks;
+        pl->max_seq_chunks = (int)mx;
+        pl->NC = 0;
+    } else {
+        if (pr->cu_seqlens_host) return GDN_ERR_INVALID_ARG;
+        if (pr->n_seqs != pr->B) return GDN_ERR_INVALID_ARG;
+        pl->n_seqs = (int)pr->B;
+        pl->NC = (int)((pr->T + C - 1) / C);
+        pl->total_chunks = pl->NC * pl->B;
+        pl->max_seq_chunks = pl->NC;
+    }
+    return GDN_OK;
+}
+
+struct FwdWs {
+    size_t err, chunk_off, gam64, A32, P32, total;
+};
+struct BwdWs {
+    size_t err, chunk_off, gam64, A32, P32, hbuf, dSe, total;
+};
+
+FwdWs fwd_layout(const Plan &p) {
+    Carve c;
+    FwdWs w;
+    size_t tokens = (size_t)p.B * p.T;
+    size_t mats = (size_t)p.total_chunks * p.Hv * C * C;
+    w.err = c.take<uint32_t>(64);
+    w.chunk_off = c.take<int32_t>((size_t)p.n_seqs + 1);
+    w.gam64 = c.take<double>(tokens * p.Hv);
+    w.A32 = c.take<float>(mats);
+    w.P32 = c.take<float>(mats);
+    w.total = c.off;
+    return w;
+}
+
+BwdWs bwd_layout(const Plan &p) {
+    Carve c;
+    BwdWs w;
+    size_t tokens = (size_t)p.B * p.T;
+    size_t mats = (size_t)p.total_chunks * p.Hv * C * C;
+    size_t states = (size_t)p.total_chunks * p.Hv * p.K * p.V;
+    w.err = c.take<uint32_t>(64);
+    w.chunk_off = c.take<int32_t>((size_t)p.n_seqs + 1);
+    w.gam64 = c.take<double>(tokens * p.Hv);
+    w.A32 = c.take<float>(mats);
+    w.P32 = c.take<float>(mats);
+    w.hbuf = c.take<float>(states);
+    w.dSe = c.take<float>(states);
+    w.total = c.off;
+    return w;
+}
+
+template <typename T> T *at(void *ws, size_t off) {
+    return reinterpret_cast<T *>(static_cast<unsigned char *>(ws) + off);
+}
+
+#define GDN_TRY(expr)                                  \
+    do {                                               \
+        cudaError_t e_ = (expr);                       \
+        if (e_ != cudaSuccess) return GDN_ERR_CUDA;    \
+    } while (0)
+
+// Launch with an optional timing bracket named after the kernel.
+#define GDN_LAUNCH(name, expr)                         \
+    do {                                               \
+        ProfScope ps_(name, st);                       \
+        GDN_TRY(expr);                                 \
+    } while (0)
+
+}  // namespace
+
+extern "C" {
+
+size_t gdn_fwd_workspace_bytes(const gdn_problem *p) {
+    Plan pl;
+    if (make_plan(p, &pl) != GDN_OK) return 0;
+    return fwd_layout(pl).total;
+}
+
+size_t gdn_bwd_workspace_bytes(const gdn_problem *p) {
+    Plan pl;
+    if (make_plan(p, &pl) != GDN_OK) return 0;
+    return bwd_layout(pl).total;
+}
+
+gdn_status gdn_fwd(const gdn_problem *p, const void *q, const void *k, const void *v, const float *g,
+                   const float *beta, const float *h0, void *o, float *g_cum, void *A, float *h,
+                   float *final_state, void *workspace, size_t workspace_bytes, gdn_stream_t stream) {
+    Plan pl;
+    gdn_status s = make_plan(p, &pl);
+    if (s != GDN_OK) return s;
+    const bool any_tok = (size_t)pl.B * pl.T > 0;
+    if (any_tok && !(ok_ptr(q) && ok_ptr(k) && ok_ptr(v) && ok_ptr(g) && ok_ptr(beta) && ok_ptr(o)))
+        return GDN_ERR_INVALID_ARG;
+    if (!(ok_opt(h0) && ok_opt(g_cum) && ok_opt(A) && ok_opt(h) && ok_opt(final_state)))
+        return GDN_ERR_INVALID_ARG;
+    FwdWs w = fwd_layout(pl);
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < w.total)
+        return GDN_ERR_WORKSPACE;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    pl.err = at<uint32_t>(workspace, w.err);
+    pl.chunk_off = pl.cu ? at<int32_t>(workspace, w.chunk_off) : nullptr;
+    GDN_TRY(cudaMemsetAsync(pl.err, 0, 256, st));
+    GDN_LAUNCH("chunk_table", launch_chunk_table(pl, st));
+    double *gam64 = at<double>(workspace, w.gam64);
+    float *A32 = at<float>(workspace, w.A32), *P32 = at<float>(workspace, w.P32);
+    if (pl.total_chunks > 0)
+        GDN_LAUNCH("fwd_prep", launch_simt_prep(pl, q, k, g, 0, beta, g_cum, A, gam64, A32, P32, st));
+    GDN_LAUNCH("fwd_scan", launch_simt_scan(pl, q, k, v, beta, gam64, A32, P32, h0, o, h, final_state, st));
+    return GDN_OK;
+}
+
+gdn_status gdn_bwd(const gdn_problem *p, const void *q, const void *k, const void *v, const float *g_cum,
+                   const float *beta, const void *A, const void *d_o, const float *dht, const float *h0,
+                   void *dq, void *dk, void *dv, float *dbeta, float *dg, float *dh0, void *workspace,
+                   size_t workspace_bytes, gdn_stream_t stream) {
+    (void)A;  // the inverse is recomputed in fp32 (see the header)
+    Plan pl;
+    gdn_status s = make_plan(p, &pl);
+    if (s != GDN_OK) return s;
+    const bool any_tok = (size_t)pl.B * pl.T > 0;
+    if (any_tok && !(ok_ptr(q) && ok_ptr(k) && ok_ptr(v) && ok_ptr(g_cum) && ok_ptr(beta) && ok_ptr(d_o) &&
+                     ok_ptr(dq) && ok_ptr(dk) && ok_ptr(dv) && ok_ptr(dbeta) && ok_ptr(dg)))
+        return GDN_ERR_INVALID_ARG;
+    if (!(ok_opt(A) && ok_opt(dht) && ok_opt(h0) && ok_opt(dh0))) return GDN_ERR_INVALID_ARG;
+    if ((h0 == nullptr) != (dh0 == nullptr)) return GDN_ERR_INVALID_ARG;
+    BwdWs w = bwd_layout(pl);
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < w.total)
+        return GDN_ERR_WORKSPACE;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    pl.err = at<uint32_t>(workspace, w.err);
+    pl.chunk_off = pl.cu ? at<int32_t>(workspace, w.chunk_off) : nullptr;
+    GDN_TRY(cudaMemsetAsync(pl.err, 0, 256, st));
+    GDN_LAUNCH("chunk_table", launch_chunk_table(pl, st));
+    double *gam64 = at<double>(workspace, w.gam64);
+    float *A32 = at<float>(workspace, w.A32), *P32 = at<float>(workspace, w.P32);
+    float *hbuf = at<float>(workspace, w.hbuf), *dSe = at<float>(workspace, w.dSe);
+    if (pl.total_chunks > 0) {
+        GDN_LAUNCH("bwd_prep", launch_simt_prep(pl, q, k, g_cum, 1, beta, nullptr, nullptr, gam64, A32, P32, st));
+        GDN_LAUNCH("bwd_state", launch_simt_scan(pl, q, k, v, beta, gam64, A32, P32, h0, nullptr, hbuf, nullptr, st));
+    }
+    GDN_LAUNCH("bwd_dscan", launch_simt_dscan(pl, q, k, d_o, beta, gam64, A32, P32, dht, dSe, dh0, st));
+    if (pl.total_chunks > 0)
+        GDN_LAUNCH("bwd_intra", launch_simt_bwd_intra(pl, q, k, v, d_o, beta, gam64, A32, P32, hbuf, dSe, dq, dk,
+                                                     dv, dbeta, dg, st));
+    return GDN_OK;
+}
+
+gdn_status gdn_workspace_error(const void *workspace, gdn_stream_t stream) {
+    if (!workspace) return GDN_ERR_INVALID_ARG;
+    uint32_t word = 0;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaMemcpyAsync(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+        return GDN_ERR_CUDA;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return GDN_ERR_CUDA;
+    return word == ERR_NONE ? GDN_OK : GDN_ERR_TIMEOUT;
+}
+
+const char *gdn_status_str(gdn_status s) {
+    switch (s) {
+        case GDN_OK: return "ok";
+        case GDN_ERR_INVALID_ARG: return "invalid argument";
+        case GDN_ERR_UNSUPPORTED: return "unsupported problem";
+        case GDN_ERR_WORKSPACE: return "workspace too small or misaligned";
+        case GDN_ERR_CUDA: return "CUDA error";
+        case GDN_ERR_TIMEOUT: return "device-side wait timed out";
+    }
+    return "unknown status";
+}
+
+const char *gdn_version(void) { return "gdn-gb300 0.1 sm_103a"; }
+
+}  // extern "C"

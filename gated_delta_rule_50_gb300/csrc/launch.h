@@ -1,0 +1,26 @@
+// launch.h -- internal host launchers shared between the C ABI and the kernel files.
+#pragma once
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+
+namespace gdn {
+
+cudaError_t launch_chunk_table(const Plan &p, cudaStream_t st);
+
+// CUDA-core (FFMA) path
+cudaError_t launch_simt_prep(const Plan &p, const void *q, const void *k, const float *g, int g_is_cum,
+                             const float *beta, float *g_cum, void *A_out, double *gam64, float *A32,
+                             float *P32, cudaStream_t st);
+cudaError_t launch_simt_scan(const Plan &p, const void *q, const void *k, const void *v, const float *beta,
+                             const double *gam64, const float *A32, const float *P32, const float *h0,
+                             void *o, float *h, float *ht, cudaStream_t st);
+cudaError_t launch_simt_dscan(const Plan &p, const void *q, const void *k, const void *d_o, const float *beta,
+                              const double *gam64, const float *A32, const float *P32, const float *dht,
+                              float *dSe, float *dh0, cudaStream_t st);
+cudaError_t launch_simt_bwd_intra(const Plan &p, const void *q, const void *k, const void *v, const void *d_o,
+                                  const float *beta, const double *gam64, const float *A32,
+                                  const float *P32, const float *hbuf, const float *dSe, void *dq, void *dk,
+                                  void *dv, float *dbeta, float *dg, cudaStream_t st);
+
+}  // namespace gdn

@@ -1,0 +1,160 @@
+/*
+ * gdn.h -- C ABI of the GB300 (sm_103a) gated delta rule chunked-prefill library.
+ *
+ * The operator (Gated DeltaNet, per value head, state S in R^{K x V}):
+ *
+ *     S_t = exp(g_t) S_{t-1} + k_t (beta_t (v_t - exp(g_t) S_{t-1}^T k_t))^T
+ *     o_t = scale * S_t^T q_t
+ *
+ * computed chunk-parallel with chunk size GDN_CHUNK = 64.  The entry points
+ * mirror the two-level API of the flash_qla 0.1.2 README (PyPI METADATA page,
+ * sections "Usage / High-level API" and "Usage / Low-level API"):
+ *
+ *     chunk_gated_delta_rule_fwd(q, k, v, g, beta, scale, initial_state, cu_seqlens)
+ *         -> (g, A, o, h, final_state)                          == gdn_fwd
+ *     chunk_gated_delta_rule_bwd(q, k, v, g, beta, A, do, dht, scale, initial_state, cu_seqlens)
+ *         -> (dq, dk, dv, db, dg, dh0)                          == gdn_bwd
+ *
+ * General conventions (every entry point):
+ *  - All tensor pointers are caller-owned DEVICE memory, row-major and
+ *    contiguous, 16-byte aligned.  The library never allocates device memory,
+ *    never synchronises the device or the stream, and enqueues all work on
+ *    the caller's `stream`.  It keeps no state between calls: concurrent calls
+ *    on different streams with different workspaces are safe.
+ *  - Arguments are validated on the host before anything is enqueued; a bad
+ *    argument returns a status and enqueues nothing.  A failed launch returns
+ *    GDN_ERR_CUDA.  Kernels that wait on an mbarrier give up after a bounded
+ *    number of polls and record GDN_ERR_TIMEOUT in the workspace's error word;
+ *    gdn_workspace_error() reads it back.
+ *  - Shapes (B = batch, T = tokens per sequence, Hq = query/key heads,
+ *    Hv = value heads, N = number of sequences):
+ *        q, k            [B, T, Hq, K]   io dtype
+ *        v, o, do, dv    [B, T, Hv, V]   io dtype
+ *        dq, dk          [B, T, Hq, K]   io dtype
+ *        g, g_cum, dg    [B, T, Hv]      fp32
+ *        beta, dbeta     [B, T, Hv]      fp32
+ *        A               [B, T, Hv, 64]  io dtype (row r of a chunk's 64x64
+ *                                        matrix stored at that chunk's token r)
+ *        h               [B, NC, Hv, K, V] fp32 (NC = chunks per sequence;
+ *                                        varlen: [total chunks, Hv, K, V])
+ *        h0, ht, dht, dh0 [N, Hv, K, V]  fp32
+ *  - Grouped value heads: Hv % Hq == 0 and value head hv reads q/k head
+ *    hv / (Hv / Hq).
+ *  - Varlen: cu_seqlens != NULL requires B == 1; sequence s covers tokens
+ *    [cu_seqlens[s], cu_seqlens[s+1]) and has its own h0 / ht; chunks never
+ *    cross a sequence boundary.
+ */
+#ifndef GDN_H_
+#define GDN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define GDN_CHUNK 64
+
+typedef struct CUstream_st *gdn_stream_t; /* == cudaStream_t; NULL = legacy default stream */
+
+typedef enum {
+    GDN_OK = 0,
+    GDN_ERR_INVALID_ARG = 1, /* null / misaligned pointer, bad shape, bad enum       */
+    GDN_ERR_UNSUPPORTED = 2, /* valid but not implemented (e.g. K or V not 64 / 128) */
+    GDN_ERR_WORKSPACE = 3,   /* workspace too small or misaligned                    */
+    GDN_ERR_CUDA = 4,        /* a CUDA launch or async call failed                   */
+    GDN_ERR_TIMEOUT = 5      /* a device-side bounded wait expired (see header)      */
+} gdn_status;
+
+typedef enum { GDN_F32 = 0, GDN_BF16 = 1 } gdn_dtype;
+
+typedef enum {
+    GDN_CP_AUTO = 0,   /* exact path; sequence splitting only where it is exact   */
+    GDN_CP_OFF = 1,    /* one serial scan per (sequence, value head)             */
+    GDN_CP_WARMUP = 2  /* approximate: segments start from a warmup state, see
+                          gdn_fwd; used only when the page's trigger rule fires   */
+} gdn_cp_mode;
+
+typedef struct {
+    int64_t B, T, Hq, Hv, K, V;      /* K, V in {64, 128}; Hv % Hq == 0              */
+    int64_t n_seqs;                  /* = B, or number of sequences when varlen      */
+    const int32_t *cu_seqlens;       /* device [n_seqs + 1] or NULL                  */
+    const int32_t *cu_seqlens_host;  /* host copy of the same offsets; required iff
+                                        cu_seqlens != NULL (used for launch planning) */
+    gdn_dtype io_dtype;              /* dtype of q, k, v, o, A, do, dq, dk, dv       */
+    float scale;                     /* output scale; K^-0.5 is the usual choice     */
+    int32_t cp_mode;                 /* gdn_cp_mode                                  */
+    int32_t warmup_chunks;           /* GDN_CP_WARMUP only: chunks of warmup (6..8)  */
+} gdn_problem;
+
+/* Bytes of device workspace gdn_fwd / gdn_bwd need for this problem (0 on a
+ * bad problem).  The workspace must be 256-byte aligned. */
+size_t gdn_fwd_workspace_bytes(const gdn_problem *p);
+size_t gdn_bwd_workspace_bytes(const gdn_problem *p);
+
+/*
+ * Forward (the README's chunk_gated_delta_rule_fwd; the high-level
+ * chunk_gated_delta_rule returns (o, final_state) of this call).
+ *   in : q, k, v (io dtype), g (raw log-decay, fp32, <= 0 expected), beta
+ *        (fp32), h0 (nullable: zero initial state).
+ *   out: o; g_cum = chunk-local inclusive cumsum of g (the README's returned
+ *        `g`); A = (I + L)^{-1} per chunk, L = strict_lower(diag(beta)
+ *        (D o K K^T)), D_ri = exp(g_cum_r - g_cum_i) (nullable: not written);
+ *        h = state entering every chunk (nullable); final_state (nullable).
+ * GDN_CP_WARMUP (the pages' sliding-window warmup, FlashQLA news page,
+ * "Technical Principles"): when the trigger fires, each segment after the
+ * first starts from the state obtained by running warmup_chunks chunks from a
+ * zero state; the result is then approximate, with error bounded by
+ * exp(sum of g over the warmup window) * |S| (see the design notes).
+ */
+gdn_status gdn_fwd(const gdn_problem *p,
+                   const void *q, const void *k, const void *v,
+                   const float *g, const float *beta, const float *h0,
+                   void *o, float *g_cum, void *A, float *h, float *final_state,
+                   void *workspace, size_t workspace_bytes, gdn_stream_t stream);
+
+/*
+ * Backward (the README's chunk_gated_delta_rule_bwd).
+ *   in : q, k, v, g_cum (the forward's returned g), beta, A (the forward's A;
+ *        nullable -- the backward recomputes the inverse in fp32 from k, beta
+ *        and g_cum because the stored copy is rounded to the io dtype),
+ *        d_o = dL/do, dht = dL/dfinal_state (nullable: zero), h0 (nullable).
+ *   out: dq, dk, dv (io dtype), dbeta, dg (fp32; dg is the gradient with
+ *        respect to the RAW g given to the forward), dh0 (required iff h0 !=
+ *        NULL; must be NULL otherwise).
+ */
+gdn_status gdn_bwd(const gdn_problem *p,
+                   const void *q, const void *k, const void *v,
+                   const float *g_cum, const float *beta, const void *A,
+                   const void *d_o, const float *dht, const float *h0,
+                   void *dq, void *dk, void *dv, float *dbeta, float *dg, float *dh0,
+                   void *workspace, size_t workspace_bytes, gdn_stream_t stream);
+
+/* Reads the device error word a previous gdn_fwd / gdn_bwd left in
+ * `workspace` (synchronises `stream`).  Returns GDN_OK or GDN_ERR_TIMEOUT. */
+gdn_status gdn_workspace_error(const void *workspace, gdn_stream_t stream);
+
+/* Static description of a status code. */
+const char *gdn_status_str(gdn_status s);
+
+/*
+ * Kernel timing (tracing; process-wide, off by default, not for concurrent
+ * use from several host threads).  While enabled, every kernel the library
+ * launches is bracketed by a pair of CUDA events recorded on the caller's
+ * stream.  gdn_profile_read() waits for the recorded events, writes up to
+ * max_entries rows (kernel name into names + i * name_stride, at most
+ * name_stride - 1 characters; launch count; summed device milliseconds) and
+ * clears the record.  Returns the number of rows, or -1 on a CUDA error.
+ * Events are host-side objects; no device memory is allocated.
+ */
+void gdn_profile_enable(int on);
+int gdn_profile_read(char *names, int name_stride, int *counts, double *ms, int max_entries);
+
+/* Library version string, e.g. "gdn-gb300 0.1 sm_103a". */
+const char *gdn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* GDN_H_ */

@@ -129,3 +129,43 @@ def oracle_bwd(q, k, v, g, beta, do, scale=None, initial_state=None, dht=None,
     if rc != 0:
         raise ValueError(f"oracle_bwd: bad arguments (code {rc})")
     return dq, dk, dv, db, dg, dh0
+
+
+def oracle_chunk_aux(k, g, beta, cu_seqlens=None, chunk=64):
+    """The forward's auxiliary outputs, from their definitions (fp64, numpy).
+
+    For every chunk of ``chunk`` tokens of every sequence (chunks restart at
+    each sequence start, the last one may be shorter) and every value head:
+
+      g_cum_r = sum_{j <= r, j in chunk} g_j                (chunk-local cumsum)
+      L_ri    = beta_r exp(g_cum_r - g_cum_i) (k_r . k_i)    for i < r, else 0
+      A       = (I + L)^{-1}  (unit lower triangular), row r stored at token r,
+                columns beyond the chunk length are 0.
+
+    k: [B,T,Hq,K]; g, beta: [B,T,Hv].  Returns (g_cum [B,T,Hv], A [B,T,Hv,chunk]).
+    Pinned in tests/test_oracle_aux.py against the per-token oracle.
+    """
+    import scipy.linalg
+    k, g, beta = _f64(k), _f64(g), _f64(beta)
+    B, T, Hq, K = k.shape
+    Hv = g.shape[2]
+    G = Hv // Hq
+    if cu_seqlens is not None:
+        cu = [int(x) for x in np.asarray(cu_seqlens)]
+        spans = [(0, cu[i], cu[i + 1]) for i in range(len(cu) - 1)]
+    else:
+        spans = [(b, 0, T) for b in range(B)]
+    g_cum = np.zeros_like(g)
+    A = np.zeros((B, T, Hv, chunk))
+    for (b, t0, t1) in spans:
+        for s in range(t0, t1, chunk):
+            e = min(t1, s + chunk)
+            n = e - s
+            for h in range(Hv):
+                gam = np.cumsum(g[b, s:e, h])
+                g_cum[b, s:e, h] = gam
+                kc = k[b, s:e, h // G]
+                L = np.tril(beta[b, s:e, h][:, None] * np.exp(gam[:, None] - gam[None, :]) * (kc @ kc.T), -1)
+                A[b, s:e, h, :n] = scipy.linalg.solve_triangular(np.eye(n) + L, np.eye(n), lower=True,
+                                                                unit_diagonal=True)
+    return g_cum, A

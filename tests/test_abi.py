@@ -1,0 +1,104 @@
+"""Host-only checks of the C ABI: the library loads, exports every symbol the
+header declares, and rejects bad arguments before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import gated_delta_rule_50_gb300 as gdn
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gdn.h")
+
+
+def declared_symbols():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(gdn_[a-z0-9_]+)\s*\(", src)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return gdn.load_library()
+
+
+def test_exports_every_declared_symbol(lib):
+    syms = declared_symbols()
+    assert "gdn_fwd" in syms and "gdn_bwd" in syms
+    for s in syms:
+        assert hasattr(lib, s), f"missing export {s}"
+
+
+def test_status_strings_and_version(lib):
+    assert lib.gdn_status_str(0) == b"ok"
+    assert b"timed out" in lib.gdn_status_str(5)
+    assert lib.gdn_version().startswith(b"gdn-gb300")
+
+
+def _prob(**kw):
+    p = gdn._Problem()
+    p.B, p.T, p.Hq, p.Hv, p.K, p.V, p.n_seqs = 1, 128, 2, 4, 128, 128, 1
+    p.io_dtype, p.scale, p.cp_mode, p.warmup_chunks = 1, 0.1, 0, 8
+    for k, v in kw.items():
+        setattr(p, k, v)
+    return p
+
+
+@pytest.mark.parametrize("kw,ok", [
+    ({}, True), ({"Hv": 3}, False), ({"K": 96}, False), ({"io_dtype": 7}, False),
+    ({"n_seqs": 2}, False), ({"cp_mode": 9}, False), ({"cp_mode": 2, "warmup_chunks": 0}, False),
+    ({"T": 0}, True), ({"B": 0}, False)])
+def test_workspace_bytes_validation(lib, kw, ok):
+    n = lib.gdn_fwd_workspace_bytes(ctypes.byref(_prob(**kw)))
+    assert (n > 0) == ok
+
+
+def test_varlen_host_offsets_validated(lib):
+    cu = (ctypes.c_int32 * 3)(0, 100, 128)
+    bad = (ctypes.c_int32 * 3)(0, 100, 120)          # does not end at T
+    dummy = ctypes.c_void_p(256)                      # never dereferenced on this path
+    p = _prob(n_seqs=2, cu_seqlens=dummy, cu_seqlens_host=ctypes.cast(cu, ctypes.c_void_p))
+    assert lib.gdn_fwd_workspace_bytes(ctypes.byref(p)) > 0
+    p.cu_seqlens_host = ctypes.cast(bad, ctypes.c_void_p)
+    assert lib.gdn_fwd_workspace_bytes(ctypes.byref(p)) == 0
+    p.cu_seqlens_host = None                          # host copy is required
+    assert lib.gdn_fwd_workspace_bytes(ctypes.byref(p)) == 0
+
+
+def test_bad_pointers_rejected_without_launch(lib):
+    p = _prob()
+    P = ctypes.c_void_p
+    # null q: rejected on the host (status 1) before any CUDA call
+    rc = lib.gdn_fwd(ctypes.byref(p), None, P(256), P(256), P(256), P(256), None, P(256), None, None,
+                     None, None, P(256), 1 << 40, None)
+    assert rc == 1
+    # misaligned pointer
+    rc = lib.gdn_fwd(ctypes.byref(p), P(257), P(256), P(256), P(256), P(256), None, P(256), None, None,
+                     None, None, P(256), 1 << 40, None)
+    assert rc == 1
+    # workspace too small
+    rc = lib.gdn_fwd(ctypes.byref(p), P(256), P(256), P(256), P(256), P(256), None, P(256), None, None,
+                     None, None, P(256), 16, None)
+    assert rc == 3
+    # bwd: dh0 must be given iff h0 is
+    rc = lib.gdn_bwd(ctypes.byref(p), *([P(256)] * 5), None, P(256), None, P(256), *([P(256)] * 5), None,
+                     P(256), 1 << 40, None)
+    assert rc == 1
+
+
+def test_python_api_names_match_pages():
+    import json
+    c = json.load(open(os.path.join(ROOT, "tests", "golden", "api_contract.json")))
+    import inspect
+    for key in ("high_level", "low_level_fwd", "low_level_bwd"):
+        fn = getattr(gdn, c[key]["name"])
+        params = list(inspect.signature(fn).parameters)
+        assert params[:len(c[key]["args"])] == c[key]["args"], (key, params)
+
+
+def test_no_cpu_path():
+    import torch
+    x = torch.zeros(1, 64, 1, 64)
+    with pytest.raises(ValueError):
+        gdn.chunk_gated_delta_rule_fwd(x, x, x, torch.zeros(1, 64, 1), torch.zeros(1, 64, 1))

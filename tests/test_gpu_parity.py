@@ -1,0 +1,122 @@
+"""CUDA path vs the fp64 oracle, element by element (needs a GB300).
+
+Small cases span several 64-token chunks and a ragged tail and cover the
+edge cases (T = 1, exact chunk multiples, empty and 1-token sequences, no
+initial state, strong decay, beta = 0, grouped heads G = 1..4, head size 64).
+The ``full_*`` cases run each benchmark workload at its full size in the
+benchmark's launch configuration and compare sampled head groups, which the
+oracle can compute independently of the others.
+"""
+import pytest
+import torch
+
+from gpu_cases import run_bwd_case, run_fwd_case
+from synth import make_inputs, workload
+
+pytestmark = pytest.mark.gpu
+
+
+def small(name, **kw):
+    return make_inputs(workload(name).scaled(**kw))
+
+
+CASES = {
+    "tiny_fp32": lambda: make_inputs(workload("tiny_fp32")),
+    "fp32_ragged_gva": lambda: small("tiny_fp32", T=150, Hq=1, Hv=3, seed=10),
+    "bf16_ragged": lambda: small("train_b2_t8192_h64", B=2, T=300, Hq=2, Hv=4, seed=11),
+    "bf16_gva4_d64": lambda: small("train_b2_t8192_h64", B=1, T=200, Hq=1, Hv=4, K=64, V=64, seed=12),
+    "bf16_t1": lambda: small("train_b2_t8192_h64", B=3, T=1, Hq=2, Hv=2, seed=13),
+    "bf16_t64": lambda: small("prefill_b4_t4096", B=1, T=64, Hq=2, Hv=4, seed=14),
+    "bf16_no_h0": lambda: small("prefill_b4_t4096", B=2, T=129, Hq=2, Hv=4, seed=15),
+    "bf16_strong_decay": lambda: small("longseq_b1_t32k_h8", T=260, Hq=1, Hv=2, g_shift=4.0, seed=16),
+    "bf16_dk64_v128": lambda: small("prefill_b4_t4096", B=1, T=100, Hq=1, Hv=2, K=64, V=128, seed=17),
+}
+
+
+def varlen_case():
+    x = small("varlen_8seq_32k", T=341, Hq=2, Hv=2, seed=18, n_varlen=6, varlen_min=1, varlen_max=200)
+    lens = [1, 64, 65, 0, 130, 81]
+    x["cu_seqlens"] = torch.tensor([0] + list(torch.tensor(lens).cumsum(0).tolist()), dtype=torch.int32)
+    return x
+
+
+CASES["bf16_varlen_edge"] = varlen_case
+
+
+def beta0_case():
+    x = small("train_b2_t8192_h64", B=1, T=140, Hq=1, Hv=2, seed=19)
+    x["beta"][..., 0] = 0.0
+    x["g"][..., 1] = 0.0
+    return x
+
+
+CASES["bf16_beta0_g0"] = beta0_case
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_fwd_small(name):
+    x = CASES[name]()
+    run_fwd_case(x)
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_bwd_small(name):
+    x = CASES[name]()
+    if x["do"] is None:
+        pytest.skip("no upstream gradient")
+    run_bwd_case(x)
+
+
+def test_fwd_h_output_and_state_continuation():
+    """The returned chunk-entry states equal the final states of prefix runs,
+    and running two halves with state passing equals one run."""
+    import gated_delta_rule_50_gb300 as gdn
+    x = small("train_b2_t8192_h64", B=1, T=256, Hq=1, Hv=2, seed=20)
+    d = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
+    _, _, o, h, ht = gdn.chunk_gated_delta_rule_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"],
+                                                    initial_state=d["h0"], output_h=True)
+    for c in (1, 2, 3):
+        t = 64 * c
+        _, _, _, _, hp = gdn.chunk_gated_delta_rule_fwd(d["q"][:, :t], d["k"][:, :t], d["v"][:, :t],
+                                                        d["g"][:, :t], d["beta"][:, :t],
+                                                        initial_state=d["h0"])
+        assert torch.allclose(h[0, c], hp[0], atol=1e-5, rtol=1e-5)
+    _, _, o1, _, h1 = gdn.chunk_gated_delta_rule_fwd(d["q"][:, :128], d["k"][:, :128], d["v"][:, :128],
+                                                     d["g"][:, :128], d["beta"][:, :128], initial_state=d["h0"])
+    _, _, o2, _, h2 = gdn.chunk_gated_delta_rule_fwd(d["q"][:, 128:], d["k"][:, 128:], d["v"][:, 128:],
+                                                     d["g"][:, 128:], d["beta"][:, 128:], initial_state=h1)
+    assert torch.allclose(torch.cat([o1, o2], 1).float(), o.float(), atol=2e-2, rtol=0)
+    assert torch.allclose(h2, ht, atol=1e-4, rtol=1e-4)
+
+
+def test_autograd_matches_low_level():
+    import gated_delta_rule_50_gb300 as gdn
+    x = small("train_b2_t8192_h64", B=1, T=130, Hq=1, Hv=2, seed=21)
+    d = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
+    leaves = [d[k].clone().requires_grad_(True) for k in ("q", "k", "v", "g", "beta", "h0")]
+    o, ht = gdn.chunk_gated_delta_rule(*leaves[:5], initial_state=leaves[5], output_final_state=True)
+    torch.autograd.backward([o, ht], [d["do"], d["dht"]])
+    g_cum, A, _, _, _ = gdn.chunk_gated_delta_rule_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"],
+                                                       initial_state=d["h0"])
+    ref = gdn.chunk_gated_delta_rule_bwd(d["q"], d["k"], d["v"], g_cum, d["beta"], A, d["do"], dht=d["dht"],
+                                         initial_state=d["h0"])
+    for leaf, r in zip(leaves, [ref[0], ref[1], ref[2], ref[4], ref[3], ref[5]]):
+        assert torch.equal(leaf.grad, r)
+
+
+# ------------------------------------------------------------- full-size workloads
+@pytest.mark.parametrize("name,groups", [("prefill_b4_t4096", [0, 9]),
+                                         ("train_b2_t8192_h64", [3]),
+                                         ("varlen_8seq_32k", [5]),
+                                         ("longseq_b1_t32k_h8", [2])])
+def test_fwd_full_size_sampled(name, groups):
+    x = make_inputs(workload(name))
+    run_fwd_case(x, groups=groups, check_aux=(name != "train_b2_t8192_h64"))
+
+
+@pytest.mark.parametrize("name,groups", [("train_b2_t8192_h64", [7]),
+                                         ("varlen_8seq_32k", [11]),
+                                         ("longseq_b1_t32k_h8", [1])])
+def test_bwd_full_size_sampled(name, groups):
+    x = make_inputs(workload(name))
+    run_bwd_case(x, groups=groups)
