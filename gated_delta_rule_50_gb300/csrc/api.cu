@@ -216,6 +216,7 @@ const char *gdn_status_str(gdn_status s) {
         case GDN_ERR_WORKSPACE: return "workspace too small or misaligned";
         case GDN_ERR_CUDA: return "CUDA error";
         case GDN_ERR_TIMEOUT: return "device-side wait timed out";
+        case GDN_ERR_TOO_LARGE: return "problem exceeds the fixed no-alloc scratch";
     }
     return "unknown status";
 }

@@ -64,7 +64,8 @@ typedef enum {
     GDN_ERR_UNSUPPORTED = 2, /* valid but not implemented (e.g. K or V not 64 / 128) */
     GDN_ERR_WORKSPACE = 3,   /* workspace too small or misaligned                    */
     GDN_ERR_CUDA = 4,        /* a CUDA launch or async call failed                   */
-    GDN_ERR_TIMEOUT = 5      /* a device-side bounded wait expired (see header)      */
+    GDN_ERR_TIMEOUT = 5,     /* a device-side bounded wait expired (see header)      */
+    GDN_ERR_TOO_LARGE = 6    /* gdn_fwd_noalloc: problem exceeds its fixed scratch     */
 } gdn_status;
 
 typedef enum { GDN_F32 = 0, GDN_BF16 = 1 } gdn_dtype;
@@ -130,6 +131,33 @@ gdn_status gdn_bwd(const gdn_problem *p,
                    const void *d_o, const float *dht, const float *h0,
                    void *dq, void *dk, void *dv, float *dbeta, float *dg, float *dh0,
                    void *workspace, size_t workspace_bytes, gdn_stream_t stream);
+
+/*
+ * gdn_fwd_noalloc -- gdn_fwd for callers that cannot allocate device memory
+ * (no counterpart in the FlashQLA pages; this is a deployment convenience).
+ * Hosts such as inference runtimes or plugin frameworks that own every device
+ * allocation, code replaying a captured CUDA graph with a frozen memory pool,
+ * or plain C callers without an allocator cannot provide gdn_fwd's
+ * workspace.  This call takes the workspace from a file-scope __device__
+ * array of GDN_NOALLOC_SCRATCH_BYTES bytes instead; it calls no cudaMalloc,
+ * cudaFree or other allocating routine.  Inputs and outputs are the caller's,
+ * exactly as for gdn_fwd.
+ *   - Problems with gdn_fwd_workspace_bytes(p) > GDN_NOALLOC_SCRATCH_BYTES
+ *     return GDN_ERR_TOO_LARGE and enqueue nothing.
+ *   - Every GPU that loads the library holds the array until process exit.
+ *   - All calls share the array; it keeps the last call's contents (each call
+ *     rewrites what it reads and clears its error word), so calls whose GPU
+ *     work overlaps -- on different streams or host threads -- race on it and
+ *     must be serialised by the caller.
+ *   - The first call on each device looks the array's address up with that
+ *     device current; make that first call before any stream capture.
+ */
+#define GDN_NOALLOC_SCRATCH_BYTES (32u << 20)
+gdn_status gdn_fwd_noalloc(const gdn_problem *p,
+                           const void *q, const void *k, const void *v,
+                           const float *g, const float *beta, const float *h0,
+                           void *o, float *g_cum, void *A, float *h, float *final_state,
+                           gdn_stream_t stream);
 
 /* Reads the device error word a previous gdn_fwd / gdn_bwd left in
  * `workspace` (synchronises `stream`).  Returns GDN_OK or GDN_ERR_TIMEOUT. */
