@@ -156,6 +156,10 @@ gdn_status gdn_fwd(const gdn_problem *p, const void *q, const void *k, const voi
     GDN_LAUNCH("chunk_table", launch_chunk_table(pl, st));
     double *gam64 = at<double>(workspace, w.gam64);
     float *A32 = at<float>(workspace, w.A32), *P32 = at<float>(workspace, w.P32);
+    if (tc_fwd_supported(pl) && p->cp_mode != GDN_CP_WARMUP) {
+        GDN_LAUNCH("fwd_tc", launch_tc_fwd(pl, q, k, v, g, beta, h0, o, g_cum, A, h, final_state, st));
+        return GDN_OK;
+    }
     if (pl.total_chunks > 0)
         GDN_LAUNCH("fwd_prep", launch_simt_prep(pl, q, k, g, 0, beta, g_cum, A, gam64, A32, P32, st));
     GDN_LAUNCH("fwd_scan", launch_simt_scan(pl, q, k, v, beta, gam64, A32, P32, h0, o, h, final_state, st));

@@ -23,4 +23,10 @@ cudaError_t launch_simt_bwd_intra(const Plan &p, const void *q, const void *k, c
                                   const float *P32, const float *hbuf, const float *dSe, void *dq, void *dk,
                                   void *dv, float *dbeta, float *dg, cudaStream_t st);
 
+// tensor-core (tcgen05) fused forward: bf16 io, K = V = 128
+bool tc_fwd_supported(const Plan &p);
+cudaError_t launch_tc_fwd(const Plan &p, const void *q, const void *k, const void *v, const float *g,
+                          const float *beta, const float *h0, void *o, float *g_cum, void *A, float *h,
+                          float *ht, cudaStream_t st);
+
 }  // namespace gdn
