@@ -193,7 +193,12 @@ gdn_status gdn_bwd(const gdn_problem *p, const void *q, const void *k, const voi
     float *hbuf = at<float>(workspace, w.hbuf), *dSe = at<float>(workspace, w.dSe);
     if (pl.total_chunks > 0) {
         GDN_LAUNCH("bwd_prep", launch_simt_prep(pl, q, k, g_cum, 1, beta, nullptr, nullptr, gam64, A32, P32, st));
-        GDN_LAUNCH("bwd_state", launch_simt_scan(pl, q, k, v, beta, gam64, A32, P32, h0, nullptr, hbuf, nullptr, st));
+        if (tc_fwd_supported(pl))
+            GDN_LAUNCH("bwd_state_tc", launch_tc_fwd(pl, q, k, v, g_cum, beta, h0, nullptr, nullptr, nullptr, hbuf,
+                                                     nullptr, st, true));
+        else
+            GDN_LAUNCH("bwd_state", launch_simt_scan(pl, q, k, v, beta, gam64, A32, P32, h0, nullptr, hbuf, nullptr,
+                                                     st));
     }
     GDN_LAUNCH("bwd_dscan", launch_simt_dscan(pl, q, k, d_o, beta, gam64, A32, P32, dht, dSe, dh0, st));
     if (pl.total_chunks > 0)

@@ -27,6 +27,6 @@ cudaError_t launch_simt_bwd_intra(const Plan &p, const void *q, const void *k, c
 bool tc_fwd_supported(const Plan &p);
 cudaError_t launch_tc_fwd(const Plan &p, const void *q, const void *k, const void *v, const float *g,
                           const float *beta, const float *h0, void *o, float *g_cum, void *A, float *h,
-                          float *ht, cudaStream_t st);
+                          float *ht, cudaStream_t st, bool g_is_cum = false);
 
 }  // namespace gdn

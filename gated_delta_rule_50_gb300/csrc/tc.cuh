@@ -51,19 +51,29 @@ __device__ __forceinline__ uint64_t global_ns() {
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
     return t;
 }
+// Potentially blocking probe: the hardware may park the warp until the phase
+// completes or a short system-defined interval elapses.
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
 // Bounded wait.  Returns false if the barrier did not complete within WAIT_NS
 // or another thread already raised *abort; on its own expiry it raises *abort.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort) {
     if (mbar_test(bar, parity)) return true;
     const uint64_t t0 = global_ns();
-    for (uint32_t i = 1;; ++i) {
-        if (mbar_test(bar, parity)) return true;
-        if ((i & 31u) == 0u) {
-            if (*abort) return false;
-            if (global_ns() - t0 > WAIT_NS) {
-                *abort = 1;
-                return false;
-            }
+    for (;;) {
+        if (mbar_try(bar, parity)) return true;
+        if (*abort) return false;
+        if (global_ns() - t0 > WAIT_NS) {
+            *abort = 1;
+            return false;
         }
     }
 }

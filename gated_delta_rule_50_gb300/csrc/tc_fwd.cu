@@ -76,6 +76,7 @@ struct FwdArgs {
     const float *g, *beta, *h0;
     __nv_bfloat16 *o, *A;
     float *g_cum, *h, *ht;
+    int g_is_cum;  // g already holds the chunk-local cumsum (backward recompute)
 };
 
 // Records the first expired wait: err[1] = barrier + 1, err[2] = chunk,
@@ -312,7 +313,7 @@ k_tc_fwd(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
                 gv = a.g[gi];
                 bv = a.beta[gi];
             }
-            if (row < 64) {
+            if (row < 64 && !a.g_is_cum) {
                 x = gv;
 #pragma unroll
                 for (int off = 1; off < 32; off <<= 1) {
@@ -322,7 +323,12 @@ k_tc_fwd(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
                 if (row == 31) *mtot = x;
             }
             named_bar(1, 128);
-            if (row >= 32 && row < 64) x += *mtot;
+            if (a.g_is_cum) {  // rows past the chunk end repeat the last value, as a cumsum of zeros would
+                const int rr = row < n ? row : n - 1;
+                x = row < 64 ? a.g[(size_t)(tok0 + rr) * p.Hv + hv] : 0.f;
+            } else if (row >= 32 && row < 64) {
+                x += *mtot;
+            }
             if (row < 64) {
                 gam[row] = x;
                 bet[row] = bv;
@@ -576,7 +582,7 @@ bool tc_fwd_supported(const Plan &p) { return p.io == GDN_BF16 && p.K == DK && p
 
 cudaError_t launch_tc_fwd(const Plan &p, const void *q, const void *k, const void *v, const float *g,
                           const float *beta, const float *h0, void *o, float *g_cum, void *A, float *h,
-                          float *ht, cudaStream_t st) {
+                          float *ht, cudaStream_t st, bool g_is_cum) {
     CUtensorMap tk, tq;
     if (!make_qk_map(&tk, k, p) || !make_qk_map(&tq, q, p)) return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(k_tc_fwd, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
@@ -591,6 +597,7 @@ cudaError_t launch_tc_fwd(const Plan &p, const void *q, const void *k, const voi
     a.g_cum = g_cum;
     a.h = h;
     a.ht = ht;
+    a.g_is_cum = g_is_cum ? 1 : 0;
     dim3 grid(p.n_seqs, p.Hv);
     k_tc_fwd<<<grid, NUM_THREADS, SMEM_BYTES, st>>>(tk, tq, p, a);
     return cudaGetLastError();
