@@ -2,6 +2,8 @@
 #pragma once
 #include <cuda_runtime.h>
 
+#include <cuda.h>
+
 #include "common.cuh"
 
 namespace gdn {
@@ -28,5 +30,13 @@ bool tc_fwd_supported(const Plan &p);
 cudaError_t launch_tc_fwd(const Plan &p, const void *q, const void *k, const void *v, const float *g,
                           const float *beta, const float *h0, void *o, float *g_cum, void *A, float *h,
                           float *ht, cudaStream_t st, bool g_is_cum = false);
+
+// TMA map of a [tokens][heads][128] bf16 tensor (64 x 1 x 64 boxes, 128-byte swizzle)
+bool make_head_map(CUtensorMap *m, const void *ptr, int heads, const Plan &p);
+
+// tensor-core reverse scan of the state gradient: bf16 io, K = V = 128
+cudaError_t launch_tc_dscan(const Plan &p, const void *q, const void *k, const void *d_o, const float *g_cum,
+                            const float *beta, const float *A32, const float *P32, const float *dht, float *dSe,
+                            float *dh0, cudaStream_t st);
 
 }  // namespace gdn

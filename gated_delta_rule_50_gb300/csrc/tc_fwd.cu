@@ -564,12 +564,12 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 }  // namespace
 
-// [tokens][Hq][128] bf16 as a 3-D tensor, boxes of 64 keys x 1 head x 64 tokens, 128-byte swizzle.
-bool make_qk_map(CUtensorMap *m, const void *ptr, const Plan &p) {
+// [tokens][heads][128] bf16 as a 3-D tensor, boxes of 64 columns x 1 head x 64 tokens, 128-byte swizzle.
+bool make_head_map(CUtensorMap *m, const void *ptr, int heads, const Plan &p) {
     auto fn = encode_fn();
     if (!fn) return false;
-    cuuint64_t dims[3] = {(cuuint64_t)DK, (cuuint64_t)p.Hq, (cuuint64_t)p.B * (cuuint64_t)p.T};
-    cuuint64_t strides[2] = {(cuuint64_t)DK * 2, (cuuint64_t)p.Hq * DK * 2};
+    cuuint64_t dims[3] = {(cuuint64_t)DK, (cuuint64_t)heads, (cuuint64_t)p.B * (cuuint64_t)p.T};
+    cuuint64_t strides[2] = {(cuuint64_t)DK * 2, (cuuint64_t)heads * DK * 2};
     cuuint32_t box[3] = {64, 1, 64};
     cuuint32_t es[3] = {1, 1, 1};
     CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box, es,
@@ -584,7 +584,7 @@ cudaError_t launch_tc_fwd(const Plan &p, const void *q, const void *k, const voi
                           const float *beta, const float *h0, void *o, float *g_cum, void *A, float *h,
                           float *ht, cudaStream_t st, bool g_is_cum) {
     CUtensorMap tk, tq;
-    if (!make_qk_map(&tk, k, p) || !make_qk_map(&tq, q, p)) return cudaErrorInvalidValue;
+    if (!make_head_map(&tk, k, p.Hq, p) || !make_head_map(&tq, q, p.Hq, p)) return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(k_tc_fwd, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
     if (e != cudaSuccess) return e;
     FwdArgs a;
