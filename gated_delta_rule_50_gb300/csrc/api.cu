@@ -204,7 +204,10 @@ gdn_status gdn_bwd(const gdn_problem *p, const void *q, const void *k, const voi
         GDN_LAUNCH("bwd_dscan_tc", launch_tc_dscan(pl, q, k, d_o, g_cum, beta, A32, P32, dht, dSe, dh0, st));
     else
         GDN_LAUNCH("bwd_dscan", launch_simt_dscan(pl, q, k, d_o, beta, gam64, A32, P32, dht, dSe, dh0, st));
-    if (pl.total_chunks > 0)
+    if (pl.total_chunks > 0 && tc_fwd_supported(pl))
+        GDN_LAUNCH("bwd_intra_tc", launch_tc_bwd_intra(pl, q, k, v, d_o, g_cum, beta, A32, P32, hbuf, dSe, dq, dk, dv,
+                                                       dbeta, dg, st));
+    else if (pl.total_chunks > 0)
         GDN_LAUNCH("bwd_intra", launch_simt_bwd_intra(pl, q, k, v, d_o, beta, gam64, A32, P32, hbuf, dSe, dq, dk,
                                                      dv, dbeta, dg, st));
     return GDN_OK;

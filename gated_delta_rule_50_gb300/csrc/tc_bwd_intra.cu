@@ -1,0 +1,661 @@
+// tc_bwd_intra.cu -- tensor-core per-chunk gradients of the chunked gated delta
+// rule (bf16 io, K = V = 128, chunk 64).
+//
+// One CTA per (chunk, q/k head) loops over the value heads of the group.  It
+// needs the chunk-entry state h and the state gradient at the chunk end dSe
+// (both from the scans) and the chunk matrices A = (I + L)^{-1}, P = D o Q K^T.
+// Per value head, with X^T denoting value-major tiles ([v][c]):
+//
+//   KS^T = h^T K^T,  QS^T = h^T Q^T                       R = diag(beta)(V - diag(Gam) KS)
+//   Dl^T = R^T A^T,  KdS^T = dSe^T K^T,  PdO^T = dO^T P   dDl = scale P^T dO + diag(E) K dSe
+//   dR^T = dDl^T A                                        dV = diag(beta) dR
+//   [Dl; R] dO^T -> dP^T (rows 0..63),  [Dl; R] dDl^T -> dA^T (rows 64..127)
+//   dL = -(A^T dA A^T) strictly lower                     (CUDA cores)
+//   dq^T += h (scale Gam o dO)^T + K^T dQK^T               dQK = D o scale dP
+//   dk^T += dSe (E o Dl)^T - h (beta Gam o dR)^T + Q^T dQK + K^T (dKK + dKK^T),  dKK = beta D o dL
+//
+// and the gate / beta gradients as row sums (dg is the reverse cumsum of dgam
+// inside the chunk).  dq and dk accumulate over the group's value heads in
+// TMEM.  Every derived operand is split into bf16 hi + lo (3 products when both
+// sides are derived); scalings are folded into the operand tiles so that the
+// TMEM accumulation is exact in structure.
+//
+// The kernel is phase-sequential: 256 threads, one of them issues the MMAs of
+// a phase and all wait on one mbarrier before the next phase.  Many CTAs (one
+// per chunk and q/k head) keep the GPU busy.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "launch.h"
+#include "tc.cuh"
+
+namespace gdn {
+namespace {
+
+using namespace tc;
+
+constexpr int DK = 128, DV = 128;
+constexpr int NT = 256;
+
+// shared memory map (bytes from a 1024-aligned base)
+constexpr uint32_t S_KQ = 0;         // [kb0: K 8K, Q 8K][kb1: K 8K, Q 8K]
+constexpr uint32_t S_DO = 32768;     // dO [r][v] 2 x 8K; later dQK hi / lo [r][i]
+constexpr uint32_t S_A = 49152;      // A hi / lo [r][i]
+constexpr uint32_t S_P = 65536;      // P hi / lo [r'][r]; later (dKK + dKK^T) hi / lo
+constexpr uint32_t S_DR = 81920;     // Dl^T hi | R^T hi | Dl^T lo | R^T lo ([v][i], 16K each); later E Dl, Y
+constexpr uint32_t S_DD = 147456;    // dDl^T hi / lo [v][r]; later scale Gam dO hi / lo [r][v]
+constexpr uint32_t S_F = 180224;     // fp32 [64][65]: dA, then dL
+constexpr uint32_t S_F2 = S_F + 64 * 65 * 4;   // fp32 [64][65]: A^T dA
+constexpr uint32_t S_VEC = S_F2 + 64 * 65 * 4; // gam, Gam, E, beta, beta Gam (64 each); per-warp partial sums
+constexpr uint32_t S_BAR = S_VEC + 5 * 256 + 2 * 8 * 64 * 4 + 2 * 8 * 4;
+constexpr uint32_t S_MISC = S_BAR + 16;
+constexpr uint32_t S_TOTAL = S_MISC + 16;
+constexpr uint32_t SMEM_BYTES = S_TOTAL + 1024;
+
+// TMEM columns
+constexpr uint32_t C_DQ = 0, C_DK = 64, C_HT = 128, C_KS = 256, C_QS = 320, C_DL = 384, C_DR = 448;
+
+constexpr uint32_t ID_KK = idesc_bf16(128, 64, 0, 0);
+constexpr uint32_t ID_MK = idesc_bf16(128, 64, 1, 0);
+constexpr uint32_t ID_MM = idesc_bf16(128, 64, 1, 1);
+constexpr uint32_t ID_KM = idesc_bf16(128, 64, 0, 1);
+
+struct IntraArgs {
+    const __nv_bfloat16 *v, *d_o;
+    const float *g_cum, *beta, *A32, *P32, *hbuf, *dSe;
+    __nv_bfloat16 *dq, *dk, *dv;
+    float *dbeta, *dg;
+};
+
+__device__ __forceinline__ uint64_t kdesc(uint32_t a) { return sdesc_sw128(a, 16, 1024); }
+__device__ __forceinline__ uint64_t mdesc(uint32_t a, uint32_t lbo) { return sdesc_sw128(a, lbo, 1024); }
+
+// x[j] on every lane -> lane l returns sum over the warp's lanes of x[l].
+__device__ __forceinline__ float warp_transpose_sum(float (&x)[32]) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+        const bool up = (lane & o) != 0;
+#pragma unroll
+        for (int j = 0; j < o; ++j) {
+            const float send = up ? x[j] : x[j + o];
+            const float keep = up ? x[j + o] : x[j];
+            x[j] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+        }
+    }
+    return x[0];
+}
+
+__device__ __forceinline__ float bf16_lo_f(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi_f(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// element (row, col) of a 64-wide bf16 hi / lo swizzled tile pair, summed
+__device__ __forceinline__ float tile_hl(const unsigned char *sm, uint32_t hi_off, uint32_t lo_off, int row, int col) {
+    const uint32_t o = (uint32_t)row * 128u + ((uint32_t)((col >> 3) ^ (row & 7)) << 4) + (uint32_t)(col & 7) * 2u;
+    const __nv_bfloat16 h = *reinterpret_cast<const __nv_bfloat16 *>(sm + hi_off + o);
+    const __nv_bfloat16 l = *reinterpret_cast<const __nv_bfloat16 *>(sm + lo_off + o);
+    return __bfloat162float(h) + __bfloat162float(l);
+}
+__device__ __forceinline__ void tile_st_hl(unsigned char *sm, uint32_t hi_off, uint32_t lo_off, int row, int col,
+                                           float x) {
+    const uint32_t o = (uint32_t)row * 128u + ((uint32_t)((col >> 3) ^ (row & 7)) << 4) + (uint32_t)(col & 7) * 2u;
+    const __nv_bfloat16 h = __float2bfloat16_rn(x);
+    *reinterpret_cast<__nv_bfloat16 *>(sm + hi_off + o) = h;
+    *reinterpret_cast<__nv_bfloat16 *>(sm + lo_off + o) = __float2bfloat16_rn(x - __bfloat162float(h));
+}
+
+__global__ void __launch_bounds__(NT, 1)
+k_tc_bwd_intra(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
+               const __grid_constant__ CUtensorMap tm_do, Plan p, IntraArgs a) {
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    unsigned char *sm = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                          ~uintptr_t(1023));
+    const uint32_t sb = smem_u32(sm);
+    const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+    const int lq = warp & 3, hh = warp >> 2;
+    const int lrow = 32 * lq + lane;  // TMEM lane of this thread (value v, or key)
+    const uint32_t trow = (uint32_t)(32 * lq) << 16;
+    uint32_t *misc = reinterpret_cast<uint32_t *>(sm + S_MISC);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(misc + 1);
+    float *gam = reinterpret_cast<float *>(sm + S_VEC), *Gm = gam + 64, *Ev = gam + 128, *bet = gam + 192,
+          *bg = gam + 256;
+    // per-warp partial sums (summed in a fixed order, so the result is deterministic):
+    // rdb / rdg [8 warps][64 rows] for dbeta / dgam, sH / sF [8] for <h, dSe> and sum F
+    float *rdb_all = gam + 320, *rdg_all = rdb_all + 8 * 64, *sH = rdg_all + 8 * 64, *sF = sH + 8;
+    float *rdb = rdb_all + 64 * warp, *rdg = rdg_all + 64 * warp;
+    float *Fa = reinterpret_cast<float *>(sm + S_F), *Fb = reinterpret_cast<float *>(sm + S_F2);
+    const uint32_t bar_tma = sb + S_BAR, bar_mma = sb + S_BAR + 8;
+
+    const int gc = blockIdx.x, hq = blockIdx.y;
+    const ChunkPos cp = chunk_pos(p, gc);
+    const int tok0 = cp.tok0, n = cp.len;
+
+    if (t == 0) {
+        mbar_init(bar_tma, 1);
+        mbar_init(bar_mma, 1);
+        misc[1] = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0) tmem_alloc(sb + S_MISC, 512);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = misc[0];
+    uint32_t tma_ph = 0, mma_ph = 0, tma_issued = 0;
+    bool ok = true;
+
+    // waits for the MMAs issued so far by thread 0 (which commits first)
+    auto mma_sync = [&]() {
+        if (t == 0) mma_commit(bar_mma);
+        bool w = mbar_wait(bar_mma, mma_ph & 1, abort_flag);
+        ++mma_ph;
+        ok = __syncthreads_and(w && ok) != 0;
+        tc_fence_after();
+    };
+    // makes generic-proxy smem writes and TMEM stores of all threads visible to the MMA issuer
+    auto pre_mma = [&]() {
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+    };
+    auto tma_wait = [&]() {
+        bool w = mbar_wait(bar_tma, tma_ph & 1, abort_flag);
+        ++tma_ph;
+        ok = __syncthreads_and(w && ok) != 0;
+    };
+
+    if (t == 0) {
+        ++tma_issued;
+        mbar_arrive_expect_tx(bar_tma, 32768);
+        tma_load_3d(sb + S_KQ, &tm_k, bar_tma, 0, hq, tok0);
+        tma_load_3d(sb + S_KQ + 8192, &tm_q, bar_tma, 0, hq, tok0);
+        tma_load_3d(sb + S_KQ + 16384, &tm_k, bar_tma, 64, hq, tok0);
+        tma_load_3d(sb + S_KQ + 24576, &tm_q, bar_tma, 64, hq, tok0);
+    }
+    tma_wait();
+
+    for (int g = 0; ok && g < p.G; ++g) {
+        const int hv = hq * p.G + g;
+        const size_t st_off = ((size_t)gc * p.Hv + hv) * DK * DV;
+        const size_t mat = ((size_t)gc * p.Hv + hv) * C * C;
+        // ---------------------------------------------------------------- per-head vectors, dO tile, A / P tiles
+        ++tma_issued;
+        if (t == 0) {
+            mbar_arrive_expect_tx(bar_tma, 16384);
+            tma_load_3d(sb + S_DO, &tm_do, bar_tma, 0, hv, tok0);
+            tma_load_3d(sb + S_DO + 8192, &tm_do, bar_tma, 64, hv, tok0);
+        }
+        if (t < 64) {
+            const float glast = a.g_cum[(size_t)(tok0 + n - 1) * p.Hv + hv];
+            float gv = glast, bv = 0.f;
+            if (t < n) {
+                gv = a.g_cum[(size_t)(tok0 + t) * p.Hv + hv];
+                bv = a.beta[(size_t)(tok0 + t) * p.Hv + hv];
+            }
+            gam[t] = gv;
+            Gm[t] = t < n ? __expf(gv) : 0.f;
+            Ev[t] = t < n ? __expf(glast - gv) : 0.f;
+            bet[t] = bv;
+            bg[t] = t < n ? bv * __expf(gv) : 0.f;
+        }
+        for (int o = t; o < 2 * 8 * 64 + 16; o += NT) rdb_all[o] = 0.f;  // rdb, rdg, sH, sF
+        {
+            const int r = t >> 2, q = t & 3;  // 16 columns of row r
+            const float *ar = a.A32 + mat + (size_t)r * C + 16 * q, *pr = a.P32 + mat + (size_t)r * C + 16 * q;
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                float av[8], pv[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    av[e] = ar[8 * hf + e];
+                    pv[e] = pr[8 * hf + e];
+                }
+                st_split_chunk(sb + S_A, sb + S_A + 8192, r, 2 * q + hf, av);
+                st_split_chunk(sb + S_P, sb + S_P + 8192, r, 2 * q + hf, pv);
+            }
+        }
+        // ---------------------------------------------------------------- P1: h^T (lane v) -> TMEM; KS, QS
+        {
+            const float *hc = a.hbuf + st_off + (size_t)(64 * hh) * DV + lrow;
+            float x[64];
+#pragma unroll
+            for (int i = 0; i < 64; ++i) x[i] = hc[(size_t)i * DV];
+            uint32_t hi[32], lo[32];
+            split_pack32(x, hi, lo);
+            tmem_st32(tmem + trow + C_HT + 32 * hh, hi);
+            tmem_st32(tmem + trow + C_HT + 64 + 32 * hh, lo);
+            tmem_wait_st();
+        }
+        __syncthreads();  // vectors visible
+        pre_mma();
+        if (t == 0) {
+            for (int sp = 0; sp < 2; ++sp)
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint32_t bo = sb + S_KQ + (kk >> 2) * 16384 + (kk & 3) * 32;
+                    mma_bf16_ta(tmem + C_KS, tmem + C_HT + 64 * sp + 8 * kk, kdesc(bo), ID_KK, (sp | kk) != 0);
+                    mma_bf16_ta(tmem + C_QS, tmem + C_HT + 64 * sp + 8 * kk, kdesc(bo + 8192), ID_KK, (sp | kk) != 0);
+                }
+        }
+        mma_sync();
+        if (!ok) break;
+        // ---------------------------------------------------------------- P2: R^T tile, dgam (scale Gam dO . QS)
+        float Xr[32], KSr[32];  // (V - Gam KS) and KS at chunk rows c = 32 hh + i, value lrow
+        {
+            uint32_t ks[32], qs[32];
+            tmem_ld32(tmem + trow + C_KS + 32 * hh, ks);
+            tmem_ld32(tmem + trow + C_QS + 32 * hh, qs);
+            tmem_wait_ld();
+            float part[32];
+            const uint16_t *vp = reinterpret_cast<const uint16_t *>(a.v) + (size_t)hv * DV + lrow;
+            const uint16_t *dp = reinterpret_cast<const uint16_t *>(a.d_o) + (size_t)hv * DV + lrow;
+            const size_t rs = (size_t)p.Hv * DV;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const int c = 32 * hh + i;
+                float vv = 0.f, dd = 0.f;
+                if (c < n) {
+                    vv = __uint_as_float((uint32_t)vp[(size_t)(tok0 + c) * rs] << 16);
+                    dd = __uint_as_float((uint32_t)dp[(size_t)(tok0 + c) * rs] << 16);
+                }
+                KSr[i] = __uint_as_float(ks[i]);
+                Xr[i] = vv - Gm[c] * KSr[i];
+                part[i] = p.scale * Gm[c] * dd * __uint_as_float(qs[i]);
+            }
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+                float r8[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) r8[e] = bet[32 * hh + 8 * q4 + e] * Xr[8 * q4 + e];
+                st_split_chunk(sb + S_DR + 16384, sb + S_DR + 49152, lrow, 4 * hh + q4, r8);
+            }
+            rdg[32 * hh + lane] += warp_transpose_sum(part);
+        }
+        // dSe^T (lane v) -> TMEM (h^T no longer needed); <h, dSe> partial
+        {
+            const float *dc = a.dSe + st_off + (size_t)(64 * hh) * DV + lrow;
+            const float *hc = a.hbuf + st_off + (size_t)(64 * hh) * DV + lrow;
+            float x[64], hd = 0.f;
+#pragma unroll
+            for (int i = 0; i < 64; ++i) {
+                x[i] = dc[(size_t)i * DV];
+                hd = fmaf(x[i], hc[(size_t)i * DV], hd);
+            }
+#pragma unroll
+            for (int o = 16; o >= 1; o >>= 1) hd += __shfl_xor_sync(0xffffffffu, hd, o);
+            if (lane == 0) sH[warp] += hd;
+            uint32_t hi[32], lo[32];
+            split_pack32(x, hi, lo);
+            tmem_st32(tmem + trow + C_HT + 32 * hh, hi);
+            tmem_st32(tmem + trow + C_HT + 64 + 32 * hh, lo);
+            tmem_wait_st();
+        }
+        tma_wait();  // dO tile of this head
+        if (!ok) break;
+        pre_mma();
+        if (t == 0) {
+            for (int tt = 0; tt < 3; ++tt)  // Dl^T = R^T A^T
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_bf16(tmem + C_DL, kdesc(sb + S_DR + 16384 + (tt == 2 ? 32768 : 0) + kk * 32),
+                             kdesc(sb + S_A + (tt == 1 ? 8192 : 0) + kk * 32), ID_KK, (tt | kk) != 0);
+            for (int sp = 0; sp < 2; ++sp)  // KdS^T = dSe^T K^T
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_bf16_ta(tmem + C_KS, tmem + C_HT + 64 * sp + 8 * kk,
+                                kdesc(sb + S_KQ + (kk >> 2) * 16384 + (kk & 3) * 32), ID_KK, (sp | kk) != 0);
+            for (int sp = 0; sp < 2; ++sp)  // PdO^T = dO^T P
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_bf16(tmem + C_QS, mdesc(sb + S_DO + kk * 2048, 8192),
+                             mdesc(sb + S_P + 8192 * sp + kk * 2048, 8192), ID_MM, (sp | kk) != 0);
+        }
+        mma_sync();
+        if (!ok) break;
+        // ---------------------------------------------------------------- P3: dDl^T and Dl^T tiles; F
+        {
+            uint32_t dl[32], kd[32], pd[32];
+            tmem_ld32(tmem + trow + C_DL + 32 * hh, dl);
+            tmem_ld32(tmem + trow + C_KS + 32 * hh, kd);
+            tmem_ld32(tmem + trow + C_QS + 32 * hh, pd);
+            tmem_wait_ld();
+            float part[32];
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+                float x8[8], d8[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const int i = 8 * q4 + e, c = 32 * hh + i;
+                    x8[e] = fmaf(p.scale, __uint_as_float(pd[i]), Ev[c] * __uint_as_float(kd[i]));
+                    d8[e] = __uint_as_float(dl[i]);
+                    part[i] = Ev[c] * __uint_as_float(kd[i]) * d8[e];
+                }
+                st_split_chunk(sb + S_DD, sb + S_DD + 16384, lrow, 4 * hh + q4, x8);
+                st_split_chunk(sb + S_DR, sb + S_DR + 32768, lrow, 4 * hh + q4, d8);
+            }
+            const float f = warp_transpose_sum(part);  // F of row 32 hh + lane (partial over 32 values)
+            rdg[32 * hh + lane] -= f;
+            float fs = f;
+#pragma unroll
+            for (int o = 16; o >= 1; o >>= 1) fs += __shfl_xor_sync(0xffffffffu, fs, o);
+            if (lane == 0) sF[warp] += fs;
+        }
+        pre_mma();
+        if (t == 0) {
+            for (int tt = 0; tt < 3; ++tt)  // dR^T = dDl^T A  (A read MN-major)
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_bf16(tmem + C_DR, kdesc(sb + S_DD + (tt == 2 ? 16384 : 0) + kk * 32),
+                             mdesc(sb + S_A + (tt == 1 ? 8192 : 0) + kk * 2048, 8192), ID_KM, (tt | kk) != 0);
+            for (int sp = 0; sp < 2; ++sp)  // [Dl; R] dO^T  -> dP^T in lanes 0..63
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_bf16(tmem + C_KS, mdesc(sb + S_DR + 32768 * sp + kk * 2048, 16384),
+                             kdesc(sb + S_DO + (kk >> 2) * 8192 + (kk & 3) * 32), ID_MK, (sp | kk) != 0);
+            for (int tt = 0; tt < 3; ++tt)  // [Dl; R] dDl^T -> dA^T in lanes 64..127
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_bf16(tmem + C_QS, mdesc(sb + S_DR + (tt == 2 ? 32768 : 0) + kk * 2048, 16384),
+                             mdesc(sb + S_DD + (tt == 1 ? 16384 : 0) + kk * 2048, 8192), ID_MM, (tt | kk) != 0);
+        }
+        mma_sync();
+        if (!ok) break;
+        // ---------------------------------------------------------------- P4: dV, dbeta, dgam terms, E Dl / Y tiles
+        {
+            uint32_t dr[32], dl[32];
+            tmem_ld32(tmem + trow + C_DR + 32 * hh, dr);
+            tmem_ld32(tmem + trow + C_DL + 32 * hh, dl);
+            tmem_wait_ld();
+            float pb[32], pg[32];
+            uint16_t *dvp = reinterpret_cast<uint16_t *>(a.dv) + (size_t)hv * DV + lrow;
+            const size_t rs = (size_t)p.Hv * DV;
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+                float y8[8], e8[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const int i = 8 * q4 + e, c = 32 * hh + i;
+                    const float drv = __uint_as_float(dr[i]);
+                    if (c < n) {
+                        __nv_bfloat16 b = __float2bfloat16_rn(bet[c] * drv);
+                        dvp[(size_t)(tok0 + c) * rs] = *reinterpret_cast<uint16_t *>(&b);
+                    }
+                    pb[i] = drv * Xr[i];
+                    pg[i] = -bg[c] * drv * KSr[i];
+                    y8[e] = -bg[c] * drv;
+                    e8[e] = Ev[c] * __uint_as_float(dl[i]);
+                }
+                st_split_chunk(sb + S_DR, sb + S_DR + 32768, lrow, 4 * hh + q4, e8);
+                st_split_chunk(sb + S_DR + 16384, sb + S_DR + 49152, lrow, 4 * hh + q4, y8);
+            }
+            rdb[32 * hh + lane] += warp_transpose_sum(pb);
+            rdg[32 * hh + lane] += warp_transpose_sum(pg);
+        }
+        {  // dP (lanes 0..63) and dA (lanes 64..127): thread holds column i, rows r = 32 hh + j
+            uint32_t dd[32];
+            tmem_ld32(tmem + trow + (lq < 2 ? C_KS : C_QS) + 32 * hh, dd);
+            tmem_wait_ld();
+            if (lq < 2) {
+                const int i = lrow;
+                float colsum = 0.f, rowpart[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const int r = 32 * hh + j;
+                    float m = 0.f;
+                    if (i <= r && r < n) {
+                        const float dpv = p.scale * __uint_as_float(dd[j]);
+                        m = dpv * a.P32[mat + (size_t)r * C + i];
+                        Fb[r * 65 + i] = __expf(gam[r] - gam[i]) * dpv;  // dQK, staged
+                    } else {
+                        Fb[r * 65 + i] = 0.f;
+                    }
+                    rowpart[j] = m;
+                    colsum += m;
+                }
+                rdg[i] -= colsum;
+                __syncwarp();
+                rdg[32 * hh + lane] += warp_transpose_sum(rowpart);
+            } else {
+                const int i = lrow - 64;
+#pragma unroll
+                for (int j = 0; j < 32; ++j) Fa[(32 * hh + j) * 65 + i] = __uint_as_float(dd[j]);  // dA[r][i]
+            }
+        }
+        __syncthreads();
+        // scale Gam o dO tile [r][v] into the dDl region (its last reader, dA^T, is done)
+        {
+            const int r = t >> 2, q = t & 3;  // 32 values: block q >> 1, chunks 4 (q & 1) .. + 3
+            const float gs = p.scale * Gm[r];
+            const int vb = q >> 1;
+#pragma unroll
+            for (int c4 = 0; c4 < 4; ++c4) {
+                const int ch = 4 * (q & 1) + c4;
+                const uint4 w = *reinterpret_cast<const uint4 *>(sm + S_DO + vb * 8192 + r * 128 + ((ch ^ (r & 7)) << 4));
+                const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+                float x8[8];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    x8[2 * e] = gs * bf16_lo_f(u[e]);
+                    x8[2 * e + 1] = gs * bf16_hi_f(u[e]);
+                }
+                st_split_chunk(sb + S_DD + vb * 8192, sb + S_DD + 16384 + vb * 8192, r, ch, x8);
+            }
+        }
+        __syncthreads();
+        // dQK -> hi / lo tile [r][i] in the dO region
+        for (int o = t; o < 64 * 8; o += NT) {
+            const int r = o >> 3, ch = o & 7;
+            float x8[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) x8[e] = Fb[r * 65 + 8 * ch + e];
+            st_split_chunk(sb + S_DO, sb + S_DO + 8192, r, ch, x8);
+        }
+        __syncthreads();  // the staged dQK in Fb is consumed before Fb is reused
+        // ---------------------------------------------------------------- P5: dL = -(A^T dA A^T), strictly lower
+        for (int o = t; o < 64 * 64; o += NT) {  // Fb = A^T dA
+            const int r = o >> 6, i = o & 63;
+            float s = 0.f;
+            for (int k = max(r, i); k < C; ++k) s = fmaf(tile_hl(sm, S_A, S_A + 8192, k, r), Fa[k * 65 + i], s);
+            Fb[r * 65 + i] = s;
+        }
+        __syncthreads();
+        for (int o = t; o < 64 * 64; o += NT) {  // Fa = dL
+            const int r = o >> 6, i = o & 63;
+            float s = 0.f;
+            if (i < r)
+                for (int l = 0; l <= i; ++l) s = fmaf(Fb[r * 65 + l], tile_hl(sm, S_A, S_A + 8192, i, l), s);
+            Fa[r * 65 + i] = -s;
+        }
+        __syncthreads();
+        // K K^T for the beta and gate terms of dL (lanes 0..63 of a [K; Q] K^T product)
+        pre_mma();
+        if (t == 0)
+            for (int kk = 0; kk < 8; ++kk) {
+                const uint32_t off = sb + S_KQ + (kk >> 2) * 16384 + (kk & 3) * 32;
+                mma_bf16(tmem + C_KS, kdesc(off), kdesc(off), ID_KK, kk);
+            }
+        mma_sync();
+        if (!ok) break;
+        if (lq < 2) {  // thread: row r = lrow, columns i = 32 hh + j
+            uint32_t kk[32];
+            tmem_ld32(tmem + trow + C_KS + 32 * hh, kk);
+            tmem_wait_ld();
+            const int r = lrow;
+            float sb_ = 0.f, sg = 0.f, colpart[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                const int i = 32 * hh + j;
+                float m = 0.f;
+                if (i < r && r < n) {
+                    const float w = Fa[r * 65 + i] * __expf(gam[r] - gam[i]) * __uint_as_float(kk[j]);
+                    sb_ += w;
+                    m = w * bet[r];
+                    sg += m;
+                }
+                colpart[j] = m;
+            }
+            rdb[r] += sb_;
+            rdg[r] += sg;
+            __syncwarp();
+            rdg[32 * hh + lane] -= warp_transpose_sum(colpart);
+        }
+        // dKK + dKK^T -> hi / lo tile [r][i] in the P region (dKK_ri = beta_r D_ri dL_ri, i < r)
+        for (int o = t; o < 64 * 64; o += NT) {
+            const int r = o >> 6, i = o & 63;
+            float s = 0.f;
+            if (i < r && r < n) s += bet[r] * __expf(gam[r] - gam[i]) * Fa[r * 65 + i];
+            if (r < i && i < n) s += bet[i] * __expf(gam[i] - gam[r]) * Fa[i * 65 + r];
+            tile_st_hl(sm, S_P, S_P + 8192, r, i, s);
+        }
+        tc_fence_before();  // every K K^T load is done before the columns are overwritten
+        __syncthreads();
+        tc_fence_after();
+        // h and dSe (lane = key) -> TMEM as A operands of the dq / dk products
+        {
+            const float *hr = a.hbuf + st_off + (size_t)lrow * DV + 64 * hh;
+            const float *dr = a.dSe + st_off + (size_t)lrow * DV + 64 * hh;
+            float x[64];
+            uint32_t hi[32], lo[32];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const float4 w = reinterpret_cast<const float4 *>(hr)[i];
+                x[4 * i] = w.x; x[4 * i + 1] = w.y; x[4 * i + 2] = w.z; x[4 * i + 3] = w.w;
+            }
+            split_pack32(x, hi, lo);
+            tmem_st32(tmem + trow + C_HT + 32 * hh, hi);
+            tmem_st32(tmem + trow + C_HT + 64 + 32 * hh, lo);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const float4 w = reinterpret_cast<const float4 *>(dr)[i];
+                x[4 * i] = w.x; x[4 * i + 1] = w.y; x[4 * i + 2] = w.z; x[4 * i + 3] = w.w;
+            }
+            split_pack32(x, hi, lo);
+            tmem_st32(tmem + trow + C_KS + 32 * hh, hi);
+            tmem_st32(tmem + trow + C_KS + 64 + 32 * hh, lo);
+            tmem_wait_st();
+        }
+        __syncthreads();
+        // per-row results of this head: dbeta and dg (reverse cumsum of dgam inside the chunk)
+        if (t == 0) {
+            float hd = 0.f, sf = 0.f;
+            for (int w = 0; w < 8; ++w) {
+                hd += sH[w];
+                sf += sF[w];
+            }
+            float acc = 0.f;
+            for (int r = n - 1; r >= 0; --r) {
+                float dgr = 0.f, dbr = 0.f;
+                for (int w = 0; w < 8; ++w) {
+                    dgr += rdg_all[64 * w + r];
+                    dbr += rdb_all[64 * w + r];
+                }
+                if (r == n - 1) dgr += Gm[n - 1] * hd + sf;
+                acc += dgr;
+                const size_t gi = (size_t)(tok0 + r) * p.Hv + hv;
+                a.dg[gi] = acc;
+                a.dbeta[gi] = dbr;
+            }
+        }
+        // ---------------------------------------------------------------- P6: dq^T, dk^T accumulation
+        pre_mma();
+        if (t == 0) {
+            const uint32_t acc0 = (g != 0);
+            for (int tt = 0; tt < 3; ++tt)  // dq^T += h (scale Gam dO)^T
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_bf16_ta(tmem + C_DQ, tmem + C_HT + (tt == 2 ? 64 : 0) + 8 * kk,
+                                kdesc(sb + S_DD + (tt == 1 ? 16384 : 0) + (kk >> 2) * 8192 + (kk & 3) * 32), ID_KK,
+                                acc0 | (uint32_t)(tt | kk));
+            for (int sp = 0; sp < 2; ++sp)  // dq^T += K^T dQK^T
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_bf16(tmem + C_DQ, mdesc(sb + S_KQ + kk * 2048, 16384),
+                             kdesc(sb + S_DO + 8192 * sp + kk * 32), ID_MK, 1);
+            for (int tt = 0; tt < 3; ++tt)  // dk^T += dSe (E Dl)^T
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_bf16_ta(tmem + C_DK, tmem + C_KS + (tt == 2 ? 64 : 0) + 8 * kk,
+                                mdesc(sb + S_DR + (tt == 1 ? 32768 : 0) + kk * 2048, 8192), ID_KM,
+                                acc0 | (uint32_t)(tt | kk));
+            for (int tt = 0; tt < 3; ++tt)  // dk^T += h Y^T, Y = -beta Gam dR
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_bf16_ta(tmem + C_DK, tmem + C_HT + (tt == 2 ? 64 : 0) + 8 * kk,
+                                mdesc(sb + S_DR + 16384 + (tt == 1 ? 32768 : 0) + kk * 2048, 8192), ID_KM, 1);
+            for (int sp = 0; sp < 2; ++sp)  // dk^T += Q^T dQK
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_bf16(tmem + C_DK, mdesc(sb + S_KQ + 8192 + kk * 2048, 16384),
+                             mdesc(sb + S_DO + 8192 * sp + kk * 2048, 8192), ID_MM, 1);
+            for (int sp = 0; sp < 2; ++sp)  // dk^T += K^T (dKK + dKK^T)
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_bf16(tmem + C_DK, mdesc(sb + S_KQ + kk * 2048, 16384),
+                             mdesc(sb + S_P + 8192 * sp + kk * 2048, 8192), ID_MM, 1);
+        }
+        mma_sync();
+    }
+    // ---------------------------------------------------------------- dq, dk out (thread: key lrow, rows 32 hh + j)
+    if (ok) {
+        uint32_t d[32];
+        uint16_t *dqp = reinterpret_cast<uint16_t *>(a.dq) + (size_t)hq * DK + lrow;
+        uint16_t *dkp = reinterpret_cast<uint16_t *>(a.dk) + (size_t)hq * DK + lrow;
+        const size_t rs = (size_t)p.Hq * DK;
+        tmem_ld32(tmem + trow + C_DQ + 32 * hh, d);
+        tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            const int r = 32 * hh + j;
+            if (r < n) {
+                __nv_bfloat16 b = __float2bfloat16_rn(__uint_as_float(d[j]));
+                dqp[(size_t)(tok0 + r) * rs] = *reinterpret_cast<uint16_t *>(&b);
+            }
+        }
+        tmem_ld32(tmem + trow + C_DK + 32 * hh, d);
+        tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            const int r = 32 * hh + j;
+            if (r < n) {
+                __nv_bfloat16 b = __float2bfloat16_rn(__uint_as_float(d[j]));
+                dkp[(size_t)(tok0 + r) * rs] = *reinterpret_cast<uint16_t *>(&b);
+            }
+        }
+    } else if (t == 0) {
+        if (atomicCAS(p.err + 1, 0u, 201u) == 0u) {
+            p.err[2] = (uint32_t)gc;
+            p.err[4] = blockIdx.x + blockIdx.y * gridDim.x;
+        }
+        atomicOr(p.err, ERR_TIMEOUT);
+        // leave nothing in flight: a pending TMA load and every issued MMA
+        if (tma_issued > tma_ph) mbar_drain(bar_tma, (tma_issued - 1) & 1);
+        mma_commit(bar_mma);
+        mbar_drain(bar_mma, mma_ph & 1);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0) tmem_dealloc(tmem, 512);
+}
+
+}  // namespace
+
+cudaError_t launch_tc_bwd_intra(const Plan &p, const void *q, const void *k, const void *v, const void *d_o,
+                                const float *g_cum, const float *beta, const float *A32, const float *P32,
+                                const float *hbuf, const float *dSe, void *dq, void *dk, void *dv, float *dbeta,
+                                float *dg, cudaStream_t st) {
+    CUtensorMap tk, tq, tdo;
+    if (!make_head_map(&tk, k, p.Hq, p) || !make_head_map(&tq, q, p.Hq, p) || !make_head_map(&tdo, d_o, p.Hv, p))
+        return cudaErrorInvalidValue;
+    cudaError_t e =
+        cudaFuncSetAttribute(k_tc_bwd_intra, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    IntraArgs a;
+    a.v = static_cast<const __nv_bfloat16 *>(v);
+    a.d_o = static_cast<const __nv_bfloat16 *>(d_o);
+    a.g_cum = g_cum;
+    a.beta = beta;
+    a.A32 = A32;
+    a.P32 = P32;
+    a.hbuf = hbuf;
+    a.dSe = dSe;
+    a.dq = static_cast<__nv_bfloat16 *>(dq);
+    a.dk = static_cast<__nv_bfloat16 *>(dk);
+    a.dv = static_cast<__nv_bfloat16 *>(dv);
+    a.dbeta = dbeta;
+    a.dg = dg;
+    dim3 grid(p.total_chunks, p.Hq);
+    k_tc_bwd_intra<<<grid, NT, SMEM_BYTES, st>>>(tk, tq, tdo, p, a);
+    return cudaGetLastError();
+}
+
+}  // namespace gdn
