@@ -34,8 +34,6 @@ WORKLOAD = "train_b2_t8192_h64"
 METRIC = "GDN chunked-prefill fwd/bwd tokens/s on 1 GB300; % of tensor/HBM roofline"
 L2_FLUSH_BYTES = 512 << 20
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-FFMA_LANES_PER_SM = 128
-N_SMS = 152
 
 
 def load_peaks():
@@ -74,23 +72,36 @@ def algorithmic(w, C=64):
 
 
 def kernel_work(name, w, C=64):
-    """(bound, algorithmic flops, algorithmic bytes) of one launch of a kernel
-    over workload ``w``: the share of the pass's algorithmic work that kernel
-    performs (see the design notes' kernel table)."""
+    """(algorithmic flops, algorithmic bytes) of one launch of a kernel over
+    workload ``w``: the share of its pass's algorithmic work that the kernel
+    performs (per token and value head; d = K = V, e = io bytes, G = Hv / Hq):
+
+      fwd_tc        the whole forward                       (see ``algorithmic``)
+      bwd_state_tc  recompute K K^T, W, U, W S, state update 2C(2K + V) + 4KV flops;
+                    reads k, v, g_cum, beta                 Ke/G + Ve + 8 bytes
+      bwd_dscan_tc  K dS, P^T dO, A^T dDl, state update      6KV + 4CV flops;
+                    reads q, k, do, g_cum, beta             2Ke/G + Ve + 8 bytes
+      bwd_intra_tc  the rest of the backward's flops;       bwd - state - dscan;
+                    reads q, k, v, do, g_cum, beta; writes dq, dk, dv, dbeta, dg
+                                                            4Ke/G + 3Ve + 16 bytes
+    CUDA-core kernels (fp32 io or other head sizes) use the same shares.
+    """
     K, V, G = w.K, w.V, w.Hv // w.Hq
     e = 2 if w.io_dtype == torch.bfloat16 else 4
     th = w.tokens * w.Hv
-    d = K
+    alg = algorithmic(w, C)
+    st_f = th * (2 * C * (2 * K + V) + 4 * K * V)
+    ds_f = th * (6 * K * V + 4 * C * V)
     table = {
-        # CUDA-core kernels
-        "fwd_prep": ("alu", th * 2 * 2 * C * K, th * (2 * K * e / G + 12 + C * e)),
-        "fwd_scan": ("alu", th * (2 * C * (K + 2 * V) + 6 * K * V), th * (2 * K * e / G + 2 * V * e + 8)),
-        "bwd_prep": ("alu", th * 2 * 2 * C * K, th * (2 * K * e / G + 8)),
-        "bwd_state": ("alu", th * (2 * 2 * C * d + 2 * 2 * d * d), th * (K * e / G + V * e + 8)),
-        "bwd_dscan": ("alu", th * (3 * 2 * d * d + 2 * C * d), th * (2 * K * e / G + V * e + 8)),
-        "bwd_intra": ("alu", th * (4 * d * d + 26 * C * d + 4 * C * C),
-                      th * (4 * K * e / G + 3 * V * e + 16)),
+        "fwd_tc": (alg["fwd_flops"], alg["fwd_bytes"]),
+        "bwd_state_tc": (st_f, th * (K * e / G + V * e + 8)),
+        "bwd_dscan_tc": (ds_f, th * (2 * K * e / G + V * e + 8)),
+        "bwd_intra_tc": (alg["bwd_flops"] - st_f - ds_f, th * (4 * K * e / G + 3 * V * e + 16)),
     }
+    table["fwd_scan"] = table["fwd_tc"]
+    table["bwd_state"] = table["bwd_state_tc"]
+    table["bwd_dscan"] = table["bwd_dscan_tc"]
+    table["bwd_intra"] = table["bwd_intra_tc"]
     return table.get(name)
 
 
@@ -247,26 +258,23 @@ def run_ours(args, rank, world, local_rank):
         kw = kernel_work(name, w)
         avg_s = tot / cnt / 1e3
         if kw:
-            bound, fl, by = kw
-            if bound == "alu":
-                mhz = peaks.get("sm_max_mhz", 2070.0)
-                peak = N_SMS * FFMA_LANES_PER_SM * 2 * mhz * 1e6 / 1e12
-                ach = fl / avg_s / 1e12
-                roof = {"bound": "alu", "kernel": name, "achieved": round(ach, 3), "peak": round(peak, 1),
-                        "unit": "TFLOP/s", "frac": round(ach / peak, 4), "traffic": None,
-                        "peak_source": f"FP32 FFMA: {N_SMS} SMs x {FFMA_LANES_PER_SM} lanes x 2 x {mhz:.0f} MHz"}
-            elif bound == "hbm":
+            fl, by = kw
+            t_tc = fl / (peaks["bf16_tflops"] * 1e12)
+            t_hbm = by / (peaks["hbm_gbs"] * 1e9)
+            if t_hbm >= t_tc:
                 peak = peaks["hbm_gbs"]
                 ach = by / avg_s / 1e9
                 roof = {"bound": "hbm", "kernel": name, "achieved": round(ach, 1), "peak": peak, "unit": "GB/s",
-                        "frac": round(ach / peak, 4), "traffic": None, "peak_source": f"hbm_gbs ({peak_src})"}
+                        "frac": round(ach / peak, 4), "peak_source": f"hbm_gbs, {peak_src} (burst copy)"}
             else:
                 peak = peaks["bf16_tflops"]
                 ach = fl / avg_s / 1e12
                 roof = {"bound": "tensor", "kernel": name, "achieved": round(ach, 2), "peak": peak,
-                        "unit": "TFLOP/s", "frac": round(ach / peak, 4), "traffic": None,
-                        "peak_source": f"bf16_tflops burst ({peak_src})"}
+                        "unit": "TFLOP/s", "frac": round(ach / peak, 4),
+                        "peak_source": f"bf16_tflops, {peak_src} (burst cuBLAS)"}
             roof["avg_launch_us"] = round(avg_s * 1e6, 2)
+            roof["algorithmic_flops"] = fl
+            roof["algorithmic_bytes"] = by
             roof["traffic"] = TRAFFIC.get(name)
     # whole-pass roofline (both passes, measured peaks)
     bw = peaks["hbm_gbs"] * 1e9

@@ -191,14 +191,14 @@ gdn_status gdn_bwd(const gdn_problem *p, const void *q, const void *k, const voi
     double *gam64 = at<double>(workspace, w.gam64);
     float *A32 = at<float>(workspace, w.A32), *P32 = at<float>(workspace, w.P32);
     float *hbuf = at<float>(workspace, w.hbuf), *dSe = at<float>(workspace, w.dSe);
-    if (pl.total_chunks > 0) {
+    if (pl.total_chunks > 0 && tc_fwd_supported(pl)) {
+        // tensor-core path: one forward recompute pass writes the chunk-entry states and A, P (fp32)
+        GDN_LAUNCH("bwd_state_tc", launch_tc_fwd(pl, q, k, v, g_cum, beta, h0, nullptr, nullptr, nullptr, hbuf,
+                                                 nullptr, st, true, A32, P32));
+    } else if (pl.total_chunks > 0) {
         GDN_LAUNCH("bwd_prep", launch_simt_prep(pl, q, k, g_cum, 1, beta, nullptr, nullptr, gam64, A32, P32, st));
-        if (tc_fwd_supported(pl))
-            GDN_LAUNCH("bwd_state_tc", launch_tc_fwd(pl, q, k, v, g_cum, beta, h0, nullptr, nullptr, nullptr, hbuf,
-                                                     nullptr, st, true));
-        else
-            GDN_LAUNCH("bwd_state", launch_simt_scan(pl, q, k, v, beta, gam64, A32, P32, h0, nullptr, hbuf, nullptr,
-                                                     st));
+        GDN_LAUNCH("bwd_state", launch_simt_scan(pl, q, k, v, beta, gam64, A32, P32, h0, nullptr, hbuf, nullptr,
+                                                 st));
     }
     if (tc_fwd_supported(pl))
         GDN_LAUNCH("bwd_dscan_tc", launch_tc_dscan(pl, q, k, d_o, g_cum, beta, A32, P32, dht, dSe, dh0, st));

@@ -29,7 +29,8 @@ cudaError_t launch_simt_bwd_intra(const Plan &p, const void *q, const void *k, c
 bool tc_fwd_supported(const Plan &p);
 cudaError_t launch_tc_fwd(const Plan &p, const void *q, const void *k, const void *v, const float *g,
                           const float *beta, const float *h0, void *o, float *g_cum, void *A, float *h,
-                          float *ht, cudaStream_t st, bool g_is_cum = false);
+                          float *ht, cudaStream_t st, bool g_is_cum = false, float *A32 = nullptr,
+                          float *P32 = nullptr);
 
 // TMA map of a [tokens][heads][128] bf16 tensor (64 x 1 x 64 boxes, 128-byte swizzle)
 bool make_head_map(CUtensorMap *m, const void *ptr, int heads, const Plan &p);

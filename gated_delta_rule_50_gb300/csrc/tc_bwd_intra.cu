@@ -447,19 +447,57 @@ k_tc_bwd_intra(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         }
         __syncthreads();  // the staged dQK in Fb is consumed before Fb is reused
         // ---------------------------------------------------------------- P5: dL = -(A^T dA A^T), strictly lower
-        for (int o = t; o < 64 * 64; o += NT) {  // Fb = A^T dA
-            const int r = o >> 6, i = o & 63;
-            float s = 0.f;
-            for (int k = max(r, i); k < C; ++k) s = fmaf(tile_hl(sm, S_A, S_A + 8192, k, r), Fa[k * 65 + i], s);
-            Fb[r * 65 + i] = s;
+        // on the tensor cores: Z^T = A dA~^T (dA~ = lower part of dA), then dL^T = -Z^T A.  Both are
+        // M = 128 products whose rows 64..127 read neighbouring tiles and are ignored.
+        for (int o = t; o < 64 * 8; o += NT) {  // dA~ hi / lo tile [k][l] in the P region (P is consumed)
+            const int r = o >> 3, ch = o & 7;
+            float x8[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const int i = 8 * ch + e;
+                x8[e] = i <= r ? Fa[r * 65 + i] : 0.f;
+            }
+            st_split_chunk(sb + S_P, sb + S_P + 8192, r, ch, x8);
         }
-        __syncthreads();
-        for (int o = t; o < 64 * 64; o += NT) {  // Fa = dL
-            const int r = o >> 6, i = o & 63;
-            float s = 0.f;
-            if (i < r)
-                for (int l = 0; l <= i; ++l) s = fmaf(Fb[r * 65 + l], tile_hl(sm, S_A, S_A + 8192, i, l), s);
-            Fa[r * 65 + i] = -s;
+        pre_mma();
+        if (t == 0)
+            for (int tt = 0; tt < 3; ++tt)  // Z^T[i][k] = sum_l A[i][l] dA~[k][l]
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_bf16(tmem + C_KS, kdesc(sb + S_A + (tt == 2 ? 8192 : 0) + kk * 32),
+                             kdesc(sb + S_P + (tt == 1 ? 8192 : 0) + kk * 32), ID_KK, (tt | kk) != 0);
+        mma_sync();
+        if (!ok) break;
+        if (lq < 2) {  // Z^T rows (lanes 0..63) -> hi / lo bf16 A operand in TMEM
+            uint32_t z[32], hi[16], lo[16];
+            tmem_ld32(tmem + trow + C_KS + 32 * hh, z);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                float h0, l0, h1, l1;
+                split2(__uint_as_float(z[2 * i]), h0, l0);
+                split2(__uint_as_float(z[2 * i + 1]), h1, l1);
+                hi[i] = pack_bf16(h0, h1);
+                lo[i] = pack_bf16(l0, l1);
+            }
+            tmem_st16(tmem + trow + C_QS + 16 * hh, hi);
+            tmem_st16(tmem + trow + C_QS + 32 + 16 * hh, lo);
+            tmem_wait_st();
+        }
+        pre_mma();
+        if (t == 0)
+            for (int tt = 0; tt < 3; ++tt)  // (A^T Z)^T[i][r] = sum_k Z^T[i][k] A[k][r]   (A read MN-major)
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_bf16_ta(tmem + C_KS, tmem + C_QS + (tt == 2 ? 32 : 0) + 8 * kk,
+                                mdesc(sb + S_A + (tt == 1 ? 8192 : 0) + kk * 2048, 8192), ID_KM, (tt | kk) != 0);
+        mma_sync();
+        if (!ok) break;
+        if (lq < 2) {  // Fa[r][i] = dL[r][i] = -(A^T Z)[r][i]
+            uint32_t z[32];
+            tmem_ld32(tmem + trow + C_KS + 32 * hh, z);
+            tmem_wait_ld();
+            const int i = lrow;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) Fa[(32 * hh + j) * 65 + i] = -__uint_as_float(z[j]);
         }
         __syncthreads();
         // K K^T for the beta and gate terms of dL (lanes 0..63 of a [K; Q] K^T product)

@@ -77,6 +77,7 @@ struct FwdArgs {
     __nv_bfloat16 *o, *A;
     float *g_cum, *h, *ht;
     int g_is_cum;  // g already holds the chunk-local cumsum (backward recompute)
+    float *A32, *P32;  // optional fp32 copies of A and P per chunk ([chunk][Hv][64][64])
 };
 
 // Records the first expired wait: err[1] = barrier + 1, err[2] = chunk,
@@ -370,6 +371,24 @@ k_tc_fwd(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
             }
             named_bar(1, 128);
             blocked_inverse(Lm, Tb, pt);
+            if (a.A32) {  // fp32 A and P for the backward's gradient kernels
+                const size_t mat = ((size_t)(sr.c0 + j) * p.Hv + hv) * C * C;
+                const int r = pt >> 1, hh = pt & 1;
+                float4 *dst = reinterpret_cast<float4 *>(a.A32 + mat + (size_t)r * C + 32 * hh);
+#pragma unroll
+                for (int q4 = 0; q4 < 8; ++q4)
+                    dst[q4] = make_float4(Lm[r * 65 + 32 * hh + 4 * q4], Lm[r * 65 + 32 * hh + 4 * q4 + 1],
+                                          Lm[r * 65 + 32 * hh + 4 * q4 + 2], Lm[r * 65 + 32 * hh + 4 * q4 + 3]);
+                if (row >= 64) {
+                    float4 *pd = reinterpret_cast<float4 *>(a.P32 + mat + (size_t)(row - 64) * C);
+#pragma unroll
+                    for (int q4 = 0; q4 < 16; ++q4) {
+                        const uint32_t *src = q4 < 8 ? raw0 + 4 * q4 : raw1 + 4 * (q4 - 8);
+                        pd[q4] = make_float4(__uint_as_float(src[0]), __uint_as_float(src[1]),
+                                             __uint_as_float(src[2]), __uint_as_float(src[3]));
+                    }
+                }
+            }
             // A -> hi/lo operand tile and the io-dtype output, once Dl of the previous chunk is done
             if (j >= 1 && !gwait(B_DLDONE, (j - 1) & 1, j)) break;
             {
@@ -582,7 +601,7 @@ bool tc_fwd_supported(const Plan &p) { return p.io == GDN_BF16 && p.K == DK && p
 
 cudaError_t launch_tc_fwd(const Plan &p, const void *q, const void *k, const void *v, const float *g,
                           const float *beta, const float *h0, void *o, float *g_cum, void *A, float *h,
-                          float *ht, cudaStream_t st, bool g_is_cum) {
+                          float *ht, cudaStream_t st, bool g_is_cum, float *A32, float *P32) {
     CUtensorMap tk, tq;
     if (!make_head_map(&tk, k, p.Hq, p) || !make_head_map(&tq, q, p.Hq, p)) return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(k_tc_fwd, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
@@ -598,6 +617,8 @@ cudaError_t launch_tc_fwd(const Plan &p, const void *q, const void *k, const voi
     a.h = h;
     a.ht = ht;
     a.g_is_cum = g_is_cum ? 1 : 0;
+    a.A32 = A32;
+    a.P32 = P32;
     dim3 grid(p.n_seqs, p.Hv);
     k_tc_fwd<<<grid, NUM_THREADS, SMEM_BYTES, st>>>(tk, tq, p, a);
     return cudaGetLastError();
