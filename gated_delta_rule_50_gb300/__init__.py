@@ -81,6 +81,11 @@ def load_library():
             lib.gdn_status_str.argtypes = [ctypes.c_int]
             lib.gdn_status_str.restype = ctypes.c_char_p
             lib.gdn_version.restype = ctypes.c_char_p
+            lib.gdn_cp_trigger.argtypes = [ctypes.c_int64] * 3
+            lib.gdn_cp_trigger.restype = ctypes.c_int
+            IP = ctypes.POINTER(ctypes.c_int)
+            lib.gdn_cp_plan.argtypes = [pp, IP, IP]
+            lib.gdn_cp_plan.restype = ctypes.c_int
             _lib = lib
         return _lib
 
@@ -141,6 +146,23 @@ def workspace_bytes(kind: str, q, v, cu_seqlens=None, cu_seqlens_cpu=None, cp_mo
     pr = _problem(q, v, None, cu, host, cp_mode, warmup_chunks)
     fn = lib.gdn_fwd_workspace_bytes if kind == "fwd" else lib.gdn_bwd_workspace_bytes
     return int(fn(ctypes.byref(pr)))
+
+
+def cp_trigger(n_seqs: int, n_heads: int, seq_len: int) -> bool:
+    """Whether the FlashQLA pages' rule turns sequence splitting on."""
+    return bool(load_library().gdn_cp_trigger(n_seqs, n_heads, seq_len))
+
+
+def cp_plan(q, v, cu_seqlens=None, cu_seqlens_cpu=None, cp_mode="warmup", warmup_chunks=8):
+    """(seg_len, n_seg) in chunks if the forward would split this problem, else None."""
+    lib = load_library()
+    cu, host = _cu(cu_seqlens, cu_seqlens_cpu)
+    pr = _problem(q, v, None, cu, host, cp_mode, warmup_chunks)
+    L, n = ctypes.c_int(), ctypes.c_int()
+    r = lib.gdn_cp_plan(ctypes.byref(pr), ctypes.byref(L), ctypes.byref(n))
+    if r < 0:
+        raise ValueError("gdn_cp_plan: bad problem")
+    return (L.value, n.value) if r else None
 
 
 def _workspace(nbytes: int, device) -> torch.Tensor:

@@ -36,18 +36,22 @@ gdn_status make_plan(const gdn_problem *pr, Plan *pl) {
     pl->K = (int)pr->K; pl->V = (int)pr->V; pl->G = (int)(pr->Hv / pr->Hq);
     pl->io = pr->io_dtype;
     pl->scale = pr->scale;
+    pl->cp_mode = pr->cp_mode;
+    pl->warmup_chunks = pr->warmup_chunks;
     if (pr->cu_seqlens) {
         if (pr->B != 1 || pr->n_seqs < 1 || !pr->cu_seqlens_host) return GDN_ERR_INVALID_ARG;
         if (pr->n_seqs > INT32_MAX / 4) return GDN_ERR_UNSUPPORTED;
         const int32_t *cu = pr->cu_seqlens_host;
         if (cu[0] != 0 || cu[pr->n_seqs] != pr->T) return GDN_ERR_INVALID_ARG;
-        int64_t chunks = 0, mx = 0;
+        int64_t chunks = 0, mx = 0, mxl = 0;
         for (int64_t s = 0; s < pr->n_seqs; ++s) {
             if (cu[s + 1] < cu[s]) return GDN_ERR_INVALID_ARG;
             int64_t c = (cu[s + 1] - cu[s] + C - 1) / C;
             chunks += c;
             mx = c > mx ? c : mx;
+            mxl = cu[s + 1] - cu[s] > mxl ? cu[s + 1] - cu[s] : mxl;
         }
+        pl->max_seq_len = (int)mxl;
         pl->n_seqs = (int)pr->n_seqs;
         pl->cu = pr->cu_seqlens;
         pl->total_chunks = (int)chunks;
@@ -60,16 +64,26 @@ gdn_status make_plan(const gdn_problem *pr, Plan *pl) {
         pl->NC = (int)((pr->T + C - 1) / C);
         pl->total_chunks = pl->NC * pl->B;
         pl->max_seq_chunks = pl->NC;
+        pl->max_seq_len = pl->T;
     }
     return GDN_OK;
 }
 
 struct FwdWs {
-    size_t err, chunk_off, gam64, A32, P32, total;
+    size_t err, chunk_off, gam64, A32, P32, serial, seg_states, total;
+    int seg_len, n_seg;  // n_seg > 1: sequence splitting with warmup is planned
 };
 struct BwdWs {
     size_t err, chunk_off, gam64, A32, P32, hbuf, dSe, total;
 };
+
+// Sequence splitting with warmup runs when asked for, supported and triggered.
+bool warmup_split(const Plan &p) {
+    if (p.cp_mode != GDN_CP_WARMUP || !tc_fwd_supported(p) || !cp_trigger(p)) return false;
+    int L, n;
+    cp_geometry(p, &L, &n);
+    return n > 1;
+}
 
 FwdWs fwd_layout(const Plan &p) {
     Carve c;
@@ -81,6 +95,14 @@ FwdWs fwd_layout(const Plan &p) {
     w.gam64 = c.take<double>(tokens * p.Hv);
     w.A32 = c.take<float>(mats);
     w.P32 = c.take<float>(mats);
+    w.seg_len = 0;
+    w.n_seg = 1;
+    w.serial = w.seg_states = 0;
+    if (warmup_split(p)) {
+        cp_geometry(p, &w.seg_len, &w.n_seg);
+        w.serial = c.take<uint8_t>((size_t)p.n_seqs * p.Hv);
+        w.seg_states = c.take<float>((size_t)p.n_seqs * p.Hv * w.n_seg * p.K * p.V);
+    }
     w.total = c.off;
     return w;
 }
@@ -156,7 +178,24 @@ gdn_status gdn_fwd(const gdn_problem *p, const void *q, const void *k, const voi
     GDN_LAUNCH("chunk_table", launch_chunk_table(pl, st));
     double *gam64 = at<double>(workspace, w.gam64);
     float *A32 = at<float>(workspace, w.A32), *P32 = at<float>(workspace, w.P32);
-    if (tc_fwd_supported(pl) && p->cp_mode != GDN_CP_WARMUP) {
+    if (w.n_seg > 1) {  // sequence splitting with warmup
+        CpSplit cs;
+        cs.seg_len = w.seg_len;
+        cs.n_seg = w.n_seg;
+        cs.warm = pl.warmup_chunks;
+        cs.serial = at<uint8_t>(workspace, w.serial);
+        cs.seg_states = at<float>(workspace, w.seg_states);
+        GDN_LAUNCH("cp_flags", launch_cp_flags(pl, g, cs.seg_len, cs.n_seg, cs.warm,
+                                               at<uint8_t>(workspace, w.serial), st));
+        cs.mode = CP_WARM;
+        GDN_LAUNCH("fwd_tc_warm", launch_tc_fwd(pl, q, k, v, g, beta, nullptr, nullptr, nullptr, nullptr, nullptr,
+                                                nullptr, st, false, nullptr, nullptr, &cs));
+        cs.mode = CP_MAIN;
+        GDN_LAUNCH("fwd_tc", launch_tc_fwd(pl, q, k, v, g, beta, h0, o, g_cum, A, h, final_state, st, false, nullptr,
+                                           nullptr, &cs));
+        return GDN_OK;
+    }
+    if (tc_fwd_supported(pl)) {
         GDN_LAUNCH("fwd_tc", launch_tc_fwd(pl, q, k, v, g, beta, h0, o, g_cum, A, h, final_state, st));
         return GDN_OK;
     }
@@ -211,6 +250,26 @@ gdn_status gdn_bwd(const gdn_problem *p, const void *q, const void *k, const voi
         GDN_LAUNCH("bwd_intra", launch_simt_bwd_intra(pl, q, k, v, d_o, beta, gam64, A32, P32, hbuf, dSe, dq, dk,
                                                      dv, dbeta, dg, st));
     return GDN_OK;
+}
+
+int gdn_cp_plan(const gdn_problem *p, int *seg_len, int *n_seg) {
+    Plan pl;
+    if (make_plan(p, &pl) != GDN_OK) return -1;
+    int L = 0, n = 1;
+    const int on = warmup_split(pl) ? 1 : 0;
+    if (on) cp_geometry(pl, &L, &n);
+    if (seg_len) *seg_len = on ? L : 0;
+    if (n_seg) *n_seg = on ? n : 1;
+    return on;
+}
+
+int gdn_cp_trigger(int64_t n_seqs, int64_t n_heads, int64_t seq_len) {
+    Plan pl;
+    std::memset(&pl, 0, sizeof(pl));
+    pl.n_seqs = (int)n_seqs;
+    pl.Hv = (int)n_heads;
+    pl.max_seq_len = (int)seq_len;
+    return cp_trigger(pl) ? 1 : 0;
 }
 
 gdn_status gdn_workspace_error(const void *workspace, gdn_stream_t stream) {

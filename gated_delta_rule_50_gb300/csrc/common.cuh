@@ -26,6 +26,8 @@ struct Plan {
     int NC;             // chunks per sequence (batch mode)
     int total_chunks;   // chunks over all sequences
     int max_seq_chunks; // chunks of the longest sequence
+    int max_seq_len;    // tokens of the longest sequence
+    int cp_mode, warmup_chunks;
     const int32_t *cu;  // device cu_seqlens (varlen) or nullptr
     int32_t *chunk_off; // device [n_seqs + 1] chunk offsets (varlen) or nullptr
     gdn_dtype io;

@@ -25,12 +25,26 @@ cudaError_t launch_simt_bwd_intra(const Plan &p, const void *q, const void *k, c
                                   const float *P32, const float *hbuf, const float *dSe, void *dq, void *dk,
                                   void *dv, float *dbeta, float *dg, cudaStream_t st);
 
+// Sequence splitting with warmup: each sequence is cut into n_seg segments of
+// seg_len chunks; a CP_WARM launch computes every segment's starting state by
+// running `warm` chunks from a zero state, a CP_MAIN launch runs the segments.
+enum { CP_WARM = 1, CP_MAIN = 2 };
+struct CpSplit {
+    int seg_len, n_seg, warm, mode;
+    const uint8_t *serial;  // [n_seqs][Hv] heads whose warmup windows do not decay enough
+    float *seg_states;      // [n_seqs][Hv][n_seg][K][V]
+};
+bool cp_trigger(const Plan &p);                  // the pages' small batch x heads rule
+void cp_geometry(const Plan &p, int *seg_len, int *n_seg);
+cudaError_t launch_cp_flags(const Plan &p, const float *g, int seg_len, int n_seg, int warm, uint8_t *serial,
+                            cudaStream_t st);
+
 // tensor-core (tcgen05) fused forward: bf16 io, K = V = 128
 bool tc_fwd_supported(const Plan &p);
 cudaError_t launch_tc_fwd(const Plan &p, const void *q, const void *k, const void *v, const float *g,
                           const float *beta, const float *h0, void *o, float *g_cum, void *A, float *h,
                           float *ht, cudaStream_t st, bool g_is_cum = false, float *A32 = nullptr,
-                          float *P32 = nullptr);
+                          float *P32 = nullptr, const CpSplit *cp = nullptr);
 
 // TMA map of a [tokens][heads][128] bf16 tensor (64 x 1 x 64 boxes, 128-byte swizzle)
 bool make_head_map(CUtensorMap *m, const void *ptr, int heads, const Plan &p);

@@ -78,6 +78,10 @@ struct FwdArgs {
     float *g_cum, *h, *ht;
     int g_is_cum;  // g already holds the chunk-local cumsum (backward recompute)
     float *A32, *P32;  // optional fp32 copies of A and P per chunk ([chunk][Hv][64][64])
+    // sequence splitting with warmup (see cp.cu): seg_len > 0 enables it
+    int seg_len, n_seg, warm, mode;  // mode: CP_WARM or CP_MAIN
+    const uint8_t *serial;           // [n_seqs][Hv]: 1 = this head runs unsplit
+    float *seg_states;               // [n_seqs][Hv][n_seg][K][V] warmup states
 };
 
 // Records the first expired wait: err[1] = barrier + 1, err[2] = chunk,
@@ -158,9 +162,46 @@ k_tc_fwd(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
     float *vec = reinterpret_cast<float *>(sm + SM_VEC);
     auto bar = [&](int i) { return sb + SM_BAR + 8u * (uint32_t)i; };
 
-    const int s = blockIdx.x, hv = blockIdx.y, hq = hv / p.G;
-    const SeqRange sr = seq_range(p, s);
-    const int nck = sr.c1 - sr.c0;
+    const int hv = blockIdx.y, hq = hv / p.G;
+    const int s = a.seg_len > 0 ? (int)blockIdx.x / a.n_seg : (int)blockIdx.x;
+    const int pseg = a.seg_len > 0 ? (int)blockIdx.x % a.n_seg : 0;
+    SeqRange sr = seq_range(p, s);
+    // chunk range of this CTA, its initial / final state and whether it writes the outputs
+    const int nseq_ck = sr.c1 - sr.c0;
+    int jb = 0, je = nseq_ck;
+    const size_t st_base = ((size_t)s * p.Hv + hv) * DK * DV;
+    const float *init = a.h0 ? a.h0 + st_base : nullptr;
+    float *fin = a.ht ? a.ht + st_base : nullptr;
+    bool outs = true;
+    if (a.seg_len > 0) {
+        const bool serial = a.serial[(size_t)s * p.Hv + hv] != 0;
+        const int L = a.seg_len;
+        float *segst = a.seg_states + (((size_t)s * p.Hv + hv) * a.n_seg + pseg) * DK * DV;
+        if (a.mode == CP_WARM) {  // state after the warmup window that precedes segment pseg, from zero
+            outs = false;
+            init = nullptr;
+            fin = segst;
+            if (serial || pseg == 0 || pseg * L >= nseq_ck) jb = je = 0;
+            else { jb = max(0, pseg * L - a.warm); je = pseg * L; }
+        } else {  // CP_MAIN
+            if (serial) {
+                if (pseg != 0) jb = je = 0;
+            } else {
+                jb = min(pseg * L, nseq_ck);
+                je = min(nseq_ck, (pseg + 1) * L);
+                if (pseg > 0) init = segst;
+                if (je < nseq_ck) fin = nullptr;
+            }
+        }
+        if (jb >= je) { jb = je = 0; fin = nullptr; }
+    }
+    sr.tok0 += jb * C;
+    sr.c0 += jb;
+    sr.c1 = sr.c0 + (je - jb);
+    const int nck = je - jb;
+    __nv_bfloat16 *o_out = outs ? a.o : nullptr, *A_out = outs ? a.A : nullptr;
+    float *gcum_out = outs ? a.g_cum : nullptr, *h_out = outs ? a.h : nullptr;
+    float *A32_out = outs ? a.A32 : nullptr, *P32_out = outs ? a.P32 : nullptr;
 
     if (threadIdx.x == 0) {
         const uint32_t counts[B_COUNT] = {1, 1, 1, 1, 1, 128, 256, 1, 256, 128, 1, 256, 128, 1, 1, 256, 256, 1};
@@ -333,7 +374,7 @@ k_tc_fwd(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
             if (row < 64) {
                 gam[row] = x;
                 bet[row] = bv;
-                if (row < n && a.g_cum) a.g_cum[(size_t)(tok0 + row) * p.Hv + hv] = x;
+                if (row < n && gcum_out) gcum_out[(size_t)(tok0 + row) * p.Hv + hv] = x;
             }
             named_bar(1, 128);
             const float glast = gam[n - 1];
@@ -371,16 +412,16 @@ k_tc_fwd(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
             }
             named_bar(1, 128);
             blocked_inverse(Lm, Tb, pt);
-            if (a.A32) {  // fp32 A and P for the backward's gradient kernels
+            if (A32_out) {  // fp32 A and P for the backward's gradient kernels
                 const size_t mat = ((size_t)(sr.c0 + j) * p.Hv + hv) * C * C;
                 const int r = pt >> 1, hh = pt & 1;
-                float4 *dst = reinterpret_cast<float4 *>(a.A32 + mat + (size_t)r * C + 32 * hh);
+                float4 *dst = reinterpret_cast<float4 *>(A32_out + mat + (size_t)r * C + 32 * hh);
 #pragma unroll
                 for (int q4 = 0; q4 < 8; ++q4)
                     dst[q4] = make_float4(Lm[r * 65 + 32 * hh + 4 * q4], Lm[r * 65 + 32 * hh + 4 * q4 + 1],
                                           Lm[r * 65 + 32 * hh + 4 * q4 + 2], Lm[r * 65 + 32 * hh + 4 * q4 + 3]);
                 if (row >= 64) {
-                    float4 *pd = reinterpret_cast<float4 *>(a.P32 + mat + (size_t)(row - 64) * C);
+                    float4 *pd = reinterpret_cast<float4 *>(P32_out + mat + (size_t)(row - 64) * C);
 #pragma unroll
                     for (int q4 = 0; q4 < 16; ++q4) {
                         const uint32_t *src = q4 < 8 ? raw0 + 4 * q4 : raw1 + 4 * (q4 - 8);
@@ -400,10 +441,10 @@ k_tc_fwd(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
 #pragma unroll
                     for (int e = 0; e < 8; ++e) vals[e] = Lm[r * 65 + 8 * ch + e];
                     st_split_chunk(sb + SM_AHL, sb + SM_AHL + 8192, r, ch, vals);
-                    if (a.A && r < n) {
+                    if (A_out && r < n) {
                         uint4 pk = make_uint4(pack_bf16(vals[0], vals[1]), pack_bf16(vals[2], vals[3]),
                                               pack_bf16(vals[4], vals[5]), pack_bf16(vals[6], vals[7]));
-                        *reinterpret_cast<uint4 *>(a.A + ((size_t)(tok0 + r) * p.Hv + hv) * C + 8 * ch) = pk;
+                        *reinterpret_cast<uint4 *>(A_out + ((size_t)(tok0 + r) * p.Hv + hv) * C + 8 * ch) = pk;
                     }
                 }
             }
@@ -431,7 +472,6 @@ k_tc_fwd(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
         const int v = 32 * (warp & 3) + lane;          // value column = TMEM lane
         const int hh = (warp - W_STATE0) >> 2;         // key half / chunk-column half
         const uint32_t trow = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
-        const size_t st_base = ((size_t)s * p.Hv + hv) * DK * DV;
         int failed = -1, fj = 0;
         auto wwait = [&](int id, uint32_t par, int j) {  // warp-uniform bounded wait
             bool w = mbar_wait_warp(bar(id), par, abort_flag);
@@ -440,7 +480,7 @@ k_tc_fwd(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
         };
         float S[64];
 #pragma unroll
-        for (int i = 0; i < 64; ++i) S[i] = a.h0 ? a.h0[st_base + (size_t)(64 * hh + i) * DV + v] : 0.f;
+        for (int i = 0; i < 64; ++i) S[i] = init ? init[(size_t)(64 * hh + i) * DV + v] : 0.f;
 
         auto epilogue = [&](int jj) -> bool {
             const int tok0 = sr.tok0 + jj * C, n = min(C, sr.tok1 - tok0), b = jj & 1;
@@ -457,13 +497,13 @@ k_tc_fwd(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
                     tc_fence_before();
                     mbar_arrive(bar(B_EPIFREE0 + b));
                 }
-                if (a.o) {
+                if (o_out) {
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
                         const int c = 32 * hh + 16 * half + i;
                         if (c < n) {
                             float ov = p.scale * fmaf(Gm[c], __uint_as_float(qs[i]), __uint_as_float(oo[i]));
-                            a.o[((size_t)(tok0 + c) * p.Hv + hv) * DV + v] = __float2bfloat16_rn(ov);
+                            o_out[((size_t)(tok0 + c) * p.Hv + hv) * DV + v] = __float2bfloat16_rn(ov);
                         }
                     }
                 }
@@ -481,10 +521,10 @@ k_tc_fwd(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
                 st_split_chunk(sb + SM_SS + hh * 16384, sb + SM_SS + 32768 + hh * 16384, v, ch, S + 8 * ch);
             fence_proxy_async_smem();
             mbar_arrive(bar(B_SSREADY));
-            if (a.h) {
+            if (h_out) {
                 const size_t hb = ((size_t)(sr.c0 + j) * p.Hv + hv) * DK * DV;
 #pragma unroll
-                for (int i = 0; i < 64; ++i) a.h[hb + (size_t)(64 * hh + i) * DV + v] = S[i];
+                for (int i = 0; i < 64; ++i) h_out[hb + (size_t)(64 * hh + i) * DV + v] = S[i];
             }
             // value column v at chunk rows 32hh .. 32hh + 31, as bf16 pairs (consumed in (c))
             uint32_t vr[16];
@@ -556,9 +596,9 @@ k_tc_fwd(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
             tc_fence_before();
         }
         if (ok && nck > 0) ok = epilogue(nck - 1);
-        if (ok && a.ht) {
+        if (ok && fin) {
 #pragma unroll
-            for (int i = 0; i < 64; ++i) a.ht[st_base + (size_t)(64 * hh + i) * DV + v] = S[i];
+            for (int i = 0; i < 64; ++i) fin[(size_t)(64 * hh + i) * DV + v] = S[i];
         }
         if (failed >= 0) record_timeout(p, failed, fj);
     }
@@ -601,7 +641,7 @@ bool tc_fwd_supported(const Plan &p) { return p.io == GDN_BF16 && p.K == DK && p
 
 cudaError_t launch_tc_fwd(const Plan &p, const void *q, const void *k, const void *v, const float *g,
                           const float *beta, const float *h0, void *o, float *g_cum, void *A, float *h,
-                          float *ht, cudaStream_t st, bool g_is_cum, float *A32, float *P32) {
+                          float *ht, cudaStream_t st, bool g_is_cum, float *A32, float *P32, const CpSplit *cp) {
     CUtensorMap tk, tq;
     if (!make_head_map(&tk, k, p.Hq, p) || !make_head_map(&tq, q, p.Hq, p)) return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(k_tc_fwd, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
@@ -619,7 +659,21 @@ cudaError_t launch_tc_fwd(const Plan &p, const void *q, const void *k, const voi
     a.g_is_cum = g_is_cum ? 1 : 0;
     a.A32 = A32;
     a.P32 = P32;
-    dim3 grid(p.n_seqs, p.Hv);
+    a.seg_len = 0;
+    a.n_seg = 1;
+    a.warm = 0;
+    a.mode = 0;
+    a.serial = nullptr;
+    a.seg_states = nullptr;
+    if (cp) {
+        a.seg_len = cp->seg_len;
+        a.n_seg = cp->n_seg;
+        a.warm = cp->warm;
+        a.mode = cp->mode;
+        a.serial = cp->serial;
+        a.seg_states = cp->seg_states;
+    }
+    dim3 grid(p.n_seqs * a.n_seg, p.Hv);
     k_tc_fwd<<<grid, NUM_THREADS, SMEM_BYTES, st>>>(tk, tq, p, a);
     return cudaGetLastError();
 }

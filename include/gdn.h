@@ -106,8 +106,11 @@ size_t gdn_bwd_workspace_bytes(const gdn_problem *p);
  * GDN_CP_WARMUP (the pages' sliding-window warmup, FlashQLA news page,
  * "Technical Principles"): when the trigger fires, each segment after the
  * first starts from the state obtained by running warmup_chunks chunks from a
- * zero state; the result is then approximate, with error bounded by
- * exp(sum of g over the warmup window) * |S| (see the design notes).
+ * zero state; the result is then approximate: the state error at a segment
+ * start is at most exp(sum of g over its warmup window) * |S|_F, S the exact
+ * state at the window start.  A value head whose gate sum over some warmup
+ * window is above ln(1e-4) runs unsplit (exact) in that sequence.  g_cum, A
+ * and h are as in the exact path; final_state comes from the last segment.
  */
 gdn_status gdn_fwd(const gdn_problem *p,
                    const void *q, const void *k, const void *v,
@@ -158,6 +161,20 @@ gdn_status gdn_fwd_noalloc(const gdn_problem *p,
                            const float *g, const float *beta, const float *h0,
                            void *o, float *g_cum, void *A, float *h, float *final_state,
                            gdn_stream_t stream);
+
+/*
+ * Sequence splitting with warmup (the "AutoCP" of the FlashQLA pages: news
+ * page, "FlashQLA's core advantages"; blog post, section 1).
+ * gdn_cp_trigger: 1 iff the pages' rule turns splitting on for n_seqs
+ *   sequences of up to seq_len tokens and n_heads value heads
+ *   (n_seqs * n_heads <= 40, or <= 56 with seq_len >= 8192).
+ * gdn_cp_plan: 1 iff gdn_fwd would split this problem (cp_mode ==
+ *   GDN_CP_WARMUP, bf16 with K = V = 128, trigger on, more than one segment);
+ *   then *seg_len = L = round(sqrt(N)) chunks for N chunks of the longest
+ *   sequence and *n_seg = ceil(N / L).  Returns 0 otherwise, -1 on a bad problem.
+ */
+int gdn_cp_trigger(int64_t n_seqs, int64_t n_heads, int64_t seq_len);
+int gdn_cp_plan(const gdn_problem *p, int *seg_len, int *n_seg);
 
 /* Reads the device error word a previous gdn_fwd / gdn_bwd left in
  * `workspace` (synchronises `stream`).  Returns GDN_OK or GDN_ERR_TIMEOUT. */

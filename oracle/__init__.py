@@ -169,3 +169,57 @@ def oracle_chunk_aux(k, g, beta, cu_seqlens=None, chunk=64):
                 A[b, s:e, h, :n] = scipy.linalg.solve_triangular(np.eye(n) + L, np.eye(n), lower=True,
                                                                 unit_diagonal=True)
     return g_cum, A
+
+
+def oracle_fwd_warmup(q, k, v, g, beta, scale=None, initial_state=None, cu_seqlens=None, seg_len=8,
+                      warm=6, log_eps=float(np.log(1e-4)), chunk=64, lib=None):
+    """The sequence-splitting forward with warmup, built only from oracle_fwd.
+
+    FlashQLA news page ("Technical Principles": sliding window warmup) and blog
+    post (section 1): each sequence of N chunks is cut into segments of
+    ``seg_len`` chunks; segment p > 0 starts from the state obtained by running
+    the ``warm`` chunks before it from a zero state (no cross-segment
+    correction); segment 0 starts from the initial state.  A value head whose
+    warmup windows do not all decay (sum of g over a window > log_eps) runs
+    unsplit, i.e. exactly.  Returns (o, final_state) in fp64.
+    """
+    q, k, v, g, beta, h0 = map(_f64, (q, k, v, g, beta, initial_state))
+    B, T, Hq, Kd = q.shape
+    Hv, Vd = v.shape[2], v.shape[3]
+    G = Hv // Hq
+    if scale is None:
+        scale = Kd ** -0.5
+    spans = ([(0, int(a), int(b)) for a, b in zip(cu_seqlens[:-1], cu_seqlens[1:])]
+             if cu_seqlens is not None else [(b, 0, T) for b in range(B)])
+    o = np.zeros((B, T, Hv, Vd))
+    ht = np.zeros((len(spans), Hv, Kd, Vd))
+    for si, (b, t0, t1) in enumerate(spans):
+        n_ck = (t1 - t0 + chunk - 1) // chunk
+        n_seg = (n_ck + seg_len - 1) // seg_len
+        for h in range(Hv):
+            sl = lambda x, a0, a1, hh: x[b:b + 1, a0:a1, hh:hh + 1]
+            hq = h // G
+            s0 = None if h0 is None else h0[si:si + 1, h:h + 1]
+            windows = [(max(0, p * seg_len - warm) * chunk + t0, min(t1, p * seg_len * chunk + t0))
+                       for p in range(1, n_seg)]
+            serial = any(g[b, a0:a1, h].sum() > log_eps for a0, a1 in windows)
+            if serial or n_seg <= 1:
+                oo, hh_ = oracle_fwd(sl(q, t0, t1, hq), sl(k, t0, t1, hq), sl(v, t0, t1, h), sl(g, t0, t1, h),
+                                     sl(beta, t0, t1, h), scale, s0, lib=lib)
+                o[b, t0:t1, h] = oo[0, :, 0]
+                ht[si, h] = hh_[0, 0]
+                continue
+            for p in range(n_seg):
+                a0, a1 = t0 + p * seg_len * chunk, min(t1, t0 + (p + 1) * seg_len * chunk)
+                if p == 0:
+                    start = s0
+                else:
+                    w0, w1 = windows[p - 1]
+                    _, start = oracle_fwd(sl(q, w0, w1, hq), sl(k, w0, w1, hq), sl(v, w0, w1, h),
+                                          sl(g, w0, w1, h), sl(beta, w0, w1, h), scale, None, lib=lib)
+                oo, hh_ = oracle_fwd(sl(q, a0, a1, hq), sl(k, a0, a1, hq), sl(v, a0, a1, h), sl(g, a0, a1, h),
+                                     sl(beta, a0, a1, h), scale, start, lib=lib)
+                o[b, a0:a1, h] = oo[0, :, 0]
+                if p == n_seg - 1:
+                    ht[si, h] = hh_[0, 0]
+    return o, ht

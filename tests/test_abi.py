@@ -102,3 +102,30 @@ def test_no_cpu_path():
     x = torch.zeros(1, 64, 1, 64)
     with pytest.raises(ValueError):
         gdn.chunk_gated_delta_rule_fwd(x, x, x, torch.zeros(1, 64, 1), torch.zeros(1, 64, 1))
+
+
+def test_cp_trigger_matches_pages_rule(lib):
+    import json
+    rule = json.load(open(os.path.join(ROOT, "tests", "golden", "autocp_rule.json")))
+    lib.gdn_cp_trigger.argtypes = [ctypes.c_int64] * 3
+    lib.gdn_cp_trigger.restype = ctypes.c_int
+    for c in rule["cases"]:
+        assert lib.gdn_cp_trigger(1, c["bh"], c["seq_len"]) == int(c["on"]), c
+        assert lib.gdn_cp_trigger(c["bh"], 1, c["seq_len"]) == int(c["on"]), c
+
+
+def test_cp_plan_geometry(lib):
+    lib.gdn_cp_plan.argtypes = [ctypes.POINTER(gdn._Problem), ctypes.POINTER(ctypes.c_int),
+                                ctypes.POINTER(ctypes.c_int)]
+    lib.gdn_cp_plan.restype = ctypes.c_int
+    L, n = ctypes.c_int(), ctypes.c_int()
+    # small-head long sequence: 512 chunks -> L = round(sqrt(512)) = 23, 23 segments
+    p = _prob(B=1, T=32768, Hq=4, Hv=8, n_seqs=1, cp_mode=2, warmup_chunks=6)
+    assert lib.gdn_cp_plan(ctypes.byref(p), ctypes.byref(L), ctypes.byref(n)) == 1
+    assert (L.value, n.value) == (23, 23)
+    assert lib.gdn_fwd_workspace_bytes(ctypes.byref(p)) > 8 * 23 * 128 * 128 * 4
+    # exact mode, or a batch x heads product above the rule: no splitting
+    p.cp_mode = 0
+    assert lib.gdn_cp_plan(ctypes.byref(p), ctypes.byref(L), ctypes.byref(n)) == 0
+    p = _prob(B=2, T=8192, Hq=16, Hv=64, n_seqs=2, cp_mode=2)
+    assert lib.gdn_cp_plan(ctypes.byref(p), ctypes.byref(L), ctypes.byref(n)) == 0
