@@ -92,9 +92,11 @@ FwdWs fwd_layout(const Plan &p) {
     size_t mats = (size_t)p.total_chunks * p.Hv * C * C;
     w.err = c.take<uint32_t>(64);
     w.chunk_off = c.take<int32_t>((size_t)p.n_seqs + 1);
-    w.gam64 = c.take<double>(tokens * p.Hv);
-    w.A32 = c.take<float>(mats);
-    w.P32 = c.take<float>(mats);
+    // fp64 gate sums and fp32 A / P scratch serve only the CUDA-core path
+    const bool simt = !tc_fwd_supported(p);
+    w.gam64 = c.take<double>(simt ? tokens * p.Hv : 0);
+    w.A32 = c.take<float>(simt ? mats : 0);
+    w.P32 = c.take<float>(simt ? mats : 0);
     w.seg_len = 0;
     w.n_seg = 1;
     w.serial = w.seg_states = 0;
@@ -115,7 +117,7 @@ BwdWs bwd_layout(const Plan &p) {
     size_t states = (size_t)p.total_chunks * p.Hv * p.K * p.V;
     w.err = c.take<uint32_t>(64);
     w.chunk_off = c.take<int32_t>((size_t)p.n_seqs + 1);
-    w.gam64 = c.take<double>(tokens * p.Hv);
+    w.gam64 = c.take<double>(tc_fwd_supported(p) ? 0 : tokens * p.Hv);  // CUDA-core path only
     w.A32 = c.take<float>(mats);
     w.P32 = c.take<float>(mats);
     w.hbuf = c.take<float>(states);

@@ -14,7 +14,7 @@
 //   O     = scale (diag(Gam) Q S + (D o Q K^T) Delta)
 //   S'    = Gam_last S + K^T diag(E) Delta,   E_i = exp(gam_last - gam_i)
 // Delta = U - W S with W, U the pages' "W and U variables"; this file never
-// forms W or U (see the design notes on the R form).
+// forms W or U: Delta = A R needs neither.
 #include <cuda_runtime.h>
 
 #include "common.cuh"
