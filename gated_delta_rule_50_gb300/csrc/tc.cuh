@@ -211,6 +211,11 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
         "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
         : "memory");
 }
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+                 "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+                 : "memory");
+}
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 // D[tmem] (+)= A[tmem] * B[smem]^T; A: 128 lanes, 16 bf16 per k-step packed in 8 columns.
 __device__ __forceinline__ void mma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
@@ -225,6 +230,17 @@ __device__ __forceinline__ void mma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem, ui
 __device__ __forceinline__ void split_pack32(const float *x, uint32_t (&hi)[32], uint32_t (&lo)[32]) {
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
+        float h0, l0, h1, l1;
+        split2(x[2 * i], h0, l0);
+        split2(x[2 * i + 1], h1, l1);
+        hi[i] = pack_bf16(h0, h1);
+        lo[i] = pack_bf16(l0, l1);
+    }
+}
+// Packs 16 fp32 values (pairs along K) into hi / lo bf16 pair words.
+__device__ __forceinline__ void split_pack16(const float *x, uint32_t (&hi)[16], uint32_t (&lo)[16]) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
         float h0, l0, h1, l1;
         split2(x[2 * i], h0, l0);
         split2(x[2 * i + 1], h1, l1);

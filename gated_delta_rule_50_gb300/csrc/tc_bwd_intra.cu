@@ -20,9 +20,11 @@
 // sides are derived); scalings are folded into the operand tiles so that the
 // TMEM accumulation is exact in structure.
 //
-// The kernel is phase-sequential: 256 threads, one of them issues the MMAs of
-// a phase and all wait on one mbarrier before the next phase.  Many CTAs (one
-// per chunk and q/k head) keep the GPU busy.
+// The kernel is phase-sequential: 512 threads (each TMEM lane quarter is
+// served by four warps, one per 16 chunk rows), one of them issues the MMAs of
+// a phase and all wait on one mbarrier before the next phase.  The k, q, dO and
+// v chunk tiles arrive by TMA; dv leaves through a shared-memory staging tile
+// in 16-byte stores.  Many CTAs (one per chunk and q/k head) keep the GPU busy.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -36,7 +38,8 @@ namespace {
 using namespace tc;
 
 constexpr int DK = 128, DV = 128;
-constexpr int NT = 256;
+constexpr int NT = 512;     // 16 warps: TMEM lane quarter = warp & 3, column quarter = warp >> 2
+constexpr int NW = NT / 32;
 
 // shared memory map (bytes from a 1024-aligned base)
 constexpr uint32_t S_KQ = 0;         // [kb0: K 8K, Q 8K][kb1: K 8K, Q 8K]
@@ -44,14 +47,15 @@ constexpr uint32_t S_DO = 32768;     // dO [r][v] 2 x 8K; later dQK hi / lo [r][
 constexpr uint32_t S_A = 49152;      // A hi / lo [r][i]
 constexpr uint32_t S_P = 65536;      // P hi / lo [r'][r]; later (dKK + dKK^T) hi / lo
 constexpr uint32_t S_DR = 81920;     // Dl^T hi | R^T hi | Dl^T lo | R^T lo ([v][i], 16K each); later E Dl, Y
-constexpr uint32_t S_DD = 147456;    // dDl^T hi / lo [v][r]; later scale Gam dO hi / lo [r][v]
+constexpr uint32_t S_DD = 147456;    // V [r][v] (TMA); dDl^T hi / lo [v][r]; dv staging; scale Gam dO hi / lo [r][v]
 constexpr uint32_t S_F = 180224;     // fp32 [64][65]: dA, then dL
-constexpr uint32_t S_F2 = S_F + 64 * 65 * 4;   // fp32 [64][65]: A^T dA
+constexpr uint32_t S_F2 = S_F + 64 * 65 * 4;   // fp32 [64][65]: dQK staging
 constexpr uint32_t S_VEC = S_F2 + 64 * 65 * 4; // gam, Gam, E, beta, beta Gam (64 each); per-warp partial sums
-constexpr uint32_t S_BAR = S_VEC + 5 * 256 + 2 * 8 * 64 * 4 + 2 * 8 * 4;
+constexpr uint32_t S_BAR = S_VEC + (5 * 64 + 2 * NW * 64 + 2 * NW) * 4;
 constexpr uint32_t S_MISC = S_BAR + 16;
 constexpr uint32_t S_TOTAL = S_MISC + 16;
 constexpr uint32_t SMEM_BYTES = S_TOTAL + 1024;
+static_assert(SMEM_BYTES <= 232448, "shared memory");
 
 // TMEM columns
 constexpr uint32_t C_DQ = 0, C_DK = 64, C_HT = 128, C_KS = 256, C_QS = 320, C_DL = 384, C_DR = 448;
@@ -62,7 +66,6 @@ constexpr uint32_t ID_MM = idesc_bf16(128, 64, 1, 1);
 constexpr uint32_t ID_KM = idesc_bf16(128, 64, 0, 1);
 
 struct IntraArgs {
-    const __nv_bfloat16 *v, *d_o;
     const float *g_cum, *beta, *A32, *P32, *hbuf, *dSe;
     __nv_bfloat16 *dq, *dk, *dv;
     float *dbeta, *dg;
@@ -71,11 +74,11 @@ struct IntraArgs {
 __device__ __forceinline__ uint64_t kdesc(uint32_t a) { return sdesc_sw128(a, 16, 1024); }
 __device__ __forceinline__ uint64_t mdesc(uint32_t a, uint32_t lbo) { return sdesc_sw128(a, lbo, 1024); }
 
-// x[j] on every lane -> lane l returns sum over the warp's lanes of x[l].
-__device__ __forceinline__ float warp_transpose_sum(float (&x)[32]) {
+// x[j] (16 values) on every lane -> every lane l returns the sum over all 32 lanes of x[l & 15].
+__device__ __forceinline__ float warp_transpose_sum16(float (&x)[16]) {
     const int lane = threadIdx.x & 31;
 #pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) {
+    for (int o = 8; o >= 1; o >>= 1) {
         const bool up = (lane & o) != 0;
 #pragma unroll
         for (int j = 0; j < o; ++j) {
@@ -84,18 +87,20 @@ __device__ __forceinline__ float warp_transpose_sum(float (&x)[32]) {
             x[j] = keep + __shfl_xor_sync(0xffffffffu, send, o);
         }
     }
-    return x[0];
+    return x[0] + __shfl_xor_sync(0xffffffffu, x[0], 16);
 }
 
 __device__ __forceinline__ float bf16_lo_f(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi_f(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
+// element (row, col) of a 64-wide bf16 swizzled tile
+__device__ __forceinline__ float tile_at(const unsigned char *sm, uint32_t off, int row, int col) {
+    const uint32_t o = (uint32_t)row * 128u + ((uint32_t)((col >> 3) ^ (row & 7)) << 4) + (uint32_t)(col & 7) * 2u;
+    return __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(sm + off + o));
+}
 // element (row, col) of a 64-wide bf16 hi / lo swizzled tile pair, summed
 __device__ __forceinline__ float tile_hl(const unsigned char *sm, uint32_t hi_off, uint32_t lo_off, int row, int col) {
-    const uint32_t o = (uint32_t)row * 128u + ((uint32_t)((col >> 3) ^ (row & 7)) << 4) + (uint32_t)(col & 7) * 2u;
-    const __nv_bfloat16 h = *reinterpret_cast<const __nv_bfloat16 *>(sm + hi_off + o);
-    const __nv_bfloat16 l = *reinterpret_cast<const __nv_bfloat16 *>(sm + lo_off + o);
-    return __bfloat162float(h) + __bfloat162float(l);
+    return tile_at(sm, hi_off, row, col) + tile_at(sm, lo_off, row, col);
 }
 __device__ __forceinline__ void tile_st_hl(unsigned char *sm, uint32_t hi_off, uint32_t lo_off, int row, int col,
                                            float x) {
@@ -104,25 +109,30 @@ __device__ __forceinline__ void tile_st_hl(unsigned char *sm, uint32_t hi_off, u
     *reinterpret_cast<__nv_bfloat16 *>(sm + hi_off + o) = h;
     *reinterpret_cast<__nv_bfloat16 *>(sm + lo_off + o) = __float2bfloat16_rn(x - __bfloat162float(h));
 }
+// element (row, v) of a [64 rows][128] bf16 tile loaded by two 64-column TMA boxes (8 KB each)
+__device__ __forceinline__ float tile128_at(const unsigned char *sm, uint32_t off, int row, int v) {
+    return tile_at(sm, off + (uint32_t)(v >> 6) * 8192u, row, v & 63);
+}
 
 __global__ void __launch_bounds__(NT, 1)
 k_tc_bwd_intra(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
-               const __grid_constant__ CUtensorMap tm_do, Plan p, IntraArgs a) {
+               const __grid_constant__ CUtensorMap tm_do, const __grid_constant__ CUtensorMap tm_v, Plan p,
+               IntraArgs a) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char *sm = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                           ~uintptr_t(1023));
     const uint32_t sb = smem_u32(sm);
     const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
-    const int lq = warp & 3, hh = warp >> 2;
-    const int lrow = 32 * lq + lane;  // TMEM lane of this thread (value v, or key)
+    const int lq = warp & 3, hh = warp >> 2;  // TMEM lane quarter; chunk rows 16 hh .. 16 hh + 15
+    const int lrow = 32 * lq + lane;          // TMEM lane of this thread (value v, or key)
     const uint32_t trow = (uint32_t)(32 * lq) << 16;
     uint32_t *misc = reinterpret_cast<uint32_t *>(sm + S_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(misc + 1);
     float *gam = reinterpret_cast<float *>(sm + S_VEC), *Gm = gam + 64, *Ev = gam + 128, *bet = gam + 192,
           *bg = gam + 256;
     // per-warp partial sums (summed in a fixed order, so the result is deterministic):
-    // rdb / rdg [8 warps][64 rows] for dbeta / dgam, sH / sF [8] for <h, dSe> and sum F
-    float *rdb_all = gam + 320, *rdg_all = rdb_all + 8 * 64, *sH = rdg_all + 8 * 64, *sF = sH + 8;
+    // rdb / rdg [16 warps][64 rows] for dbeta / dgam, sH / sF [16] for <h, dSe> and sum F
+    float *rdb_all = gam + 320, *rdg_all = rdb_all + NW * 64, *sH = rdg_all + NW * 64, *sF = sH + NW;
     float *rdb = rdb_all + 64 * warp, *rdg = rdg_all + 64 * warp;
     float *Fa = reinterpret_cast<float *>(sm + S_F), *Fb = reinterpret_cast<float *>(sm + S_F2);
     const uint32_t bar_tma = sb + S_BAR, bar_mma = sb + S_BAR + 8;
@@ -180,12 +190,14 @@ k_tc_bwd_intra(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         const int hv = hq * p.G + g;
         const size_t st_off = ((size_t)gc * p.Hv + hv) * DK * DV;
         const size_t mat = ((size_t)gc * p.Hv + hv) * C * C;
-        // ---------------------------------------------------------------- per-head vectors, dO tile, A / P tiles
+        // ---------------------------------------------------------------- per-head vectors, dO / V tiles, A / P tiles
         ++tma_issued;
         if (t == 0) {
-            mbar_arrive_expect_tx(bar_tma, 16384);
+            mbar_arrive_expect_tx(bar_tma, 32768);
             tma_load_3d(sb + S_DO, &tm_do, bar_tma, 0, hv, tok0);
             tma_load_3d(sb + S_DO + 8192, &tm_do, bar_tma, 64, hv, tok0);
+            tma_load_3d(sb + S_DD, &tm_v, bar_tma, 0, hv, tok0);
+            tma_load_3d(sb + S_DD + 8192, &tm_v, bar_tma, 64, hv, tok0);
         }
         if (t < 64) {
             const float glast = a.g_cum[(size_t)(tok0 + n - 1) * p.Hv + hv];
@@ -200,32 +212,27 @@ k_tc_bwd_intra(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
             bet[t] = bv;
             bg[t] = t < n ? bv * __expf(gv) : 0.f;
         }
-        for (int o = t; o < 2 * 8 * 64 + 16; o += NT) rdb_all[o] = 0.f;  // rdb, rdg, sH, sF
+        for (int o = t; o < 2 * NW * 64 + 2 * NW; o += NT) rdb_all[o] = 0.f;  // rdb, rdg, sH, sF
         {
-            const int r = t >> 2, q = t & 3;  // 16 columns of row r
-            const float *ar = a.A32 + mat + (size_t)r * C + 16 * q, *pr = a.P32 + mat + (size_t)r * C + 16 * q;
-#pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {
-                float av[8], pv[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    av[e] = ar[8 * hf + e];
-                    pv[e] = pr[8 * hf + e];
-                }
-                st_split_chunk(sb + S_A, sb + S_A + 8192, r, 2 * q + hf, av);
-                st_split_chunk(sb + S_P, sb + S_P + 8192, r, 2 * q + hf, pv);
-            }
+            const int r = t >> 3, q = t & 7;  // 8 columns of row r
+            const float4 *ar = reinterpret_cast<const float4 *>(a.A32 + mat + (size_t)r * C + 8 * q);
+            const float4 *pr = reinterpret_cast<const float4 *>(a.P32 + mat + (size_t)r * C + 8 * q);
+            const float4 a0 = ar[0], a1 = ar[1], p0 = pr[0], p1 = pr[1];
+            const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+            const float pv[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+            st_split_chunk(sb + S_A, sb + S_A + 8192, r, q, av);
+            st_split_chunk(sb + S_P, sb + S_P + 8192, r, q, pv);
         }
         // ---------------------------------------------------------------- P1: h^T (lane v) -> TMEM; KS, QS
         {
-            const float *hc = a.hbuf + st_off + (size_t)(64 * hh) * DV + lrow;
-            float x[64];
+            const float *hc = a.hbuf + st_off + (size_t)(32 * hh) * DV + lrow;
+            float x[32];
 #pragma unroll
-            for (int i = 0; i < 64; ++i) x[i] = hc[(size_t)i * DV];
-            uint32_t hi[32], lo[32];
-            split_pack32(x, hi, lo);
-            tmem_st32(tmem + trow + C_HT + 32 * hh, hi);
-            tmem_st32(tmem + trow + C_HT + 64 + 32 * hh, lo);
+            for (int i = 0; i < 32; ++i) x[i] = hc[(size_t)i * DV];
+            uint32_t hi[16], lo[16];
+            split_pack16(x, hi, lo);
+            tmem_st16(tmem + trow + C_HT + 16 * hh, hi);
+            tmem_st16(tmem + trow + C_HT + 64 + 16 * hh, lo);
             tmem_wait_st();
         }
         __syncthreads();  // vectors visible
@@ -238,61 +245,54 @@ k_tc_bwd_intra(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
                     mma_bf16_ta(tmem + C_QS, tmem + C_HT + 64 * sp + 8 * kk, kdesc(bo + 8192), ID_KK, (sp | kk) != 0);
                 }
         }
+        // dSe^T (lane v) loads overlap the MMAs; stored to TMEM once h^T has been consumed
+        float xd[32];
+        {
+            const float *dc = a.dSe + st_off + (size_t)(32 * hh) * DV + lrow;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) xd[i] = dc[(size_t)i * DV];
+        }
         mma_sync();
         if (!ok) break;
+        tma_wait();  // dO and V tiles of this head
+        if (!ok) break;
         // ---------------------------------------------------------------- P2: R^T tile, dgam (scale Gam dO . QS)
-        float Xr[32], KSr[32];  // (V - Gam KS) and KS at chunk rows c = 32 hh + i, value lrow
+        float Xr[16], KSr[16];  // (V - Gam KS) and KS at chunk rows c = 16 hh + i, value lrow
         {
-            uint32_t ks[32], qs[32];
-            tmem_ld32(tmem + trow + C_KS + 32 * hh, ks);
-            tmem_ld32(tmem + trow + C_QS + 32 * hh, qs);
+            uint32_t ks[16], qs[16];
+            tmem_ld16(tmem + trow + C_KS + 16 * hh, ks);
+            tmem_ld16(tmem + trow + C_QS + 16 * hh, qs);
             tmem_wait_ld();
-            float part[32];
-            const uint16_t *vp = reinterpret_cast<const uint16_t *>(a.v) + (size_t)hv * DV + lrow;
-            const uint16_t *dp = reinterpret_cast<const uint16_t *>(a.d_o) + (size_t)hv * DV + lrow;
-            const size_t rs = (size_t)p.Hv * DV;
+            float part[16];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                const int c = 32 * hh + i;
+            for (int i = 0; i < 16; ++i) {
+                const int c = 16 * hh + i;
                 float vv = 0.f, dd = 0.f;
                 if (c < n) {
-                    vv = __uint_as_float((uint32_t)vp[(size_t)(tok0 + c) * rs] << 16);
-                    dd = __uint_as_float((uint32_t)dp[(size_t)(tok0 + c) * rs] << 16);
+                    vv = tile128_at(sm, S_DD, c, lrow);
+                    dd = tile128_at(sm, S_DO, c, lrow);
                 }
                 KSr[i] = __uint_as_float(ks[i]);
                 Xr[i] = vv - Gm[c] * KSr[i];
                 part[i] = p.scale * Gm[c] * dd * __uint_as_float(qs[i]);
             }
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
+            for (int q2 = 0; q2 < 2; ++q2) {
                 float r8[8];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) r8[e] = bet[32 * hh + 8 * q4 + e] * Xr[8 * q4 + e];
-                st_split_chunk(sb + S_DR + 16384, sb + S_DR + 49152, lrow, 4 * hh + q4, r8);
+                for (int e = 0; e < 8; ++e) r8[e] = bet[16 * hh + 8 * q2 + e] * Xr[8 * q2 + e];
+                st_split_chunk(sb + S_DR + 16384, sb + S_DR + 49152, lrow, 2 * hh + q2, r8);
             }
-            rdg[32 * hh + lane] += warp_transpose_sum(part);
+            const float s = warp_transpose_sum16(part);
+            if (lane < 16) rdg[16 * hh + lane] += s;
         }
-        // dSe^T (lane v) -> TMEM (h^T no longer needed); <h, dSe> partial
-        {
-            const float *dc = a.dSe + st_off + (size_t)(64 * hh) * DV + lrow;
-            const float *hc = a.hbuf + st_off + (size_t)(64 * hh) * DV + lrow;
-            float x[64], hd = 0.f;
-#pragma unroll
-            for (int i = 0; i < 64; ++i) {
-                x[i] = dc[(size_t)i * DV];
-                hd = fmaf(x[i], hc[(size_t)i * DV], hd);
-            }
-#pragma unroll
-            for (int o = 16; o >= 1; o >>= 1) hd += __shfl_xor_sync(0xffffffffu, hd, o);
-            if (lane == 0) sH[warp] += hd;
-            uint32_t hi[32], lo[32];
-            split_pack32(x, hi, lo);
-            tmem_st32(tmem + trow + C_HT + 32 * hh, hi);
-            tmem_st32(tmem + trow + C_HT + 64 + 32 * hh, lo);
+        {  // dSe^T (lane v) -> TMEM (h^T no longer needed)
+            uint32_t hi[16], lo[16];
+            split_pack16(xd, hi, lo);
+            tmem_st16(tmem + trow + C_HT + 16 * hh, hi);
+            tmem_st16(tmem + trow + C_HT + 64 + 16 * hh, lo);
             tmem_wait_st();
         }
-        tma_wait();  // dO tile of this head
-        if (!ok) break;
         pre_mma();
         if (t == 0) {
             for (int tt = 0; tt < 3; ++tt)  // Dl^T = R^T A^T
@@ -312,30 +312,30 @@ k_tc_bwd_intra(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         if (!ok) break;
         // ---------------------------------------------------------------- P3: dDl^T and Dl^T tiles; F
         {
-            uint32_t dl[32], kd[32], pd[32];
-            tmem_ld32(tmem + trow + C_DL + 32 * hh, dl);
-            tmem_ld32(tmem + trow + C_KS + 32 * hh, kd);
-            tmem_ld32(tmem + trow + C_QS + 32 * hh, pd);
+            uint32_t dl[16], kd[16], pd[16];
+            tmem_ld16(tmem + trow + C_DL + 16 * hh, dl);
+            tmem_ld16(tmem + trow + C_KS + 16 * hh, kd);
+            tmem_ld16(tmem + trow + C_QS + 16 * hh, pd);
             tmem_wait_ld();
-            float part[32];
+            float part[16];
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
+            for (int q2 = 0; q2 < 2; ++q2) {
                 float x8[8], d8[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
-                    const int i = 8 * q4 + e, c = 32 * hh + i;
+                    const int i = 8 * q2 + e, c = 16 * hh + i;
                     x8[e] = fmaf(p.scale, __uint_as_float(pd[i]), Ev[c] * __uint_as_float(kd[i]));
                     d8[e] = __uint_as_float(dl[i]);
                     part[i] = Ev[c] * __uint_as_float(kd[i]) * d8[e];
                 }
-                st_split_chunk(sb + S_DD, sb + S_DD + 16384, lrow, 4 * hh + q4, x8);
-                st_split_chunk(sb + S_DR, sb + S_DR + 32768, lrow, 4 * hh + q4, d8);
+                st_split_chunk(sb + S_DD, sb + S_DD + 16384, lrow, 2 * hh + q2, x8);
+                st_split_chunk(sb + S_DR, sb + S_DR + 32768, lrow, 2 * hh + q2, d8);
             }
-            const float f = warp_transpose_sum(part);  // F of row 32 hh + lane (partial over 32 values)
-            rdg[32 * hh + lane] -= f;
-            float fs = f;
+            const float f = warp_transpose_sum16(part);  // F of row 16 hh + (lane & 15), partial over 32 values
+            if (lane < 16) rdg[16 * hh + lane] -= f;
+            float fs = lane < 16 ? f : 0.f;
 #pragma unroll
-            for (int o = 16; o >= 1; o >>= 1) fs += __shfl_xor_sync(0xffffffffu, fs, o);
+            for (int o = 8; o >= 1; o >>= 1) fs += __shfl_xor_sync(0xffffffffu, fs, o);
             if (lane == 0) sF[warp] += fs;
         }
         pre_mma();
@@ -357,74 +357,85 @@ k_tc_bwd_intra(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         if (!ok) break;
         // ---------------------------------------------------------------- P4: dV, dbeta, dgam terms, E Dl / Y tiles
         {
-            uint32_t dr[32], dl[32];
-            tmem_ld32(tmem + trow + C_DR + 32 * hh, dr);
-            tmem_ld32(tmem + trow + C_DL + 32 * hh, dl);
+            uint32_t dr[16], dl[16];
+            tmem_ld16(tmem + trow + C_DR + 16 * hh, dr);
+            tmem_ld16(tmem + trow + C_DL + 16 * hh, dl);
             tmem_wait_ld();
-            float pb[32], pg[32];
-            uint16_t *dvp = reinterpret_cast<uint16_t *>(a.dv) + (size_t)hv * DV + lrow;
-            const size_t rs = (size_t)p.Hv * DV;
+            float pb[16], pg[16];
+            __nv_bfloat16 *dvs = reinterpret_cast<__nv_bfloat16 *>(sm + S_DD);  // dv staging [r][128]
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
+            for (int q2 = 0; q2 < 2; ++q2) {
                 float y8[8], e8[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
-                    const int i = 8 * q4 + e, c = 32 * hh + i;
+                    const int i = 8 * q2 + e, c = 16 * hh + i;
                     const float drv = __uint_as_float(dr[i]);
-                    if (c < n) {
-                        __nv_bfloat16 b = __float2bfloat16_rn(bet[c] * drv);
-                        dvp[(size_t)(tok0 + c) * rs] = *reinterpret_cast<uint16_t *>(&b);
-                    }
+                    dvs[c * DV + lrow] = __float2bfloat16_rn(bet[c] * drv);
                     pb[i] = drv * Xr[i];
                     pg[i] = -bg[c] * drv * KSr[i];
                     y8[e] = -bg[c] * drv;
                     e8[e] = Ev[c] * __uint_as_float(dl[i]);
                 }
-                st_split_chunk(sb + S_DR, sb + S_DR + 32768, lrow, 4 * hh + q4, e8);
-                st_split_chunk(sb + S_DR + 16384, sb + S_DR + 49152, lrow, 4 * hh + q4, y8);
+                st_split_chunk(sb + S_DR, sb + S_DR + 32768, lrow, 2 * hh + q2, e8);
+                st_split_chunk(sb + S_DR + 16384, sb + S_DR + 49152, lrow, 2 * hh + q2, y8);
             }
-            rdb[32 * hh + lane] += warp_transpose_sum(pb);
-            rdg[32 * hh + lane] += warp_transpose_sum(pg);
+            const float sbt = warp_transpose_sum16(pb);
+            const float sgt = warp_transpose_sum16(pg);
+            if (lane < 16) {
+                rdb[16 * hh + lane] += sbt;
+                rdg[16 * hh + lane] += sgt;
+            }
         }
-        {  // dP (lanes 0..63) and dA (lanes 64..127): thread holds column i, rows r = 32 hh + j
-            uint32_t dd[32];
-            tmem_ld32(tmem + trow + (lq < 2 ? C_KS : C_QS) + 32 * hh, dd);
+        {  // dP (lanes 0..63) and dA (lanes 64..127): thread holds column i, rows r = 16 hh + j
+            uint32_t dd[16];
+            tmem_ld16(tmem + trow + (lq < 2 ? C_KS : C_QS) + 16 * hh, dd);
             tmem_wait_ld();
             if (lq < 2) {
                 const int i = lrow;
-                float colsum = 0.f, rowpart[32];
+                float colsum = 0.f, rowpart[16];
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const int r = 32 * hh + j;
-                    float m = 0.f;
+                for (int j = 0; j < 16; ++j) {
+                    const int r = 16 * hh + j;
+                    float m = 0.f, qk = 0.f;
                     if (i <= r && r < n) {
                         const float dpv = p.scale * __uint_as_float(dd[j]);
-                        m = dpv * a.P32[mat + (size_t)r * C + i];
-                        Fb[r * 65 + i] = __expf(gam[r] - gam[i]) * dpv;  // dQK, staged
-                    } else {
-                        Fb[r * 65 + i] = 0.f;
+                        m = dpv * tile_hl(sm, S_P, S_P + 8192, r, i);
+                        qk = __expf(gam[r] - gam[i]) * dpv;
                     }
+                    Fb[r * 65 + i] = qk;  // dQK, staged
                     rowpart[j] = m;
                     colsum += m;
                 }
+                __syncwarp();
                 rdg[i] -= colsum;
                 __syncwarp();
-                rdg[32 * hh + lane] += warp_transpose_sum(rowpart);
+                const float s = warp_transpose_sum16(rowpart);
+                if (lane < 16) rdg[16 * hh + lane] += s;
             } else {
                 const int i = lrow - 64;
 #pragma unroll
-                for (int j = 0; j < 32; ++j) Fa[(32 * hh + j) * 65 + i] = __uint_as_float(dd[j]);  // dA[r][i]
+                for (int j = 0; j < 16; ++j) Fa[(16 * hh + j) * 65 + i] = __uint_as_float(dd[j]);  // dA[r][i]
+            }
+        }
+        __syncthreads();
+        {  // dv out: 64 rows x 256 bytes from the staging tile, 16-byte stores
+            const uint4 *src = reinterpret_cast<const uint4 *>(sm + S_DD);
+            for (int o = t; o < 64 * 16; o += NT) {
+                const int r = o >> 4, c16 = o & 15;
+                if (r < n)
+                    *reinterpret_cast<uint4 *>(a.dv + (size_t)(tok0 + r) * p.Hv * DV + (size_t)hv * DV + 8 * c16) =
+                        src[o];
             }
         }
         __syncthreads();
         // scale Gam o dO tile [r][v] into the dDl region (its last reader, dA^T, is done)
         {
-            const int r = t >> 2, q = t & 3;  // 32 values: block q >> 1, chunks 4 (q & 1) .. + 3
+            const int r = t >> 3, q = t & 7;  // 16 values: block q >> 2, chunks 2 (q & 3), + 1
             const float gs = p.scale * Gm[r];
-            const int vb = q >> 1;
+            const int vb = q >> 2;
 #pragma unroll
-            for (int c4 = 0; c4 < 4; ++c4) {
-                const int ch = 4 * (q & 1) + c4;
+            for (int c2 = 0; c2 < 2; ++c2) {
+                const int ch = 2 * (q & 3) + c2;
                 const uint4 w = *reinterpret_cast<const uint4 *>(sm + S_DO + vb * 8192 + r * 128 + ((ch ^ (r & 7)) << 4));
                 const uint32_t u[4] = {w.x, w.y, w.z, w.w};
                 float x8[8];
@@ -445,7 +456,6 @@ k_tc_bwd_intra(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
             for (int e = 0; e < 8; ++e) x8[e] = Fb[r * 65 + 8 * ch + e];
             st_split_chunk(sb + S_DO, sb + S_DO + 8192, r, ch, x8);
         }
-        __syncthreads();  // the staged dQK in Fb is consumed before Fb is reused
         // ---------------------------------------------------------------- P5: dL = -(A^T dA A^T), strictly lower
         // on the tensor cores: Z^T = A dA~^T (dA~ = lower part of dA), then dL^T = -Z^T A.  Both are
         // M = 128 products whose rows 64..127 read neighbouring tiles and are ignored.
@@ -468,19 +478,19 @@ k_tc_bwd_intra(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         mma_sync();
         if (!ok) break;
         if (lq < 2) {  // Z^T rows (lanes 0..63) -> hi / lo bf16 A operand in TMEM
-            uint32_t z[32], hi[16], lo[16];
-            tmem_ld32(tmem + trow + C_KS + 32 * hh, z);
+            uint32_t z[16], hi[8], lo[8];
+            tmem_ld16(tmem + trow + C_KS + 16 * hh, z);
             tmem_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
+            for (int i = 0; i < 8; ++i) {
                 float h0, l0, h1, l1;
                 split2(__uint_as_float(z[2 * i]), h0, l0);
                 split2(__uint_as_float(z[2 * i + 1]), h1, l1);
                 hi[i] = pack_bf16(h0, h1);
                 lo[i] = pack_bf16(l0, l1);
             }
-            tmem_st16(tmem + trow + C_QS + 16 * hh, hi);
-            tmem_st16(tmem + trow + C_QS + 32 + 16 * hh, lo);
+            tmem_st8(tmem + trow + C_QS + 8 * hh, hi);
+            tmem_st8(tmem + trow + C_QS + 32 + 8 * hh, lo);
             tmem_wait_st();
         }
         pre_mma();
@@ -492,12 +502,12 @@ k_tc_bwd_intra(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         mma_sync();
         if (!ok) break;
         if (lq < 2) {  // Fa[r][i] = dL[r][i] = -(A^T Z)[r][i]
-            uint32_t z[32];
-            tmem_ld32(tmem + trow + C_KS + 32 * hh, z);
+            uint32_t z[16];
+            tmem_ld16(tmem + trow + C_KS + 16 * hh, z);
             tmem_wait_ld();
             const int i = lrow;
 #pragma unroll
-            for (int j = 0; j < 32; ++j) Fa[(32 * hh + j) * 65 + i] = -__uint_as_float(z[j]);
+            for (int j = 0; j < 16; ++j) Fa[(16 * hh + j) * 65 + i] = -__uint_as_float(z[j]);
         }
         __syncthreads();
         // K K^T for the beta and gate terms of dL (lanes 0..63 of a [K; Q] K^T product)
@@ -509,15 +519,15 @@ k_tc_bwd_intra(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
             }
         mma_sync();
         if (!ok) break;
-        if (lq < 2) {  // thread: row r = lrow, columns i = 32 hh + j
-            uint32_t kk[32];
-            tmem_ld32(tmem + trow + C_KS + 32 * hh, kk);
+        if (lq < 2) {  // thread: row r = lrow, columns i = 16 hh + j
+            uint32_t kk[16];
+            tmem_ld16(tmem + trow + C_KS + 16 * hh, kk);
             tmem_wait_ld();
             const int r = lrow;
-            float sb_ = 0.f, sg = 0.f, colpart[32];
+            float sb_ = 0.f, sg = 0.f, colpart[16];
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                const int i = 32 * hh + j;
+            for (int j = 0; j < 16; ++j) {
+                const int i = 16 * hh + j;
                 float m = 0.f;
                 if (i < r && r < n) {
                     const float w = Fa[r * 65 + i] * __expf(gam[r] - gam[i]) * __uint_as_float(kk[j]);
@@ -530,7 +540,8 @@ k_tc_bwd_intra(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
             rdb[r] += sb_;
             rdg[r] += sg;
             __syncwarp();
-            rdg[32 * hh + lane] -= warp_transpose_sum(colpart);
+            const float s = warp_transpose_sum16(colpart);
+            if (lane < 16) rdg[16 * hh + lane] -= s;
         }
         // dKK + dKK^T -> hi / lo tile [r][i] in the P region (dKK_ri = beta_r D_ri dL_ri, i < r)
         for (int o = t; o < 64 * 64; o += NT) {
@@ -543,50 +554,73 @@ k_tc_bwd_intra(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         tc_fence_before();  // every K K^T load is done before the columns are overwritten
         __syncthreads();
         tc_fence_after();
-        // h and dSe (lane = key) -> TMEM as A operands of the dq / dk products
+        // h and dSe (lane = key) -> TMEM as A operands of the dq / dk products; <h, dSe> partial
         {
-            const float *hr = a.hbuf + st_off + (size_t)lrow * DV + 64 * hh;
-            const float *dr = a.dSe + st_off + (size_t)lrow * DV + 64 * hh;
-            float x[64];
-            uint32_t hi[32], lo[32];
+            const float4 *hr = reinterpret_cast<const float4 *>(a.hbuf + st_off + (size_t)lrow * DV + 32 * hh);
+            const float4 *dr = reinterpret_cast<const float4 *>(a.dSe + st_off + (size_t)lrow * DV + 32 * hh);
+            float xh[32], xs[32];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const float4 w = reinterpret_cast<const float4 *>(hr)[i];
-                x[4 * i] = w.x; x[4 * i + 1] = w.y; x[4 * i + 2] = w.z; x[4 * i + 3] = w.w;
+            for (int i = 0; i < 8; ++i) {
+                const float4 w = hr[i], u = dr[i];
+                xh[4 * i] = w.x; xh[4 * i + 1] = w.y; xh[4 * i + 2] = w.z; xh[4 * i + 3] = w.w;
+                xs[4 * i] = u.x; xs[4 * i + 1] = u.y; xs[4 * i + 2] = u.z; xs[4 * i + 3] = u.w;
             }
-            split_pack32(x, hi, lo);
-            tmem_st32(tmem + trow + C_HT + 32 * hh, hi);
-            tmem_st32(tmem + trow + C_HT + 64 + 32 * hh, lo);
+            float hd = 0.f;
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const float4 w = reinterpret_cast<const float4 *>(dr)[i];
-                x[4 * i] = w.x; x[4 * i + 1] = w.y; x[4 * i + 2] = w.z; x[4 * i + 3] = w.w;
-            }
-            split_pack32(x, hi, lo);
-            tmem_st32(tmem + trow + C_KS + 32 * hh, hi);
-            tmem_st32(tmem + trow + C_KS + 64 + 32 * hh, lo);
+            for (int i = 0; i < 32; ++i) hd = fmaf(xh[i], xs[i], hd);
+#pragma unroll
+            for (int o = 16; o >= 1; o >>= 1) hd += __shfl_xor_sync(0xffffffffu, hd, o);
+            if (lane == 0) sH[warp] += hd;
+            uint32_t hi[16], lo[16];
+            split_pack16(xh, hi, lo);
+            tmem_st16(tmem + trow + C_HT + 16 * hh, hi);
+            tmem_st16(tmem + trow + C_HT + 64 + 16 * hh, lo);
+            split_pack16(xs, hi, lo);
+            tmem_st16(tmem + trow + C_KS + 16 * hh, hi);
+            tmem_st16(tmem + trow + C_KS + 64 + 16 * hh, lo);
             tmem_wait_st();
         }
         __syncthreads();
-        // per-row results of this head: dbeta and dg (reverse cumsum of dgam inside the chunk)
-        if (t == 0) {
+        // per-row results of this head (warp 0; lane holds rows lane and lane + 32): dbeta, and dg as
+        // the reverse cumsum of dgam inside the chunk
+        if (warp == 0) {
             float hd = 0.f, sf = 0.f;
-            for (int w = 0; w < 8; ++w) {
+#pragma unroll
+            for (int w = 0; w < NW; ++w) {
                 hd += sH[w];
                 sf += sF[w];
             }
-            float acc = 0.f;
-            for (int r = n - 1; r >= 0; --r) {
+            float dgv[2], dbv[2];
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                const int r = lane + 32 * hf;
                 float dgr = 0.f, dbr = 0.f;
-                for (int w = 0; w < 8; ++w) {
+#pragma unroll
+                for (int w = 0; w < NW; ++w) {
                     dgr += rdg_all[64 * w + r];
                     dbr += rdb_all[64 * w + r];
                 }
                 if (r == n - 1) dgr += Gm[n - 1] * hd + sf;
-                acc += dgr;
-                const size_t gi = (size_t)(tok0 + r) * p.Hv + hv;
-                a.dg[gi] = acc;
-                a.dbeta[gi] = dbr;
+                dgv[hf] = r < n ? dgr : 0.f;
+                dbv[hf] = dbr;
+            }
+            // suffix sums within each half, then the upper half's total is added to the lower half
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf)
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const float y = __shfl_down_sync(0xffffffffu, dgv[hf], o);
+                    if (lane + o < 32) dgv[hf] += y;
+                }
+            dgv[0] += __shfl_sync(0xffffffffu, dgv[1], 0);
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                const int r = lane + 32 * hf;
+                if (r < n) {
+                    const size_t gi = (size_t)(tok0 + r) * p.Hv + hv;
+                    a.dg[gi] = dgv[hf];
+                    a.dbeta[gi] = dbv[hf];
+                }
             }
         }
         // ---------------------------------------------------------------- P6: dq^T, dk^T accumulation
@@ -622,27 +656,27 @@ k_tc_bwd_intra(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         }
         mma_sync();
     }
-    // ---------------------------------------------------------------- dq, dk out (thread: key lrow, rows 32 hh + j)
+    // ---------------------------------------------------------------- dq, dk out (thread: key lrow, rows 16 hh + j)
     if (ok) {
-        uint32_t d[32];
+        uint32_t d[16];
         uint16_t *dqp = reinterpret_cast<uint16_t *>(a.dq) + (size_t)hq * DK + lrow;
         uint16_t *dkp = reinterpret_cast<uint16_t *>(a.dk) + (size_t)hq * DK + lrow;
         const size_t rs = (size_t)p.Hq * DK;
-        tmem_ld32(tmem + trow + C_DQ + 32 * hh, d);
+        tmem_ld16(tmem + trow + C_DQ + 16 * hh, d);
         tmem_wait_ld();
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-            const int r = 32 * hh + j;
+        for (int j = 0; j < 16; ++j) {
+            const int r = 16 * hh + j;
             if (r < n) {
                 __nv_bfloat16 b = __float2bfloat16_rn(__uint_as_float(d[j]));
                 dqp[(size_t)(tok0 + r) * rs] = *reinterpret_cast<uint16_t *>(&b);
             }
         }
-        tmem_ld32(tmem + trow + C_DK + 32 * hh, d);
+        tmem_ld16(tmem + trow + C_DK + 16 * hh, d);
         tmem_wait_ld();
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-            const int r = 32 * hh + j;
+        for (int j = 0; j < 16; ++j) {
+            const int r = 16 * hh + j;
             if (r < n) {
                 __nv_bfloat16 b = __float2bfloat16_rn(__uint_as_float(d[j]));
                 dkp[(size_t)(tok0 + r) * rs] = *reinterpret_cast<uint16_t *>(&b);
@@ -671,15 +705,14 @@ cudaError_t launch_tc_bwd_intra(const Plan &p, const void *q, const void *k, con
                                 const float *g_cum, const float *beta, const float *A32, const float *P32,
                                 const float *hbuf, const float *dSe, void *dq, void *dk, void *dv, float *dbeta,
                                 float *dg, cudaStream_t st) {
-    CUtensorMap tk, tq, tdo;
-    if (!make_head_map(&tk, k, p.Hq, p) || !make_head_map(&tq, q, p.Hq, p) || !make_head_map(&tdo, d_o, p.Hv, p))
+    CUtensorMap tk, tq, tdo, tv;
+    if (!make_head_map(&tk, k, p.Hq, p) || !make_head_map(&tq, q, p.Hq, p) || !make_head_map(&tdo, d_o, p.Hv, p) ||
+        !make_head_map(&tv, v, p.Hv, p))
         return cudaErrorInvalidValue;
     cudaError_t e =
         cudaFuncSetAttribute(k_tc_bwd_intra, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
     if (e != cudaSuccess) return e;
     IntraArgs a;
-    a.v = static_cast<const __nv_bfloat16 *>(v);
-    a.d_o = static_cast<const __nv_bfloat16 *>(d_o);
     a.g_cum = g_cum;
     a.beta = beta;
     a.A32 = A32;
@@ -692,7 +725,7 @@ cudaError_t launch_tc_bwd_intra(const Plan &p, const void *q, const void *k, con
     a.dbeta = dbeta;
     a.dg = dg;
     dim3 grid(p.total_chunks, p.Hq);
-    k_tc_bwd_intra<<<grid, NT, SMEM_BYTES, st>>>(tk, tq, tdo, p, a);
+    k_tc_bwd_intra<<<grid, NT, SMEM_BYTES, st>>>(tk, tq, tdo, tv, p, a);
     return cudaGetLastError();
 }
 
