@@ -226,6 +226,25 @@ __device__ __forceinline__ void mma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem, ui
         "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
+// A chain of NK MMAs accumulating over K steps.  Descriptors advance by compile-time steps in
+// 16-byte units (K-major 16-element step: 2; MN-major 16-row step: 128), so issuing one MMA costs
+// a few instructions; acc_first says whether the first MMA adds to D.
+template <int NK, int ASTEP, int BSTEP>
+__device__ __forceinline__ void mma_chain(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                          uint32_t acc_first) {
+#pragma unroll
+    for (int j = 0; j < NK; ++j)
+        mma_bf16(d_tmem, adesc + (uint64_t)(j * ASTEP), bdesc + (uint64_t)(j * BSTEP), idesc, j ? 1u : acc_first);
+}
+// The same with A in TMEM (8 columns per 16-element K step).
+template <int NK, int BSTEP>
+__device__ __forceinline__ void mma_chain_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                             uint32_t acc_first) {
+#pragma unroll
+    for (int j = 0; j < NK; ++j)
+        mma_bf16_ta(d_tmem, a_tmem + 8u * j, bdesc + (uint64_t)(j * BSTEP), idesc, j ? 1u : acc_first);
+}
+
 // Packs 32 fp32 values (pairs along K) into hi / lo bf16 pair words.
 __device__ __forceinline__ void split_pack32(const float *x, uint32_t (&hi)[32], uint32_t (&lo)[32]) {
 #pragma unroll

@@ -56,6 +56,7 @@ constexpr uint32_t S_MISC = S_BAR + 16;
 constexpr uint32_t S_TOTAL = S_MISC + 16;
 constexpr uint32_t SMEM_BYTES = S_TOTAL + 1024;
 static_assert(SMEM_BYTES <= 232448, "shared memory");
+static_assert(S_F + 2048 * NW <= S_VEC, "transpose buffers fit in the fp32 scratch");
 
 // TMEM columns
 constexpr uint32_t C_DQ = 0, C_DK = 64, C_HT = 128, C_KS = 256, C_QS = 320, C_DL = 384, C_DR = 448;
@@ -64,6 +65,8 @@ constexpr uint32_t ID_KK = idesc_bf16(128, 64, 0, 0);
 constexpr uint32_t ID_MK = idesc_bf16(128, 64, 1, 0);
 constexpr uint32_t ID_MM = idesc_bf16(128, 64, 1, 1);
 constexpr uint32_t ID_KM = idesc_bf16(128, 64, 0, 1);
+constexpr uint32_t ID_N128 = idesc_bf16(128, 128, 0, 0);
+static_assert(C_QS == C_KS + 64, "KS and QS accumulators must be adjacent");
 
 struct IntraArgs {
     const float *g_cum, *beta, *A32, *P32, *hbuf, *dSe;
@@ -114,6 +117,65 @@ __device__ __forceinline__ float tile128_at(const unsigned char *sm, uint32_t of
     return tile_at(sm, off + (uint32_t)(v >> 6) * 8192u, row, v & 63);
 }
 
+// dq^T, dk^T accumulation of one value head (issued by one thread).  A separate, non-inlined
+// function keeps the issue sequence compact and out of the kernel's register pressure.
+__device__ __noinline__ void issue_dq_dk(uint32_t sb, uint32_t tmem, uint32_t acc0) {
+        for (int tt = 0; tt < 3; ++tt)  // dq^T += h (scale Gam dO)^T
+            for (int blk = 0; blk < 2; ++blk)
+                mma_chain_ta<4, 2>(tmem + C_DQ, tmem + C_HT + (tt == 2 ? 64 : 0) + 32 * blk,
+                                   kdesc(sb + S_DD + (tt == 1 ? 16384 : 0) + 8192 * blk), ID_KK,
+                                   acc0 | (uint32_t)((tt | blk) != 0));
+        for (int sp = 0; sp < 2; ++sp)  // dq^T += K^T dQK^T
+            mma_chain<4, 128, 2>(tmem + C_DQ, mdesc(sb + S_KQ, 16384), kdesc(sb + S_DO + 8192 * sp), ID_MK, 1);
+        // dk^T += dSe (E Dl)^T
+        mma_chain_ta<8, 128>(tmem + C_DK, tmem + C_KS, mdesc(sb + S_DR, 8192), ID_KM, acc0);
+        mma_chain_ta<8, 128>(tmem + C_DK, tmem + C_KS, mdesc(sb + S_DR + 32768, 8192), ID_KM, 1);
+        mma_chain_ta<8, 128>(tmem + C_DK, tmem + C_KS + 64, mdesc(sb + S_DR, 8192), ID_KM, 1);
+        // dk^T += h Y^T, Y = -beta Gam dR
+        mma_chain_ta<8, 128>(tmem + C_DK, tmem + C_HT, mdesc(sb + S_DR + 16384, 8192), ID_KM, 1);
+        mma_chain_ta<8, 128>(tmem + C_DK, tmem + C_HT, mdesc(sb + S_DR + 49152, 8192), ID_KM, 1);
+        mma_chain_ta<8, 128>(tmem + C_DK, tmem + C_HT + 64, mdesc(sb + S_DR + 16384, 8192), ID_KM, 1);
+        for (int sp = 0; sp < 2; ++sp) {
+            // dk^T += Q^T dQK
+            mma_chain<4, 128, 128>(tmem + C_DK, mdesc(sb + S_KQ + 8192, 16384), mdesc(sb + S_DO + 8192 * sp, 8192),
+                                   ID_MM, 1);
+            // dk^T += K^T (dKK + dKK^T)
+            mma_chain<4, 128, 128>(tmem + C_DK, mdesc(sb + S_KQ, 16384), mdesc(sb + S_P + 8192 * sp, 8192),
+                                   ID_MM, 1);
+        }
+        }
+
+// Row k = lane of a 32 x 32 fp32 block (row stride 128 floats) into x[32]: coalesced loads of 4 rows
+// of 128 bytes per instruction, transposed through the warp's 2 KB swizzled buffer at tb, 16 rows
+// at a time.
+__device__ __forceinline__ void key_rows(const float *__restrict__ src, uint32_t tb, float (&x)[32]) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int rr = 4 * j + (lane >> 3), c = lane & 7;
+            const float4 w = __ldg(reinterpret_cast<const float4 *>(src + (size_t)(16 * hf + rr) * 128 + 4 * c));
+            st_shared_v4(tb + rr * 128 + ((c ^ (rr & 7)) << 4), __float_as_uint(w.x), __float_as_uint(w.y),
+                         __float_as_uint(w.z), __float_as_uint(w.w));
+        }
+        __syncwarp();
+        const int rr = lane & 15;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            uint32_t v0, v1, v2, v3;
+            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(v0), "=r"(v1), "=r"(v2), "=r"(v3)
+                         : "r"(tb + rr * 128 + ((c ^ (rr & 7)) << 4)));
+            if ((lane >> 4) == hf) {
+                x[4 * c] = __uint_as_float(v0); x[4 * c + 1] = __uint_as_float(v1);
+                x[4 * c + 2] = __uint_as_float(v2); x[4 * c + 3] = __uint_as_float(v3);
+            }
+        }
+        __syncwarp();
+    }
+}
+
 __global__ void __launch_bounds__(NT, 1)
 k_tc_bwd_intra(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
                const __grid_constant__ CUtensorMap tm_do, const __grid_constant__ CUtensorMap tm_v, Plan p,
@@ -155,10 +217,16 @@ k_tc_bwd_intra(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     uint32_t tma_ph = 0, mma_ph = 0, tma_issued = 0;
     bool ok = true;
 
-    // waits for the MMAs issued so far by thread 0 (which commits first)
+    // Waits for the MMAs issued so far by thread 0 (which commits first).  Only warp 0 polls the
+    // mbarrier; the other warps block in the CTA barrier, so no polling competes with the tensor
+    // core for shared memory while the MMAs run.
     auto mma_sync = [&]() {
-        if (t == 0) mma_commit(bar_mma);
-        bool w = mbar_wait(bar_mma, mma_ph & 1, abort_flag);
+        bool w = true;
+        if (warp == 0) {
+            if (lane == 0) mma_commit(bar_mma);
+            __syncwarp();
+            w = mbar_wait_warp(bar_mma, mma_ph & 1, abort_flag);
+        }
         ++mma_ph;
         ok = __syncthreads_and(w && ok) != 0;
         tc_fence_after();
@@ -171,7 +239,8 @@ k_tc_bwd_intra(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         tc_fence_after();
     };
     auto tma_wait = [&]() {
-        bool w = mbar_wait(bar_tma, tma_ph & 1, abort_flag);
+        bool w = true;
+        if (warp == 0) w = mbar_wait_warp(bar_tma, tma_ph & 1, abort_flag);
         ++tma_ph;
         ok = __syncthreads_and(w && ok) != 0;
     };
@@ -185,6 +254,7 @@ k_tc_bwd_intra(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         tma_load_3d(sb + S_KQ + 24576, &tm_q, bar_tma, 64, hq, tok0);
     }
     tma_wait();
+
 
     for (int g = 0; ok && g < p.G; ++g) {
         const int hv = hq * p.G + g;
@@ -226,11 +296,11 @@ k_tc_bwd_intra(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         // ---------------------------------------------------------------- P1: h^T (lane v) -> TMEM; KS, QS
         {
             const float *hc = a.hbuf + st_off + (size_t)(32 * hh) * DV + lrow;
-            float x[32];
+            float xh[32];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) x[i] = hc[(size_t)i * DV];
+            for (int i = 0; i < 32; ++i) xh[i] = hc[(size_t)i * DV];
             uint32_t hi[16], lo[16];
-            split_pack16(x, hi, lo);
+            split_pack16(xh, hi, lo);
             tmem_st16(tmem + trow + C_HT + 16 * hh, hi);
             tmem_st16(tmem + trow + C_HT + 64 + 16 * hh, lo);
             tmem_wait_st();
@@ -238,12 +308,12 @@ k_tc_bwd_intra(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         __syncthreads();  // vectors visible
         pre_mma();
         if (t == 0) {
+            // [KS^T | QS^T] = h^T [K; Q]^T: one N = 128 product (K and Q rows are adjacent, as are the
+            // two accumulators)
             for (int sp = 0; sp < 2; ++sp)
-                for (int kk = 0; kk < 8; ++kk) {
-                    const uint32_t bo = sb + S_KQ + (kk >> 2) * 16384 + (kk & 3) * 32;
-                    mma_bf16_ta(tmem + C_KS, tmem + C_HT + 64 * sp + 8 * kk, kdesc(bo), ID_KK, (sp | kk) != 0);
-                    mma_bf16_ta(tmem + C_QS, tmem + C_HT + 64 * sp + 8 * kk, kdesc(bo + 8192), ID_KK, (sp | kk) != 0);
-                }
+                for (int blk = 0; blk < 2; ++blk)
+                    mma_chain_ta<4, 2>(tmem + C_KS, tmem + C_HT + 64 * sp + 32 * blk, kdesc(sb + S_KQ + 16384 * blk),
+                                       ID_N128, (sp | blk) != 0);
         }
         // dSe^T (lane v) loads overlap the MMAs; stored to TMEM once h^T has been consumed
         float xd[32];
@@ -295,18 +365,17 @@ k_tc_bwd_intra(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         }
         pre_mma();
         if (t == 0) {
-            for (int tt = 0; tt < 3; ++tt)  // Dl^T = R^T A^T
-                for (int kk = 0; kk < 4; ++kk)
-                    mma_bf16(tmem + C_DL, kdesc(sb + S_DR + 16384 + (tt == 2 ? 32768 : 0) + kk * 32),
-                             kdesc(sb + S_A + (tt == 1 ? 8192 : 0) + kk * 32), ID_KK, (tt | kk) != 0);
+            // Dl^T = R^T A^T (hi hi, hi lo, lo hi)
+            mma_chain<4, 2, 2>(tmem + C_DL, kdesc(sb + S_DR + 16384), kdesc(sb + S_A), ID_KK, 0);
+            mma_chain<4, 2, 2>(tmem + C_DL, kdesc(sb + S_DR + 16384), kdesc(sb + S_A + 8192), ID_KK, 1);
+            mma_chain<4, 2, 2>(tmem + C_DL, kdesc(sb + S_DR + 49152), kdesc(sb + S_A), ID_KK, 1);
             for (int sp = 0; sp < 2; ++sp)  // KdS^T = dSe^T K^T
-                for (int kk = 0; kk < 8; ++kk)
-                    mma_bf16_ta(tmem + C_KS, tmem + C_HT + 64 * sp + 8 * kk,
-                                kdesc(sb + S_KQ + (kk >> 2) * 16384 + (kk & 3) * 32), ID_KK, (sp | kk) != 0);
+                for (int blk = 0; blk < 2; ++blk)
+                    mma_chain_ta<4, 2>(tmem + C_KS, tmem + C_HT + 64 * sp + 32 * blk, kdesc(sb + S_KQ + 16384 * blk),
+                                       ID_KK, (sp | blk) != 0);
             for (int sp = 0; sp < 2; ++sp)  // PdO^T = dO^T P
-                for (int kk = 0; kk < 4; ++kk)
-                    mma_bf16(tmem + C_QS, mdesc(sb + S_DO + kk * 2048, 8192),
-                             mdesc(sb + S_P + 8192 * sp + kk * 2048, 8192), ID_MM, (sp | kk) != 0);
+                mma_chain<4, 128, 128>(tmem + C_QS, mdesc(sb + S_DO, 8192), mdesc(sb + S_P + 8192 * sp, 8192), ID_MM,
+                                       sp);
         }
         mma_sync();
         if (!ok) break;
@@ -340,18 +409,18 @@ k_tc_bwd_intra(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         }
         pre_mma();
         if (t == 0) {
-            for (int tt = 0; tt < 3; ++tt)  // dR^T = dDl^T A  (A read MN-major)
-                for (int kk = 0; kk < 4; ++kk)
-                    mma_bf16(tmem + C_DR, kdesc(sb + S_DD + (tt == 2 ? 16384 : 0) + kk * 32),
-                             mdesc(sb + S_A + (tt == 1 ? 8192 : 0) + kk * 2048, 8192), ID_KM, (tt | kk) != 0);
+            // dR^T = dDl^T A  (A read MN-major)
+            mma_chain<4, 2, 128>(tmem + C_DR, kdesc(sb + S_DD), mdesc(sb + S_A, 8192), ID_KM, 0);
+            mma_chain<4, 2, 128>(tmem + C_DR, kdesc(sb + S_DD), mdesc(sb + S_A + 8192, 8192), ID_KM, 1);
+            mma_chain<4, 2, 128>(tmem + C_DR, kdesc(sb + S_DD + 16384), mdesc(sb + S_A, 8192), ID_KM, 1);
             for (int sp = 0; sp < 2; ++sp)  // [Dl; R] dO^T  -> dP^T in lanes 0..63
-                for (int kk = 0; kk < 8; ++kk)
-                    mma_bf16(tmem + C_KS, mdesc(sb + S_DR + 32768 * sp + kk * 2048, 16384),
-                             kdesc(sb + S_DO + (kk >> 2) * 8192 + (kk & 3) * 32), ID_MK, (sp | kk) != 0);
-            for (int tt = 0; tt < 3; ++tt)  // [Dl; R] dDl^T -> dA^T in lanes 64..127
-                for (int kk = 0; kk < 8; ++kk)
-                    mma_bf16(tmem + C_QS, mdesc(sb + S_DR + (tt == 2 ? 32768 : 0) + kk * 2048, 16384),
-                             mdesc(sb + S_DD + (tt == 1 ? 16384 : 0) + kk * 2048, 8192), ID_MM, (tt | kk) != 0);
+                for (int blk = 0; blk < 2; ++blk)
+                    mma_chain<4, 128, 2>(tmem + C_KS, mdesc(sb + S_DR + 32768 * sp + 8192 * blk, 16384),
+                                         kdesc(sb + S_DO + 8192 * blk), ID_MK, (sp | blk) != 0);
+            // [Dl; R] dDl^T -> dA^T in lanes 64..127
+            mma_chain<8, 128, 128>(tmem + C_QS, mdesc(sb + S_DR, 16384), mdesc(sb + S_DD, 8192), ID_MM, 0);
+            mma_chain<8, 128, 128>(tmem + C_QS, mdesc(sb + S_DR, 16384), mdesc(sb + S_DD + 16384, 8192), ID_MM, 1);
+            mma_chain<8, 128, 128>(tmem + C_QS, mdesc(sb + S_DR + 32768, 16384), mdesc(sb + S_DD, 8192), ID_MM, 1);
         }
         mma_sync();
         if (!ok) break;
@@ -470,11 +539,11 @@ k_tc_bwd_intra(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
             st_split_chunk(sb + S_P, sb + S_P + 8192, r, ch, x8);
         }
         pre_mma();
-        if (t == 0)
-            for (int tt = 0; tt < 3; ++tt)  // Z^T[i][k] = sum_l A[i][l] dA~[k][l]
-                for (int kk = 0; kk < 4; ++kk)
-                    mma_bf16(tmem + C_KS, kdesc(sb + S_A + (tt == 2 ? 8192 : 0) + kk * 32),
-                             kdesc(sb + S_P + (tt == 1 ? 8192 : 0) + kk * 32), ID_KK, (tt | kk) != 0);
+        if (t == 0) {  // Z^T[i][k] = sum_l A[i][l] dA~[k][l]
+            mma_chain<4, 2, 2>(tmem + C_KS, kdesc(sb + S_A), kdesc(sb + S_P), ID_KK, 0);
+            mma_chain<4, 2, 2>(tmem + C_KS, kdesc(sb + S_A), kdesc(sb + S_P + 8192), ID_KK, 1);
+            mma_chain<4, 2, 2>(tmem + C_KS, kdesc(sb + S_A + 8192), kdesc(sb + S_P), ID_KK, 1);
+        }
         mma_sync();
         if (!ok) break;
         if (lq < 2) {  // Z^T rows (lanes 0..63) -> hi / lo bf16 A operand in TMEM
@@ -494,11 +563,11 @@ k_tc_bwd_intra(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
             tmem_wait_st();
         }
         pre_mma();
-        if (t == 0)
-            for (int tt = 0; tt < 3; ++tt)  // (A^T Z)^T[i][r] = sum_k Z^T[i][k] A[k][r]   (A read MN-major)
-                for (int kk = 0; kk < 4; ++kk)
-                    mma_bf16_ta(tmem + C_KS, tmem + C_QS + (tt == 2 ? 32 : 0) + 8 * kk,
-                                mdesc(sb + S_A + (tt == 1 ? 8192 : 0) + kk * 2048, 8192), ID_KM, (tt | kk) != 0);
+        if (t == 0) {  // (A^T Z)^T[i][r] = sum_k Z^T[i][k] A[k][r]   (A read MN-major)
+            mma_chain_ta<4, 128>(tmem + C_KS, tmem + C_QS, mdesc(sb + S_A, 8192), ID_KM, 0);
+            mma_chain_ta<4, 128>(tmem + C_KS, tmem + C_QS, mdesc(sb + S_A + 8192, 8192), ID_KM, 1);
+            mma_chain_ta<4, 128>(tmem + C_KS, tmem + C_QS + 32, mdesc(sb + S_A, 8192), ID_KM, 1);
+        }
         mma_sync();
         if (!ok) break;
         if (lq < 2) {  // Fa[r][i] = dL[r][i] = -(A^T Z)[r][i]
@@ -513,10 +582,9 @@ k_tc_bwd_intra(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         // K K^T for the beta and gate terms of dL (lanes 0..63 of a [K; Q] K^T product)
         pre_mma();
         if (t == 0)
-            for (int kk = 0; kk < 8; ++kk) {
-                const uint32_t off = sb + S_KQ + (kk >> 2) * 16384 + (kk & 3) * 32;
-                mma_bf16(tmem + C_KS, kdesc(off), kdesc(off), ID_KK, kk);
-            }
+            for (int blk = 0; blk < 2; ++blk)
+                mma_chain<4, 2, 2>(tmem + C_KS, kdesc(sb + S_KQ + 16384 * blk), kdesc(sb + S_KQ + 16384 * blk), ID_KK,
+                                   blk);
         mma_sync();
         if (!ok) break;
         if (lq < 2) {  // thread: row r = lrow, columns i = 16 hh + j
@@ -554,30 +622,40 @@ k_tc_bwd_intra(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         tc_fence_before();  // every K K^T load is done before the columns are overwritten
         __syncthreads();
         tc_fence_after();
-        // h and dSe (lane = key) -> TMEM as A operands of the dq / dk products; <h, dSe> partial
+        // h and dSe (lane = key) -> TMEM as A operands of the dq / dk products.
+        // The warp's 32 x 32 blocks are read with coalesced row loads (4 rows of 128 bytes per
+        // instruction) and transposed through a private 2 KB swizzled buffer in the fp32 scratch
+        // region (free since the dKK tile), 16 rows at a time.
         {
-            const float4 *hr = reinterpret_cast<const float4 *>(a.hbuf + st_off + (size_t)lrow * DV + 32 * hh);
-            const float4 *dr = reinterpret_cast<const float4 *>(a.dSe + st_off + (size_t)lrow * DV + 32 * hh);
-            float xh[32], xs[32];
+            const uint32_t tb = sb + S_F + 2048u * (uint32_t)warp;
+            {
+                float x[32];
+                uint32_t hi[16], lo[16];
+                key_rows(a.hbuf + st_off + (size_t)(32 * lq) * DV + 32 * hh, tb, x);
+                split_pack16(x, hi, lo);
+                tmem_st16(tmem + trow + C_HT + 16 * hh, hi);
+                tmem_st16(tmem + trow + C_HT + 64 + 16 * hh, lo);
+                key_rows(a.dSe + st_off + (size_t)(32 * lq) * DV + 32 * hh, tb, x);
+                {  // <h, dSe> partial: h read back from its hi / lo TMEM pair (about 16 significant bits)
+                    uint32_t h2[16], l2[16];
+                    tmem_wait_st();
+                    tmem_ld16(tmem + trow + C_HT + 16 * hh, h2);
+                    tmem_ld16(tmem + trow + C_HT + 64 + 16 * hh, l2);
+                    tmem_wait_ld();
+                    float hd = 0.f;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const float4 w = hr[i], u = dr[i];
-                xh[4 * i] = w.x; xh[4 * i + 1] = w.y; xh[4 * i + 2] = w.z; xh[4 * i + 3] = w.w;
-                xs[4 * i] = u.x; xs[4 * i + 1] = u.y; xs[4 * i + 2] = u.z; xs[4 * i + 3] = u.w;
+                    for (int i = 0; i < 16; ++i) {
+                        hd = fmaf(bf16_lo_f(h2[i]) + bf16_lo_f(l2[i]), x[2 * i], hd);
+                        hd = fmaf(bf16_hi_f(h2[i]) + bf16_hi_f(l2[i]), x[2 * i + 1], hd);
+                    }
+#pragma unroll
+                    for (int o = 16; o >= 1; o >>= 1) hd += __shfl_xor_sync(0xffffffffu, hd, o);
+                    if (lane == 0) sH[warp] = hd;
+                }
+                split_pack16(x, hi, lo);
+                tmem_st16(tmem + trow + C_KS + 16 * hh, hi);
+                tmem_st16(tmem + trow + C_KS + 64 + 16 * hh, lo);
             }
-            float hd = 0.f;
-#pragma unroll
-            for (int i = 0; i < 32; ++i) hd = fmaf(xh[i], xs[i], hd);
-#pragma unroll
-            for (int o = 16; o >= 1; o >>= 1) hd += __shfl_xor_sync(0xffffffffu, hd, o);
-            if (lane == 0) sH[warp] += hd;
-            uint32_t hi[16], lo[16];
-            split_pack16(xh, hi, lo);
-            tmem_st16(tmem + trow + C_HT + 16 * hh, hi);
-            tmem_st16(tmem + trow + C_HT + 64 + 16 * hh, lo);
-            split_pack16(xs, hi, lo);
-            tmem_st16(tmem + trow + C_KS + 16 * hh, hi);
-            tmem_st16(tmem + trow + C_KS + 64 + 16 * hh, lo);
             tmem_wait_st();
         }
         __syncthreads();
@@ -625,35 +703,7 @@ k_tc_bwd_intra(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         }
         // ---------------------------------------------------------------- P6: dq^T, dk^T accumulation
         pre_mma();
-        if (t == 0) {
-            const uint32_t acc0 = (g != 0);
-            for (int tt = 0; tt < 3; ++tt)  // dq^T += h (scale Gam dO)^T
-                for (int kk = 0; kk < 8; ++kk)
-                    mma_bf16_ta(tmem + C_DQ, tmem + C_HT + (tt == 2 ? 64 : 0) + 8 * kk,
-                                kdesc(sb + S_DD + (tt == 1 ? 16384 : 0) + (kk >> 2) * 8192 + (kk & 3) * 32), ID_KK,
-                                acc0 | (uint32_t)(tt | kk));
-            for (int sp = 0; sp < 2; ++sp)  // dq^T += K^T dQK^T
-                for (int kk = 0; kk < 4; ++kk)
-                    mma_bf16(tmem + C_DQ, mdesc(sb + S_KQ + kk * 2048, 16384),
-                             kdesc(sb + S_DO + 8192 * sp + kk * 32), ID_MK, 1);
-            for (int tt = 0; tt < 3; ++tt)  // dk^T += dSe (E Dl)^T
-                for (int kk = 0; kk < 8; ++kk)
-                    mma_bf16_ta(tmem + C_DK, tmem + C_KS + (tt == 2 ? 64 : 0) + 8 * kk,
-                                mdesc(sb + S_DR + (tt == 1 ? 32768 : 0) + kk * 2048, 8192), ID_KM,
-                                acc0 | (uint32_t)(tt | kk));
-            for (int tt = 0; tt < 3; ++tt)  // dk^T += h Y^T, Y = -beta Gam dR
-                for (int kk = 0; kk < 8; ++kk)
-                    mma_bf16_ta(tmem + C_DK, tmem + C_HT + (tt == 2 ? 64 : 0) + 8 * kk,
-                                mdesc(sb + S_DR + 16384 + (tt == 1 ? 32768 : 0) + kk * 2048, 8192), ID_KM, 1);
-            for (int sp = 0; sp < 2; ++sp)  // dk^T += Q^T dQK
-                for (int kk = 0; kk < 4; ++kk)
-                    mma_bf16(tmem + C_DK, mdesc(sb + S_KQ + 8192 + kk * 2048, 16384),
-                             mdesc(sb + S_DO + 8192 * sp + kk * 2048, 8192), ID_MM, 1);
-            for (int sp = 0; sp < 2; ++sp)  // dk^T += K^T (dKK + dKK^T)
-                for (int kk = 0; kk < 4; ++kk)
-                    mma_bf16(tmem + C_DK, mdesc(sb + S_KQ + kk * 2048, 16384),
-                             mdesc(sb + S_P + 8192 * sp + kk * 2048, 8192), ID_MM, 1);
-        }
+        if (t == 0) issue_dq_dk(sb, tmem, g != 0);
         mma_sync();
     }
     // ---------------------------------------------------------------- dq, dk out (thread: key lrow, rows 16 hh + j)
