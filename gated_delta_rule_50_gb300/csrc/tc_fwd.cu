@@ -8,7 +8,7 @@
 // S^T[v][:] in registers.  Per chunk (n <= 64 rows, entry state S):
 //
 //   D1   = [K; Q] K^T                  -> K K^T, Q K^T            (exact bf16 operands)
-//   KS^T = S^T K^T,  QS^T = S^T Q^T                               (S split hi + lo)
+//   KS^T = S^T K^T,  QS^T = S^T Q^T                               (S split hi + lo, from TMEM)
 //   R^T  = (V - diag(Gam) K S)^T diag(beta)                        (CUDA cores)
 //   Dl^T = R^T A^T                                                 (R, A split; 3 products)
 //   U^T  = (diag(E) Dl)^T K          (K read MN-major)             (E Dl split)
@@ -24,11 +24,13 @@
 // same Dl is formed as A R, which needs neither W nor U.
 //
 // Warp roles (448 threads):
-//   warp 0      TMA producer: k and q chunk tiles (128-byte swizzle), 2 stages
+//   warp 0      TMA producer: k, q and v chunk tiles (128-byte swizzle), 2 stages
 //   warp 1      TMEM allocator and single-thread MMA issuer
 //   warps 2-5   prep: gate cumsum, L, A = (I + L)^{-1} (blocked, in place), P;
 //               runs one chunk ahead of the state chain; writes g_cum and A
-//   warps 6-13  state: S in registers, R, E Dl, state update, o epilogue
+//   warps 6-13  state: S in registers (written to TMEM as the A operand of the
+//               KS / QS products), R, E Dl, state update, o epilogue (staged in
+//               the consumed v tile, written with 16-byte stores)
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -48,7 +50,9 @@ constexpr int W_TMA = 0, W_MMA = 1, W_PREP0 = 2, W_STATE0 = 6;
 // shared memory map (bytes from a 1024-aligned base)
 constexpr uint32_t SM_KQ = 0;             // 2 stages x [kb0: K 8K, Q 8K][kb1: K 8K, Q 8K]
 constexpr uint32_t KQ_STAGE = 32768;
-constexpr uint32_t SM_SS = 65536;         // S^T hi / lo [128 v][128 keys]; later E Dl hi / lo [128 v][64 c]
+constexpr uint32_t SM_V = 65536;          // 2 stages x V [64 rows][2 x 64 v] (TMA); then o staging [64][128] bf16
+constexpr uint32_t V_STAGE = 16384;
+constexpr uint32_t SM_ED = 98304;         // (E Dl)^T hi / lo [128 v][64 c]
 constexpr uint32_t SM_RT = 131072;        // R^T hi / lo [128 v][64 c]; later Dl^T hi / lo
 constexpr uint32_t SM_AHL = 163840;       // A hi / lo [64][64]
 constexpr uint32_t SM_PHL = 180224;       // P hi / lo [64][64]
@@ -60,12 +64,14 @@ constexpr uint32_t SM_MISC = SM_BAR + 32 * 8;         // tmem base, abort flag, 
 constexpr uint32_t SM_TOTAL = SM_MISC + 64;
 constexpr uint32_t SMEM_BYTES = SM_TOTAL + 1024;
 
-// TMEM columns (512 allocated)
-constexpr uint32_t TM_D1 = 0, TM_KS = 64, TM_DL = 128, TM_U = 64, TM_QS = 192, TM_O = 320;
+// TMEM columns (512 allocated): S^T hi / lo are bf16 pairs along the keys (A operand)
+constexpr uint32_t TM_D1 = 0, TM_KS = 64, TM_DL = 128, TM_U = 64, TM_QS = 192, TM_O = 320, TM_SH = 384,
+                   TM_SL = 448;
 
 enum {
     B_FULL0 = 0, B_FULL1, B_EMPTY0, B_EMPTY1, B_D1FULL, B_D1FREE, B_SSREADY, B_KSDONE, B_RTREADY, B_AREADY,
-    B_DLDONE, B_EDREADY, B_PREADY, B_UPDDONE, B_ODONE, B_EPIFREE0, B_EPIFREE1, B_FINAL, B_COUNT
+    B_DLDONE, B_EDREADY, B_PREADY, B_UPDDONE, B_ODONE, B_EPIFREE0, B_EPIFREE1, B_FINAL, B_VFULL0, B_VFULL1,
+    B_VEMPTY0, B_VEMPTY1, B_STAGED0, B_STAGED1, B_COUNT
 };
 
 constexpr uint32_t ID_N64 = idesc_bf16(128, 64, 0, 0);
@@ -94,8 +100,6 @@ __device__ void record_timeout(const Plan &p, int bar_id, int chunk) {
     }
     atomicOr(p.err, ERR_TIMEOUT);
 }
-
-__device__ __forceinline__ float bf16_bits_to_f(uint32_t b16) { return __uint_as_float(b16 << 16); }
 
 // Blocked in-place inverse of the unit lower-triangular I + L held in Lm
 // ([64][65], strictly lower part = L, rest 0); afterwards Lm = (I + L)^{-1}.
@@ -151,7 +155,8 @@ __device__ void blocked_inverse(float *Lm, float *Tb, int pt) {
 }
 
 __global__ void __launch_bounds__(NUM_THREADS, 1)
-k_tc_fwd(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q, Plan p, FwdArgs a) {
+k_tc_fwd(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
+         const __grid_constant__ CUtensorMap tm_v, Plan p, FwdArgs a) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char *sm = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                           ~uintptr_t(1023));
@@ -204,7 +209,8 @@ k_tc_fwd(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
     float *A32_out = outs ? a.A32 : nullptr, *P32_out = outs ? a.P32 : nullptr;
 
     if (threadIdx.x == 0) {
-        const uint32_t counts[B_COUNT] = {1, 1, 1, 1, 1, 128, 256, 1, 256, 128, 1, 256, 128, 1, 1, 256, 256, 1};
+        const uint32_t counts[B_COUNT] = {1, 1, 1, 1, 1, 128, 256, 1, 256, 128, 1, 256, 128, 1, 1, 256, 256, 1,
+                                          1, 1, 256, 256, 256, 256};
         for (int i = 0; i < B_COUNT; ++i) mbar_init(bar(i), counts[i]);
         misc[1] = 0;
         fence_mbar_init();
@@ -213,6 +219,7 @@ k_tc_fwd(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
     if (warp == W_TMA && lane == 0) {
         prefetch_tmap(&tm_k);
         prefetch_tmap(&tm_q);
+        prefetch_tmap(&tm_v);
     }
     tc_fence_before();
     __syncthreads();
@@ -222,7 +229,7 @@ k_tc_fwd(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
     if (warp == W_TMA) {
         // ------------------------------------------------------------------ TMA producer
         if (lane == 0) {
-            int issued = 0;
+            int issued = 0, vissued = 0;
             for (int j = 0; j < nck; ++j) {
                 const int st = j & 1;
                 if (j >= 2 && !mbar_wait(bar(B_EMPTY0 + st), ((j >> 1) - 1) & 1, abort_flag)) {
@@ -237,9 +244,20 @@ k_tc_fwd(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
                 tma_load_3d(dst + 16384, &tm_k, bar(B_FULL0 + st), 64, hq, tok0);
                 tma_load_3d(dst + 24576, &tm_q, bar(B_FULL0 + st), 64, hq, tok0);
                 issued = j + 1;
+                // v tile; its buffer last held the staged o of chunk j - 2
+                if (j >= 2 && !mbar_wait(bar(B_VEMPTY0 + st), ((j >> 1) - 1) & 1, abort_flag)) {
+                    record_timeout(p, B_VEMPTY0 + st, j);
+                    break;
+                }
+                mbar_arrive_expect_tx(bar(B_VFULL0 + st), V_STAGE);
+                tma_load_3d(sb + SM_V + st * V_STAGE, &tm_v, bar(B_VFULL0 + st), 0, hv, tok0);
+                tma_load_3d(sb + SM_V + st * V_STAGE + 8192, &tm_v, bar(B_VFULL0 + st), 64, hv, tok0);
+                vissued = j + 1;
             }
             // never leave with copies in flight
             for (int j = (issued > 2 ? issued - 2 : 0); j < issued; ++j) mbar_drain(bar(B_FULL0 + (j & 1)), (j >> 1) & 1);
+            for (int j = (vissued > 2 ? vissued - 2 : 0); j < vissued; ++j)
+                mbar_drain(bar(B_VFULL0 + (j & 1)), (j >> 1) & 1);
         }
         __syncwarp();
     } else if (warp == W_MMA) {
@@ -269,23 +287,18 @@ k_tc_fwd(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
                 const int st = j & 1, ph = j & 1;
                 if (!(ok = wait(B_SSREADY, ph, j))) break;
                 tc_fence_after();
-                for (int sp = 0; sp < 2; ++sp)  // KS^T = S^T K^T (S hi, lo)
-                    for (int kk = 0; kk < 8; ++kk) {
-                        uint32_t ao = sb + SM_SS + sp * 32768 + (kk >> 2) * 16384 + (kk & 3) * 32;
-                        uint32_t bo = kq(st) + (kk >> 2) * 16384 + (kk & 3) * 32;
-                        mma_bf16(tmem + TM_KS, sdesc_sw128(ao, 16, 1024), sdesc_sw128(bo, 16, 1024), ID_N64,
-                                 (sp | kk) != 0);
-                    }
+                for (int sp = 0; sp < 2; ++sp)  // KS^T = S^T K^T (S hi, lo from TMEM)
+                    for (int blk = 0; blk < 2; ++blk)
+                        mma_chain_ta<4, 2>(tmem + TM_KS, tmem + (sp ? TM_SL : TM_SH) + 32 * blk,
+                                           sdesc_sw128(kq(st) + blk * 16384, 16, 1024), ID_N64, (sp | blk) != 0);
                 mma_commit(bar(B_KSDONE));
                 if (j >= 2 && !(ok = wait(B_EPIFREE0 + st, ((j - 2) >> 1) & 1, j))) break;
                 tc_fence_after();
                 for (int sp = 0; sp < 2; ++sp)  // QS^T = S^T Q^T
-                    for (int kk = 0; kk < 8; ++kk) {
-                        uint32_t ao = sb + SM_SS + sp * 32768 + (kk >> 2) * 16384 + (kk & 3) * 32;
-                        uint32_t bo = kq(st) + 8192 + (kk >> 2) * 16384 + (kk & 3) * 32;
-                        mma_bf16(tmem + TM_QS + 64 * st, sdesc_sw128(ao, 16, 1024), sdesc_sw128(bo, 16, 1024),
-                                 ID_N64, (sp | kk) != 0);
-                    }
+                    for (int blk = 0; blk < 2; ++blk)
+                        mma_chain_ta<4, 2>(tmem + TM_QS + 64 * st, tmem + (sp ? TM_SL : TM_SH) + 32 * blk,
+                                           sdesc_sw128(kq(st) + 8192 + blk * 16384, 16, 1024), ID_N64,
+                                           (sp | blk) != 0);
                 if (j + 1 < nck) {  // next chunk's K K^T / Q K^T for the prep warps
                     if (!(ok = wait(B_FULL0 + (st ^ 1), ((j + 1) >> 1) & 1, j + 1))) break;
                     if (!(ok = wait(B_D1FREE, ph, j))) break;
@@ -297,31 +310,22 @@ k_tc_fwd(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
                 if (!(ok = wait(B_AREADY, ph, j))) break;
                 tc_fence_after();
                 for (int t = 0; t < 3; ++t)  // Dl^T = R^T A^T: (hi,hi) (hi,lo) (lo,hi)
-                    for (int kk = 0; kk < 4; ++kk) {
-                        uint32_t ao = sb + SM_RT + (t == 2 ? 16384 : 0) + kk * 32;
-                        uint32_t bo = sb + SM_AHL + (t == 1 ? 8192 : 0) + kk * 32;
-                        mma_bf16(tmem + TM_DL, sdesc_sw128(ao, 16, 1024), sdesc_sw128(bo, 16, 1024), ID_N64,
-                                 (t | kk) != 0);
-                    }
+                    mma_chain<4, 2, 2>(tmem + TM_DL, sdesc_sw128(sb + SM_RT + (t == 2 ? 16384 : 0), 16, 1024),
+                                       sdesc_sw128(sb + SM_AHL + (t == 1 ? 8192 : 0), 16, 1024), ID_N64, t != 0);
                 mma_commit(bar(B_DLDONE));
                 if (!(ok = wait(B_EDREADY, ph, j))) break;
                 if (!(ok = wait(B_PREADY, ph, j))) break;
                 tc_fence_after();
                 for (int sp = 0; sp < 2; ++sp)  // U^T = (E Dl)^T K, K read MN-major
-                    for (int kk = 0; kk < 4; ++kk) {
-                        uint32_t ao = sb + SM_SS + sp * 16384 + kk * 32;
-                        uint32_t bo = kq(st) + kk * 2048;
-                        mma_bf16(tmem + TM_U, sdesc_sw128(ao, 16, 1024), sdesc_sw128(bo, 16384, 1024),
-                                 ID_N128_BMN, (sp | kk) != 0);
-                    }
+                    mma_chain<4, 2, 128>(tmem + TM_U, sdesc_sw128(sb + SM_ED + sp * 16384, 16, 1024),
+                                         sdesc_sw128(kq(st), 16384, 1024), ID_N128_BMN, sp);
                 mma_commit(bar(B_UPDDONE));
+                // O (one buffer): the epilogue of chunk j - 1 has read it
+                if (j >= 1 && !(ok = wait(B_EPIFREE0 + ((j - 1) & 1), ((j - 1) >> 1) & 1, j))) break;
+                tc_fence_after();
                 for (int t = 0; t < 3; ++t)  // O^T = Dl^T P^T
-                    for (int kk = 0; kk < 4; ++kk) {
-                        uint32_t ao = sb + SM_RT + (t == 2 ? 16384 : 0) + kk * 32;
-                        uint32_t bo = sb + SM_PHL + (t == 1 ? 8192 : 0) + kk * 32;
-                        mma_bf16(tmem + TM_O + 64 * st, sdesc_sw128(ao, 16, 1024), sdesc_sw128(bo, 16, 1024),
-                                 ID_N64, (t | kk) != 0);
-                    }
+                    mma_chain<4, 2, 2>(tmem + TM_O, sdesc_sw128(sb + SM_RT + (t == 2 ? 16384 : 0), 16, 1024),
+                                       sdesc_sw128(sb + SM_PHL + (t == 1 ? 8192 : 0), 16, 1024), ID_N64, t != 0);
                 mma_commit(bar(B_ODONE));
                 mma_commit(bar(B_EMPTY0 + st));
             }
@@ -482,32 +486,49 @@ k_tc_fwd(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
 #pragma unroll
         for (int i = 0; i < 64; ++i) S[i] = init ? init[(size_t)(64 * hh + i) * DV + v] : 0.f;
 
+        // o of chunk jj: scale (Gam QS + O) -> bf16, staged as [64 rows][128] in the v buffer of chunk jj
+        // (consumed: every state thread has passed R of chunk jj), then written with 16-byte stores
         auto epilogue = [&](int jj) -> bool {
             const int tok0 = sr.tok0 + jj * C, n = min(C, sr.tok1 - tok0), b = jj & 1;
             const float *Gm = vec + (jj & 3) * 256 + 64;
+            if (!o_out) {  // nothing to write: release QS / O and the v buffer (this thread is past R of jj)
+                mbar_arrive(bar(B_EPIFREE0 + b));
+                mbar_arrive(bar(B_VEMPTY0 + b));
+                return true;
+            }
             if (!wwait(B_ODONE, jj & 1, jj)) return false;
             tc_fence_after();
+            __nv_bfloat16 *stg = reinterpret_cast<__nv_bfloat16 *>(sm + SM_V + b * V_STAGE);
             uint32_t qs[16], oo[16];
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
                 tmem_ld16(trow + TM_QS + 64 * b + 32 * hh + 16 * half, qs);
-                tmem_ld16(trow + TM_O + 64 * b + 32 * hh + 16 * half, oo);
+                tmem_ld16(trow + TM_O + 32 * hh + 16 * half, oo);
                 tmem_wait_ld();
                 if (half == 1) {
                     tc_fence_before();
                     mbar_arrive(bar(B_EPIFREE0 + b));
                 }
-                if (o_out) {
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const int c = 32 * hh + 16 * half + i;
-                        if (c < n) {
-                            float ov = p.scale * fmaf(Gm[c], __uint_as_float(qs[i]), __uint_as_float(oo[i]));
-                            o_out[((size_t)(tok0 + c) * p.Hv + hv) * DV + v] = __float2bfloat16_rn(ov);
-                        }
-                    }
+                for (int i = 0; i < 16; ++i) {
+                    const int c = 32 * hh + 16 * half + i;
+                    const float ov = p.scale * fmaf(Gm[c], __uint_as_float(qs[i]), __uint_as_float(oo[i]));
+                    stg[c * DV + v] = __float2bfloat16_rn(ov);
                 }
             }
+            mbar_arrive(bar(B_STAGED0 + b));
+            if (!wwait(B_STAGED0 + b, (jj >> 1) & 1, jj)) return false;
+            {
+                const int ts = threadIdx.x - 32 * W_STATE0;
+                const uint4 *src = reinterpret_cast<const uint4 *>(stg);
+#pragma unroll
+                for (int k4 = 0; k4 < 4; ++k4) {
+                    const int idx = ts + 256 * k4, r = idx >> 4, c16 = idx & 15;
+                    if (r < n)
+                        *reinterpret_cast<uint4 *>(o_out + ((size_t)(tok0 + r) * p.Hv + hv) * DV + 8 * c16) = src[idx];
+                }
+            }
+            mbar_arrive(bar(B_VEMPTY0 + b));
             return true;
         };
 
@@ -515,47 +536,43 @@ k_tc_fwd(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
         for (int j = 0; j < nck && ok; ++j) {
             const int tok0 = sr.tok0 + j * C, n = min(C, sr.tok1 - tok0);
             const float *gam = vec + (j & 3) * 256, *Gm = gam + 64, *Ev = gam + 128, *bet = gam + 192;
-            // (a) S^T rows -> hi / lo operand tiles (K-block hh holds keys 64hh .. 64hh + 63)
-#pragma unroll
-            for (int ch = 0; ch < 8; ++ch)
-                st_split_chunk(sb + SM_SS + hh * 16384, sb + SM_SS + 32768 + hh * 16384, v, ch, S + 8 * ch);
-            fence_proxy_async_smem();
+            // (a) S^T row -> hi / lo bf16 pairs in TMEM (keys 64hh .. 64hh + 63: columns 32hh ..)
+            {
+                uint32_t shi[32], slo[32];
+                split_pack32(S, shi, slo);
+                tmem_st32(trow + TM_SH + 32 * hh, shi);
+                tmem_st32(trow + TM_SL + 32 * hh, slo);
+                tmem_wait_st();
+            }
+            tc_fence_before();
             mbar_arrive(bar(B_SSREADY));
             if (h_out) {
                 const size_t hb = ((size_t)(sr.c0 + j) * p.Hv + hv) * DK * DV;
 #pragma unroll
                 for (int i = 0; i < 64; ++i) h_out[hb + (size_t)(64 * hh + i) * DV + v] = S[i];
             }
-            // value column v at chunk rows 32hh .. 32hh + 31, as bf16 pairs (consumed in (c))
-            uint32_t vr[16];
-            {
-                const uint16_t *vp = reinterpret_cast<const uint16_t *>(a.v) + (size_t)hv * DV + v;
-                const size_t rs = (size_t)p.Hv * DV;
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const int c = 32 * hh + 2 * i;
-                    uint32_t lo = c < n ? (uint32_t)vp[(size_t)(tok0 + c) * rs] : 0u;
-                    uint32_t hi = c + 1 < n ? (uint32_t)vp[(size_t)(tok0 + c + 1) * rs] : 0u;
-                    vr[i] = lo | (hi << 16);
-                }
-            }
             if (j >= 1 && !(ok = epilogue(j - 1))) break;
             // (c) R^T = beta (V - Gam K S)^T; the gate vectors of chunk j are
             // published by the prep warps together with A (a_ready)
             if (!(ok = wwait(B_AREADY, j & 1, j))) break;
             if (!(ok = wwait(B_KSDONE, j & 1, j))) break;
+            if (!(ok = wwait(B_VFULL0 + (j & 1), (j >> 1) & 1, j))) break;
             tc_fence_after();
             uint32_t raw[32];
             tmem_ld32(trow + TM_KS + 32 * hh, raw);
             tmem_wait_ld();
+            // v at (row c, column v) of the swizzled tile (two 64-column boxes); rows past the chunk end
+            // are finite (next tokens or zero fill) and meet beta = 0
+            const unsigned char *vt = sm + SM_V + (j & 1) * V_STAGE + (v >> 6) * 8192;
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 float R[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
                     const int i = 8 * q + e, c = 32 * hh + i;
-                    const uint32_t vb = (vr[i >> 1] >> (16 * (i & 1))) & 0xFFFFu;
-                    R[e] = bet[c] * (bf16_bits_to_f(vb) - Gm[c] * __uint_as_float(raw[i]));
+                    const uint32_t vo = (uint32_t)c * 128u + ((uint32_t)(((v & 63) >> 3) ^ (c & 7)) << 4) + (uint32_t)(v & 7) * 2u;
+                    const float vv = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(vt + vo));
+                    R[e] = bet[c] * (vv - Gm[c] * __uint_as_float(raw[i]));
                 }
                 st_split_chunk(sb + SM_RT, sb + SM_RT + 16384, v, 4 * hh + q, R);
             }
@@ -575,7 +592,7 @@ k_tc_fwd(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
                     Dl[e] = __uint_as_float(raw[8 * q + e]);
                     ED[e] = Ev[32 * hh + 8 * q + e] * Dl[e];
                 }
-                st_split_chunk(sb + SM_SS, sb + SM_SS + 16384, v, 4 * hh + q, ED);
+                st_split_chunk(sb + SM_ED, sb + SM_ED + 16384, v, 4 * hh + q, ED);
                 st_split_chunk(sb + SM_RT, sb + SM_RT + 16384, v, 4 * hh + q, Dl);
             }
             tc_fence_before();
@@ -642,8 +659,9 @@ bool tc_fwd_supported(const Plan &p) { return p.io == GDN_BF16 && p.K == DK && p
 cudaError_t launch_tc_fwd(const Plan &p, const void *q, const void *k, const void *v, const float *g,
                           const float *beta, const float *h0, void *o, float *g_cum, void *A, float *h,
                           float *ht, cudaStream_t st, bool g_is_cum, float *A32, float *P32, const CpSplit *cp) {
-    CUtensorMap tk, tq;
-    if (!make_head_map(&tk, k, p.Hq, p) || !make_head_map(&tq, q, p.Hq, p)) return cudaErrorInvalidValue;
+    CUtensorMap tk, tq, tv;
+    if (!make_head_map(&tk, k, p.Hq, p) || !make_head_map(&tq, q, p.Hq, p) || !make_head_map(&tv, v, p.Hv, p))
+        return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(k_tc_fwd, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
     if (e != cudaSuccess) return e;
     FwdArgs a;
@@ -674,7 +692,7 @@ cudaError_t launch_tc_fwd(const Plan &p, const void *q, const void *k, const voi
         a.seg_states = cp->seg_states;
     }
     dim3 grid(p.n_seqs * a.n_seg, p.Hv);
-    k_tc_fwd<<<grid, NUM_THREADS, SMEM_BYTES, st>>>(tk, tq, p, a);
+    k_tc_fwd<<<grid, NUM_THREADS, SMEM_BYTES, st>>>(tk, tq, tv, p, a);
     return cudaGetLastError();
 }
 
