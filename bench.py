@@ -76,29 +76,37 @@ def kernel_work(name, w, C=64):
     workload ``w``: the share of its pass's algorithmic work that the kernel
     performs (per token and value head; d = K = V, e = io bytes, G = Hv / Hq):
 
-      fwd_tc        the whole forward                       (see ``algorithmic``)
-      bwd_state_tc  recompute K K^T, W, U, W S, state update 2C(2K + V) + 4KV flops;
-                    reads k, v, g_cum, beta                 Ke/G + Ve + 8 bytes
+      fwd_prep_tc   K K^T, Q K^T                            4CK flops;
+                    reads g, beta; writes g_cum, A          12 + Ce bytes
+      fwd_tc        the rest of the forward                 fwd - prep
+      bwd_prep_tc   K K^T, Q K^T                            4CK flops; reads g_cum, beta: 8 bytes
+      bwd_state_tc  W, U, W S, state update                 2C(K + V) + 4KV flops;
+                    reads k, v                              Ke/G + Ve bytes
       bwd_dscan_tc  K dS, P^T dO, A^T dDl, state update      6KV + 4CV flops;
                     reads q, k, do, g_cum, beta             2Ke/G + Ve + 8 bytes
-      bwd_intra_tc  the rest of the backward's flops;       bwd - state - dscan;
+      bwd_intra_tc  the rest of the backward's flops;       bwd - prep - state - dscan;
                     reads q, k, v, do, g_cum, beta; writes dq, dk, dv, dbeta, dg
                                                             4Ke/G + 3Ve + 16 bytes
-    CUDA-core kernels (fp32 io or other head sizes) use the same shares.
+    Workspace traffic (operand images, chunk states) is not algorithmic and is
+    not counted.  CUDA-core kernels (fp32 io or other head sizes) use the same
+    shares.
     """
     K, V, G = w.K, w.V, w.Hv // w.Hq
     e = 2 if w.io_dtype == torch.bfloat16 else 4
     th = w.tokens * w.Hv
     alg = algorithmic(w, C)
-    st_f = th * (2 * C * (2 * K + V) + 4 * K * V)
+    pr_f = th * 4 * C * K
+    st_f = th * (2 * C * (K + V) + 4 * K * V)
     ds_f = th * (6 * K * V + 4 * C * V)
     table = {
-        "fwd_tc": (alg["fwd_flops"], alg["fwd_bytes"]),
-        "bwd_state_tc": (st_f, th * (K * e / G + V * e + 8)),
+        "fwd_prep_tc": (pr_f, th * (12 + C * e)),
+        "fwd_tc": (alg["fwd_flops"] - pr_f, alg["fwd_bytes"] - th * (12 + C * e)),
+        "bwd_prep_tc": (pr_f, th * 8),
+        "bwd_state_tc": (st_f, th * (K * e / G + V * e)),
         "bwd_dscan_tc": (ds_f, th * (2 * K * e / G + V * e + 8)),
-        "bwd_intra_tc": (alg["bwd_flops"] - st_f - ds_f, th * (4 * K * e / G + 3 * V * e + 16)),
+        "bwd_intra_tc": (alg["bwd_flops"] - pr_f - st_f - ds_f, th * (4 * K * e / G + 3 * V * e + 16)),
     }
-    table["fwd_scan"] = table["fwd_tc"]
+    table["fwd_scan"] = (alg["fwd_flops"], alg["fwd_bytes"])
     table["bwd_state"] = table["bwd_state_tc"]
     table["bwd_dscan"] = table["bwd_dscan_tc"]
     table["bwd_intra"] = table["bwd_intra_tc"]

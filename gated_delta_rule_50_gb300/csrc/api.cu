@@ -70,11 +70,11 @@ gdn_status make_plan(const gdn_problem *pr, Plan *pl) {
 }
 
 struct FwdWs {
-    size_t err, chunk_off, gam64, A32, P32, serial, seg_states, total;
+    size_t err, chunk_off, gam64, A32, P32, tiles, vecs, serial, seg_states, total;
     int seg_len, n_seg;  // n_seg > 1: sequence splitting with warmup is planned
 };
 struct BwdWs {
-    size_t err, chunk_off, gam64, A32, P32, hbuf, dSe, total;
+    size_t err, chunk_off, gam64, A32, P32, tiles, vecs, hbuf, dSe, total;
 };
 
 // Sequence splitting with warmup runs when asked for, supported and triggered.
@@ -97,6 +97,10 @@ FwdWs fwd_layout(const Plan &p) {
     w.gam64 = c.take<double>(simt ? tokens * p.Hv : 0);
     w.A32 = c.take<float>(simt ? mats : 0);
     w.P32 = c.take<float>(simt ? mats : 0);
+    // tensor-core path: per (chunk, value head) A / P operand images and gate vectors
+    const size_t units = simt ? 0 : (size_t)p.total_chunks * p.Hv;
+    w.tiles = c.take<unsigned char>(units * TC_TILE_BYTES);
+    w.vecs = c.take<float>(units * TC_VEC_FLOATS);
     w.seg_len = 0;
     w.n_seg = 1;
     w.serial = w.seg_states = 0;
@@ -120,6 +124,9 @@ BwdWs bwd_layout(const Plan &p) {
     w.gam64 = c.take<double>(tc_fwd_supported(p) ? 0 : tokens * p.Hv);  // CUDA-core path only
     w.A32 = c.take<float>(mats);
     w.P32 = c.take<float>(mats);
+    const size_t units = tc_fwd_supported(p) ? (size_t)p.total_chunks * p.Hv : 0;
+    w.tiles = c.take<unsigned char>(units * TC_TILE_BYTES);
+    w.vecs = c.take<float>(units * TC_VEC_FLOATS);
     w.hbuf = c.take<float>(states);
     w.dSe = c.take<float>(states);
     w.total = c.off;
@@ -180,6 +187,10 @@ gdn_status gdn_fwd(const gdn_problem *p, const void *q, const void *k, const voi
     GDN_LAUNCH("chunk_table", launch_chunk_table(pl, st));
     double *gam64 = at<double>(workspace, w.gam64);
     float *A32 = at<float>(workspace, w.A32), *P32 = at<float>(workspace, w.P32);
+    unsigned char *tiles = at<unsigned char>(workspace, w.tiles);
+    float *vecs = at<float>(workspace, w.vecs);
+    if (tc_fwd_supported(pl))  // A, P and the gate vectors of every chunk, in parallel
+        GDN_LAUNCH("fwd_prep_tc", launch_tc_prep(pl, q, k, g, false, beta, g_cum, A, nullptr, nullptr, tiles, vecs, st));
     if (w.n_seg > 1) {  // sequence splitting with warmup
         CpSplit cs;
         cs.seg_len = w.seg_len;
@@ -190,15 +201,13 @@ gdn_status gdn_fwd(const gdn_problem *p, const void *q, const void *k, const voi
         GDN_LAUNCH("cp_flags", launch_cp_flags(pl, g, cs.seg_len, cs.n_seg, cs.warm,
                                                at<uint8_t>(workspace, w.serial), st));
         cs.mode = CP_WARM;
-        GDN_LAUNCH("fwd_tc_warm", launch_tc_fwd(pl, q, k, v, g, beta, nullptr, nullptr, nullptr, nullptr, nullptr,
-                                                nullptr, st, false, nullptr, nullptr, &cs));
+        GDN_LAUNCH("fwd_tc_warm", launch_tc_fwd(pl, q, k, v, tiles, vecs, nullptr, nullptr, nullptr, nullptr, st, &cs));
         cs.mode = CP_MAIN;
-        GDN_LAUNCH("fwd_tc", launch_tc_fwd(pl, q, k, v, g, beta, h0, o, g_cum, A, h, final_state, st, false, nullptr,
-                                           nullptr, &cs));
+        GDN_LAUNCH("fwd_tc", launch_tc_fwd(pl, q, k, v, tiles, vecs, h0, o, h, final_state, st, &cs));
         return GDN_OK;
     }
     if (tc_fwd_supported(pl)) {
-        GDN_LAUNCH("fwd_tc", launch_tc_fwd(pl, q, k, v, g, beta, h0, o, g_cum, A, h, final_state, st));
+        GDN_LAUNCH("fwd_tc", launch_tc_fwd(pl, q, k, v, tiles, vecs, h0, o, h, final_state, st));
         return GDN_OK;
     }
     if (pl.total_chunks > 0)
@@ -233,9 +242,12 @@ gdn_status gdn_bwd(const gdn_problem *p, const void *q, const void *k, const voi
     float *A32 = at<float>(workspace, w.A32), *P32 = at<float>(workspace, w.P32);
     float *hbuf = at<float>(workspace, w.hbuf), *dSe = at<float>(workspace, w.dSe);
     if (pl.total_chunks > 0 && tc_fwd_supported(pl)) {
-        // tensor-core path: one forward recompute pass writes the chunk-entry states and A, P (fp32)
-        GDN_LAUNCH("bwd_state_tc", launch_tc_fwd(pl, q, k, v, g_cum, beta, h0, nullptr, nullptr, nullptr, hbuf,
-                                                 nullptr, st, true, A32, P32));
+        // tensor-core path: A, P (fp32 and operand images) of every chunk, then one state recompute pass
+        unsigned char *tiles = at<unsigned char>(workspace, w.tiles);
+        float *vecs = at<float>(workspace, w.vecs);
+        GDN_LAUNCH("bwd_prep_tc", launch_tc_prep(pl, q, k, g_cum, true, beta, nullptr, nullptr, A32, P32, tiles, vecs,
+                                                 st));
+        GDN_LAUNCH("bwd_state_tc", launch_tc_fwd(pl, q, k, v, tiles, vecs, h0, nullptr, hbuf, nullptr, st));
     } else if (pl.total_chunks > 0) {
         GDN_LAUNCH("bwd_prep", launch_simt_prep(pl, q, k, g_cum, 1, beta, nullptr, nullptr, gam64, A32, P32, st));
         GDN_LAUNCH("bwd_state", launch_simt_scan(pl, q, k, v, beta, gam64, A32, P32, h0, nullptr, hbuf, nullptr,

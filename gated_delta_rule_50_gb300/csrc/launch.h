@@ -41,10 +41,14 @@ cudaError_t launch_cp_flags(const Plan &p, const float *g, int seg_len, int n_se
 
 // tensor-core (tcgen05) fused forward: bf16 io, K = V = 128
 bool tc_fwd_supported(const Plan &p);
-cudaError_t launch_tc_fwd(const Plan &p, const void *q, const void *k, const void *v, const float *g,
-                          const float *beta, const float *h0, void *o, float *g_cum, void *A, float *h,
-                          float *ht, cudaStream_t st, bool g_is_cum = false, float *A32 = nullptr,
-                          float *P32 = nullptr, const CpSplit *cp = nullptr);
+// Per (chunk, value head): A / P operand images (32 KB) and gate vectors (1 KB); see tc_prep.cu.
+constexpr size_t TC_TILE_BYTES = 32768, TC_VEC_FLOATS = 256;
+cudaError_t launch_tc_prep(const Plan &p, const void *q, const void *k, const float *g, bool g_is_cum,
+                           const float *beta, float *g_cum, void *A, float *A32, float *P32, unsigned char *tiles,
+                           float *vecs, cudaStream_t st);
+cudaError_t launch_tc_fwd(const Plan &p, const void *q, const void *k, const void *v, const unsigned char *tiles,
+                          const float *vecs, const float *h0, void *o, float *h, float *ht, cudaStream_t st,
+                          const CpSplit *cp = nullptr);
 
 // TMA map of a [tokens][heads][128] bf16 tensor (64 x 1 x 64 boxes, 128-byte swizzle)
 bool make_head_map(CUtensorMap *m, const void *ptr, int heads, const Plan &p);

@@ -1,0 +1,313 @@
+// tc_prep.cu -- per-chunk preparation for the tensor-core chain kernels (bf16 io,
+// K = V = 128, chunk 64): the gate cumsum, L, A = (I + L)^{-1} and P, for every
+// chunk at once.
+//
+// These are the intra-chunk quantities of the chunked form (the "A matrix" step
+// of the pages' step list; FlashQLA blog post, section 2).  None of them depends
+// on the state, so they are computed here, fully in parallel over chunks and
+// heads, and the serial state chains only copy them in.  One CTA per (chunk,
+// q/k head) forms K K^T and Q K^T once on the tensor cores and loops over the
+// group's value heads:
+//
+//   gam   chunk-local inclusive cumsum of g (or given, for the backward),
+//   L     = strict_lower(diag(beta) (D o K K^T)),  D_ri = exp(gam_r - gam_i),
+//   A     = (I + L)^{-1}          (blocked, in place, fp32),
+//   P     = D o Q K^T             (lower, diagonal included).
+//
+// Per (chunk, value head) it writes a 32 KB operand image -- A hi, A lo, P hi,
+// P lo, each a 64 x 64 bf16 tile in the 128-byte-swizzled K-major layout the
+// MMAs read (row r at r * 128, 16-byte chunk c at position c ^ (r & 7)) -- and a
+// 1 KB vector block {gam, exp(gam), exp(gam_last - gam), beta} x 64, ready for
+// plain bulk copies.  Optionally g_cum, A in the io dtype and fp32 A / P.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "launch.h"
+#include "tc.cuh"
+
+namespace gdn {
+namespace {
+
+using namespace tc;
+
+constexpr int DK = 128;
+constexpr int NT = 128;
+
+constexpr uint32_t S_KQ = 0;                          // [kb0: K 8K, Q 8K][kb1: K 8K, Q 8K]
+constexpr uint32_t S_LM = 32768;                      // fp32 [64][65]: L, then A in place
+constexpr uint32_t S_TB = S_LM + 64 * 65 * 4;         // fp32 3 x [16][17]
+constexpr uint32_t S_VEC = S_TB + 3 * 16 * 17 * 4;    // gam, Gam, E, beta (64 each)
+constexpr uint32_t S_BAR = S_VEC + 4 * 64 * 4;
+constexpr uint32_t S_MISC = S_BAR + 16;
+constexpr uint32_t SMEM_BYTES = S_MISC + 32 + 1024;
+
+constexpr uint32_t ID_N64 = idesc_bf16(128, 64, 0, 0);
+
+struct PrepArgs {
+    const float *g, *beta;
+    int g_is_cum;
+    float *g_cum;
+    __nv_bfloat16 *A;
+    float *A32, *P32;
+    unsigned char *tiles;  // [chunks][Hv] x 32 KB
+    float *vecs;           // [chunks][Hv] x 256
+};
+
+__device__ __forceinline__ uint64_t kdesc(uint32_t a) { return sdesc_sw128(a, 16, 1024); }
+
+// Blocked in-place inverse of the unit lower-triangular I + L held in Lm
+// ([64][65], strictly lower part = L, rest 0); afterwards Lm = (I + L)^{-1}.
+// Column blocks of 16 are processed right to left so that the inverted A_IK
+// (K > J) and the untouched L_KJ are both available:
+//     A_IJ = -(sum_{K=J+1}^{I} A_IK L_KJ) A_JJ.
+// Called by the 128 prep threads (named barrier 1).
+__device__ void blocked_inverse(float *Lm, float *Tb, int pt) {
+    constexpr int LS = 65, TS = 17;
+    float x[16];
+    const int b = pt >> 4, jc = pt & 15, base = 16 * b;
+    if (pt < 64) {  // diagonal blocks: forward substitution, one column per thread
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+            float s = 0.f;
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+                if (i >= jc && i < r) s = fmaf(Lm[(base + r) * LS + base + i], x[i], s);
+            x[r] = (r < jc) ? 0.f : (r == jc ? 1.f : -s);
+        }
+    }
+    named_bar(1, 128);
+    if (pt < 64) {
+#pragma unroll
+        for (int r = 0; r < 16; ++r) Lm[(base + r) * LS + base + jc] = x[r];
+    }
+    named_bar(1, 128);
+    for (int J = 2; J >= 0; --J) {
+        const int nblk = 3 - J;  // blocks I = J+1 .. 3
+        for (int o = pt; o < nblk * 256; o += 128) {
+            const int I = J + 1 + (o >> 8), r = (o >> 4) & 15, c = o & 15;
+            float s = 0.f;
+            for (int K = J + 1; K <= I; ++K) {
+                const float *arow = Lm + (16 * I + r) * LS + 16 * K;
+                const float *lcol = Lm + (16 * K) * LS + 16 * J + c;
+#pragma unroll
+                for (int k = 0; k < 16; ++k) s = fmaf(arow[k], lcol[k * LS], s);
+            }
+            Tb[(o >> 8) * 16 * TS + r * TS + c] = s;
+        }
+        named_bar(1, 128);
+        for (int o = pt; o < nblk * 256; o += 128) {
+            const int I = J + 1 + (o >> 8), r = (o >> 4) & 15, c = o & 15;
+            const float *trow = Tb + (o >> 8) * 16 * TS + r * TS;
+            const float *acol = Lm + (16 * J) * LS + 16 * J + c;
+            float s = 0.f;
+#pragma unroll
+            for (int k = 0; k < 16; ++k) s = fmaf(trow[k], acol[k * LS], s);
+            Lm[(16 * I + r) * LS + 16 * J + c] = -s;
+        }
+        named_bar(1, 128);
+    }
+}
+
+// 8 consecutive values of row r (chunk ch) of a 64-wide tile -> hi and lo 16-byte chunks of the image.
+__device__ __forceinline__ void put_split_chunk(unsigned char *hi_tile, unsigned char *lo_tile, int r, int ch,
+                                                const float *x) {
+    float h[8], l[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) split2(x[i], h[i], l[i]);
+    const uint32_t off = (uint32_t)r * 128u + ((uint32_t)(ch ^ (r & 7)) << 4);
+    *reinterpret_cast<uint4 *>(hi_tile + off) =
+        make_uint4(pack_bf16(h[0], h[1]), pack_bf16(h[2], h[3]), pack_bf16(h[4], h[5]), pack_bf16(h[6], h[7]));
+    *reinterpret_cast<uint4 *>(lo_tile + off) =
+        make_uint4(pack_bf16(l[0], l[1]), pack_bf16(l[2], l[3]), pack_bf16(l[4], l[5]), pack_bf16(l[6], l[7]));
+}
+
+__global__ void __launch_bounds__(NT, 4)
+k_tc_prep(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q, Plan p, PrepArgs a) {
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    unsigned char *sm = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                          ~uintptr_t(1023));
+    const uint32_t sb = smem_u32(sm);
+    const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+    uint32_t *misc = reinterpret_cast<uint32_t *>(sm + S_MISC);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(misc + 1);
+    float *Lm = reinterpret_cast<float *>(sm + S_LM), *Tb = reinterpret_cast<float *>(sm + S_TB);
+    float *gam = reinterpret_cast<float *>(sm + S_VEC), *Gm = gam + 64, *Ev = gam + 128, *bet = gam + 192;
+    float *wtot = reinterpret_cast<float *>(misc + 4);
+    const uint32_t bar_tma = sb + S_BAR, bar_mma = sb + S_BAR + 8;
+
+    const int gc = blockIdx.x, hq = blockIdx.y;
+    const ChunkPos cp = chunk_pos(p, gc);
+    const int tok0 = cp.tok0, n = cp.len;
+
+    if (t == 0) {
+        mbar_init(bar_tma, 1);
+        mbar_init(bar_mma, 1);
+        misc[1] = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0) tmem_alloc(sb + S_MISC, 64);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = misc[0];
+    bool ok = true;
+    // K K^T (lanes 0..63) and Q K^T (lanes 64..127) of this chunk: D1 = [K; Q] K^T
+    if (t == 0) {
+        mbar_arrive_expect_tx(bar_tma, 32768);
+        tma_load_3d(sb + S_KQ, &tm_k, bar_tma, 0, hq, tok0);
+        tma_load_3d(sb + S_KQ + 8192, &tm_q, bar_tma, 0, hq, tok0);
+        tma_load_3d(sb + S_KQ + 16384, &tm_k, bar_tma, 64, hq, tok0);
+        tma_load_3d(sb + S_KQ + 24576, &tm_q, bar_tma, 64, hq, tok0);
+    }
+    if (warp == 0) ok = mbar_wait_warp(bar_tma, 0, abort_flag);
+    ok = __syncthreads_and(ok) != 0;
+    if (ok && t == 0) {
+        tc_fence_after();
+        for (int blk = 0; blk < 2; ++blk)
+            mma_chain<4, 2, 2>(tmem, kdesc(sb + S_KQ + 16384 * blk), kdesc(sb + S_KQ + 16384 * blk), ID_N64, blk);
+        mma_commit(bar_mma);
+    }
+    if (ok && warp == 0) ok = mbar_wait_warp(bar_mma, 0, abort_flag);
+    ok = __syncthreads_and(ok) != 0;
+    tc_fence_after();
+    uint32_t raw[64];  // this thread's row of K K^T (t < 64) or Q K^T (t >= 64)
+    if (ok) {
+        uint32_t r0[32], r1[32];
+        tmem_ld32(tmem + ((uint32_t)(32 * warp) << 16), r0);
+        tmem_ld32(tmem + ((uint32_t)(32 * warp) << 16) + 32, r1);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            raw[i] = r0[i];
+            raw[32 + i] = r1[i];
+        }
+    }
+    for (int g = 0; ok && g < p.G; ++g) {
+        const int hv = hq * p.G + g;
+        const size_t unit = (size_t)gc * p.Hv + hv;
+        // gate cumsum over rows 0..63 (threads 0..63); rows past the chunk end hold the last value
+        float x = 0.f, bv = 0.f;
+        if (t < 64) {
+            const size_t gi = (size_t)(tok0 + (t < n ? t : n - 1)) * p.Hv + hv;
+            if (a.g_is_cum) {
+                x = a.g[gi];
+            } else {
+                x = t < n ? a.g[gi] : 0.f;
+#pragma unroll
+                for (int off = 1; off < 32; off <<= 1) {
+                    const float y = __shfl_up_sync(0xffffffffu, x, off);
+                    if (lane >= off) x += y;
+                }
+                if (t == 31) *wtot = x;
+            }
+            bv = t < n ? a.beta[gi] : 0.f;
+        }
+        __syncthreads();
+        if (t < 64) {
+            if (!a.g_is_cum && t >= 32) x += *wtot;
+            gam[t] = x;
+            bet[t] = bv;
+            if (t < n && a.g_cum) a.g_cum[(size_t)(tok0 + t) * p.Hv + hv] = x;
+        }
+        __syncthreads();
+        const float glast = gam[n - 1];
+        if (t < 64) {
+            Gm[t] = t < n ? __expf(gam[t]) : 0.f;
+            Ev[t] = t < n ? __expf(glast - gam[t]) : 0.f;
+        }
+        unsigned char *img = a.tiles + unit * 32768;
+        if (t < 64) {  // L = beta D o K K^T, strictly lower
+            const int r = t;
+            const float gr = gam[r], br = bet[r];
+#pragma unroll
+            for (int i = 0; i < 64; ++i)
+                Lm[r * 65 + i] = (i < r && r < n) ? br * __expf(gr - gam[i]) * __uint_as_float(raw[i]) : 0.f;
+        } else {  // P = D o Q K^T, lower incl. diagonal -> image (and fp32 copy)
+            const int r = t - 64;
+            const float gr = gam[r];
+            float *p32 = a.P32 ? a.P32 + unit * C * C + (size_t)r * C : nullptr;
+#pragma unroll
+            for (int ch = 0; ch < 8; ++ch) {
+                float pv[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const int i = 8 * ch + e;
+                    pv[e] = (i <= r && r < n) ? __expf(gr - gam[i]) * __uint_as_float(raw[i]) : 0.f;
+                }
+                put_split_chunk(img + 16384, img + 24576, r, ch, pv);
+                if (p32) {
+                    reinterpret_cast<float4 *>(p32)[2 * ch] = make_float4(pv[0], pv[1], pv[2], pv[3]);
+                    reinterpret_cast<float4 *>(p32)[2 * ch + 1] = make_float4(pv[4], pv[5], pv[6], pv[7]);
+                }
+            }
+        }
+        __syncthreads();
+        blocked_inverse(Lm, Tb, t);
+        {  // A -> image, io-dtype output and fp32 copy: thread holds half a row
+            const int r = t >> 1, hh = t & 1;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int ch = 4 * hh + q;
+                float vals[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) vals[e] = Lm[r * 65 + 8 * ch + e];
+                put_split_chunk(img, img + 8192, r, ch, vals);
+                if (a.A && r < n) {
+                    const uint4 pk = make_uint4(pack_bf16(vals[0], vals[1]), pack_bf16(vals[2], vals[3]),
+                                                pack_bf16(vals[4], vals[5]), pack_bf16(vals[6], vals[7]));
+                    *reinterpret_cast<uint4 *>(a.A + ((size_t)(tok0 + r) * p.Hv + hv) * C + 8 * ch) = pk;
+                }
+                if (a.A32) {
+                    float4 *d = reinterpret_cast<float4 *>(a.A32 + unit * C * C + (size_t)r * C + 8 * ch);
+                    d[0] = make_float4(vals[0], vals[1], vals[2], vals[3]);
+                    d[1] = make_float4(vals[4], vals[5], vals[6], vals[7]);
+                }
+            }
+        }
+        if (t < 64)  // vector block: 256 floats
+            reinterpret_cast<float4 *>(a.vecs + unit * 256)[t] = reinterpret_cast<const float4 *>(gam)[t];
+        __syncthreads();  // Lm, vectors reused by the next head
+    }
+    if (!ok && t == 0) {
+        if (atomicCAS(p.err + 1, 0u, 301u) == 0u) {
+            p.err[2] = (uint32_t)gc;
+            p.err[4] = blockIdx.x + blockIdx.y * gridDim.x;
+        }
+        atomicOr(p.err, ERR_TIMEOUT);
+        mbar_drain(bar_tma, 0);
+        mma_commit(bar_mma);
+        mbar_drain(bar_mma, 0);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0) tmem_dealloc(tmem, 64);
+}
+
+}  // namespace
+
+cudaError_t launch_tc_prep(const Plan &p, const void *q, const void *k, const float *g, bool g_is_cum,
+                           const float *beta, float *g_cum, void *A, float *A32, float *P32, unsigned char *tiles,
+                           float *vecs, cudaStream_t st) {
+    if (p.total_chunks == 0) return cudaSuccess;
+    CUtensorMap tk, tq;
+    if (!make_head_map(&tk, k, p.Hq, p) || !make_head_map(&tq, q, p.Hq, p)) return cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(k_tc_prep, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    PrepArgs a;
+    a.g = g;
+    a.beta = beta;
+    a.g_is_cum = g_is_cum ? 1 : 0;
+    a.g_cum = g_cum;
+    a.A = static_cast<__nv_bfloat16 *>(A);
+    a.A32 = A32;
+    a.P32 = P32;
+    a.tiles = tiles;
+    a.vecs = vecs;
+    dim3 grid(p.total_chunks, p.Hq);
+    k_tc_prep<<<grid, NT, SMEM_BYTES, st>>>(tk, tq, p, a);
+    return cudaGetLastError();
+}
+
+}  // namespace gdn
