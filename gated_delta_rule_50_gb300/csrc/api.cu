@@ -121,9 +121,10 @@ BwdWs bwd_layout(const Plan &p) {
     size_t states = (size_t)p.total_chunks * p.Hv * p.K * p.V;
     w.err = c.take<uint32_t>(64);
     w.chunk_off = c.take<int32_t>((size_t)p.n_seqs + 1);
-    w.gam64 = c.take<double>(tc_fwd_supported(p) ? 0 : tokens * p.Hv);  // CUDA-core path only
-    w.A32 = c.take<float>(mats);
-    w.P32 = c.take<float>(mats);
+    // fp64 gate sums and fp32 A / P serve only the CUDA-core path
+    w.gam64 = c.take<double>(tc_fwd_supported(p) ? 0 : tokens * p.Hv);
+    w.A32 = c.take<float>(tc_fwd_supported(p) ? 0 : mats);
+    w.P32 = c.take<float>(tc_fwd_supported(p) ? 0 : mats);
     const size_t units = tc_fwd_supported(p) ? (size_t)p.total_chunks * p.Hv : 0;
     w.tiles = c.take<unsigned char>(units * TC_TILE_BYTES);
     w.vecs = c.take<float>(units * TC_VEC_FLOATS);
@@ -245,8 +246,8 @@ gdn_status gdn_bwd(const gdn_problem *p, const void *q, const void *k, const voi
         // tensor-core path: A, P (fp32 and operand images) of every chunk, then one state recompute pass
         unsigned char *tiles = at<unsigned char>(workspace, w.tiles);
         float *vecs = at<float>(workspace, w.vecs);
-        GDN_LAUNCH("bwd_prep_tc", launch_tc_prep(pl, q, k, g_cum, true, beta, nullptr, nullptr, A32, P32, tiles, vecs,
-                                                 st));
+        GDN_LAUNCH("bwd_prep_tc", launch_tc_prep(pl, q, k, g_cum, true, beta, nullptr, nullptr, nullptr, nullptr,
+                                                 tiles, vecs, st));
         GDN_LAUNCH("bwd_state_tc", launch_tc_fwd(pl, q, k, v, tiles, vecs, h0, nullptr, hbuf, nullptr, st));
     } else if (pl.total_chunks > 0) {
         GDN_LAUNCH("bwd_prep", launch_simt_prep(pl, q, k, g_cum, 1, beta, nullptr, nullptr, gam64, A32, P32, st));
@@ -254,12 +255,14 @@ gdn_status gdn_bwd(const gdn_problem *p, const void *q, const void *k, const voi
                                                  st));
     }
     if (tc_fwd_supported(pl))
-        GDN_LAUNCH("bwd_dscan_tc", launch_tc_dscan(pl, q, k, d_o, g_cum, beta, A32, P32, dht, dSe, dh0, st));
+        GDN_LAUNCH("bwd_dscan_tc", launch_tc_dscan(pl, q, k, d_o, g_cum, beta, at<unsigned char>(workspace, w.tiles), dht,
+                                                   dSe, dh0, st));
     else
         GDN_LAUNCH("bwd_dscan", launch_simt_dscan(pl, q, k, d_o, beta, gam64, A32, P32, dht, dSe, dh0, st));
     if (pl.total_chunks > 0 && tc_fwd_supported(pl))
-        GDN_LAUNCH("bwd_intra_tc", launch_tc_bwd_intra(pl, q, k, v, d_o, g_cum, beta, A32, P32, hbuf, dSe, dq, dk, dv,
-                                                       dbeta, dg, st));
+        GDN_LAUNCH("bwd_intra_tc", launch_tc_bwd_intra(pl, q, k, v, d_o, at<unsigned char>(workspace, w.tiles),
+                                                       at<float>(workspace, w.vecs), hbuf, dSe, dq, dk, dv, dbeta,
+                                                       dg, st));
     else if (pl.total_chunks > 0)
         GDN_LAUNCH("bwd_intra", launch_simt_bwd_intra(pl, q, k, v, d_o, beta, gam64, A32, P32, hbuf, dSe, dq, dk,
                                                      dv, dbeta, dg, st));

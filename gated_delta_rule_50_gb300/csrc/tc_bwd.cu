@@ -20,7 +20,8 @@
 // Warp roles (448 threads):
 //   warp 0      TMA producer: k and do chunk tiles (128-byte swizzle), 2 stages
 //   warp 1      TMEM allocator, single-thread MMA issuer
-//   warps 2-5   aux: A and P (double-buffered) and scale Gam o Q operand tiles
+//   warps 2-5   aux: A and P operand images (bulk copies from the prep kernel's
+//               output, double-buffered) and scale Gam o Q operand tiles
 //   warps 6-13  state: dS in registers, dDl, beta Gam o dR, state update
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -67,7 +68,8 @@ constexpr uint32_t ID_N64_BMN = idesc_bf16(128, 64, 0, 1);
 
 struct DscanArgs {
     const __nv_bfloat16 *q;
-    const float *g_cum, *beta, *A32, *P32, *dht;
+    const float *g_cum, *beta, *dht;
+    const unsigned char *tiles;  // [chunks][Hv] x 32 KB: A hi / lo, P hi / lo operand images
     float *dSe, *dh0;
 };
 
@@ -99,7 +101,7 @@ k_tc_dscan(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
     auto chunk_tok0 = [&](int t) { return sr.tok0 + (nck - 1 - t) * C; };
 
     if (threadIdx.x == 0) {
-        const uint32_t counts[B_COUNT] = {1, 1, 1, 1, 128, 128, 256, 1, 256, 1, 256, 1, 1};
+        const uint32_t counts[B_COUNT] = {1, 1, 1, 1, 1, 128, 256, 1, 256, 1, 256, 1, 1};
         for (int i = 0; i < B_COUNT; ++i) mbar_init(bar(i), counts[i]);
         misc[1] = 0;
         fence_mbar_init();
@@ -218,7 +220,7 @@ k_tc_dscan(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
         // ------------------------------------------------------------------ aux warps
         const int pt = (warp - W_AUX0) * 32 + lane;  // 0..127
         const int r = pt >> 1, hh = pt & 1;          // tile row, column half
-        int failed = -1, fj = 0;
+        int failed = -1, fj = 0, ap_issued = 0;
         auto gwait = [&](int id, uint32_t par, int t) {
             bool w = mbar_wait(bar(id), par, abort_flag);
             if (!w && failed < 0) { failed = id; fj = t; }
@@ -229,21 +231,13 @@ k_tc_dscan(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
             const int sl = t & 1;
             // the MMA must have taken the previous step's tiles before this slot pair is reused
             if (t >= 1 && !gwait(B_KDDONE, (t - 1) & 1, t)) break;
-            const size_t mat = ((size_t)gc * p.Hv + hv) * C * C + (size_t)r * C + 32 * hh;
-#pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-                float av[8], pv[8];
-                const float4 a0 = *reinterpret_cast<const float4 *>(a.A32 + mat + 8 * q4);
-                const float4 a1 = *reinterpret_cast<const float4 *>(a.A32 + mat + 8 * q4 + 4);
-                const float4 p0 = *reinterpret_cast<const float4 *>(a.P32 + mat + 8 * q4);
-                const float4 p1 = *reinterpret_cast<const float4 *>(a.P32 + mat + 8 * q4 + 4);
-                av[0] = a0.x; av[1] = a0.y; av[2] = a0.z; av[3] = a0.w; av[4] = a1.x; av[5] = a1.y; av[6] = a1.z; av[7] = a1.w;
-                pv[0] = p0.x; pv[1] = p0.y; pv[2] = p0.z; pv[3] = p0.w; pv[4] = p1.x; pv[5] = p1.y; pv[6] = p1.z; pv[7] = p1.w;
-                st_split_chunk(sb + SM_A + sl * 16384, sb + SM_A + sl * 16384 + 8192, r, 4 * hh + q4, av);
-                st_split_chunk(sb + SM_P + sl * 16384, sb + SM_P + sl * 16384 + 8192, r, 4 * hh + q4, pv);
+            if (pt == 0) {  // A and P images of chunk gc into slot sl
+                const unsigned char *img = a.tiles + ((size_t)gc * p.Hv + hv) * 32768;
+                mbar_arrive_expect_tx(bar(B_APREADY), 32768);
+                bulk_load(sb + SM_A + sl * 16384, img, 16384, bar(B_APREADY));
+                bulk_load(sb + SM_P + sl * 16384, img + 16384, 16384, bar(B_APREADY));
+                ++ap_issued;
             }
-            fence_proxy_async_smem();
-            mbar_arrive(bar(B_APREADY));
             // scale Gam o Q, once the previous step's U (its only reader) is done
             if (t >= 1 && !gwait(B_DRDONE, (t - 1) & 1, t)) break;
             {
@@ -272,6 +266,7 @@ k_tc_dscan(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
             fence_proxy_async_smem();
             mbar_arrive(bar(B_GQREADY));
         }
+        if (pt == 0 && ap_issued > 0) mbar_drain(bar(B_APREADY), (ap_issued - 1) & 1);  // no copy left in flight
         if (failed >= 0) record_timeout(p, failed, fj);
     } else {
         // ------------------------------------------------------------------ state warps
@@ -395,8 +390,8 @@ k_tc_dscan(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
 }  // namespace
 
 cudaError_t launch_tc_dscan(const Plan &p, const void *q, const void *k, const void *d_o, const float *g_cum,
-                            const float *beta, const float *A32, const float *P32, const float *dht, float *dSe,
-                            float *dh0, cudaStream_t st) {
+                            const float *beta, const unsigned char *tiles, const float *dht, float *dSe, float *dh0,
+                            cudaStream_t st) {
     CUtensorMap tk, tdo;
     if (!make_head_map(&tk, k, p.Hq, p) || !make_head_map(&tdo, d_o, p.Hv, p)) return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(k_tc_dscan, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
@@ -405,8 +400,7 @@ cudaError_t launch_tc_dscan(const Plan &p, const void *q, const void *k, const v
     a.q = static_cast<const __nv_bfloat16 *>(q);
     a.g_cum = g_cum;
     a.beta = beta;
-    a.A32 = A32;
-    a.P32 = P32;
+    a.tiles = tiles;
     a.dht = dht;
     a.dSe = dSe;
     a.dh0 = dh0;

@@ -57,6 +57,7 @@ constexpr uint32_t S_TOTAL = S_MISC + 16;
 constexpr uint32_t SMEM_BYTES = S_TOTAL + 1024;
 static_assert(SMEM_BYTES <= 232448, "shared memory");
 static_assert(S_F + 2048 * NW <= S_VEC, "transpose buffers fit in the fp32 scratch");
+static_assert(S_P == S_A + 16384 && S_VEC % 16 == 0, "operand image and vector copies");
 
 // TMEM columns
 constexpr uint32_t C_DQ = 0, C_DK = 64, C_HT = 128, C_KS = 256, C_QS = 320, C_DL = 384, C_DR = 448;
@@ -69,7 +70,9 @@ constexpr uint32_t ID_N128 = idesc_bf16(128, 128, 0, 0);
 static_assert(C_QS == C_KS + 64, "KS and QS accumulators must be adjacent");
 
 struct IntraArgs {
-    const float *g_cum, *beta, *A32, *P32, *hbuf, *dSe;
+    const unsigned char *tiles;  // [chunks][Hv] x 32 KB: A hi / lo, P hi / lo operand images
+    const float *vecs;           // [chunks][Hv] x {gam, Gam, E, beta} x 64
+    const float *hbuf, *dSe;
     __nv_bfloat16 *dq, *dk, *dv;
     float *dbeta, *dg;
 };
@@ -259,40 +262,19 @@ k_tc_bwd_intra(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     for (int g = 0; ok && g < p.G; ++g) {
         const int hv = hq * p.G + g;
         const size_t st_off = ((size_t)gc * p.Hv + hv) * DK * DV;
-        const size_t mat = ((size_t)gc * p.Hv + hv) * C * C;
         // ---------------------------------------------------------------- per-head vectors, dO / V tiles, A / P tiles
         ++tma_issued;
-        if (t == 0) {
-            mbar_arrive_expect_tx(bar_tma, 32768);
+        if (t == 0) {  // dO, V tiles; A / P operand images (S_A, S_P are adjacent); gate vectors
+            const size_t unit = (size_t)gc * p.Hv + hv;
+            mbar_arrive_expect_tx(bar_tma, 32768 + 32768 + 1024);
             tma_load_3d(sb + S_DO, &tm_do, bar_tma, 0, hv, tok0);
             tma_load_3d(sb + S_DO + 8192, &tm_do, bar_tma, 64, hv, tok0);
             tma_load_3d(sb + S_DD, &tm_v, bar_tma, 0, hv, tok0);
             tma_load_3d(sb + S_DD + 8192, &tm_v, bar_tma, 64, hv, tok0);
-        }
-        if (t < 64) {
-            const float glast = a.g_cum[(size_t)(tok0 + n - 1) * p.Hv + hv];
-            float gv = glast, bv = 0.f;
-            if (t < n) {
-                gv = a.g_cum[(size_t)(tok0 + t) * p.Hv + hv];
-                bv = a.beta[(size_t)(tok0 + t) * p.Hv + hv];
-            }
-            gam[t] = gv;
-            Gm[t] = t < n ? __expf(gv) : 0.f;
-            Ev[t] = t < n ? __expf(glast - gv) : 0.f;
-            bet[t] = bv;
-            bg[t] = t < n ? bv * __expf(gv) : 0.f;
+            bulk_load(sb + S_A, a.tiles + unit * 32768, 32768, bar_tma);
+            bulk_load(sb + S_VEC, a.vecs + unit * 256, 1024, bar_tma);
         }
         for (int o = t; o < 2 * NW * 64 + 2 * NW; o += NT) rdb_all[o] = 0.f;  // rdb, rdg, sH, sF
-        {
-            const int r = t >> 3, q = t & 7;  // 8 columns of row r
-            const float4 *ar = reinterpret_cast<const float4 *>(a.A32 + mat + (size_t)r * C + 8 * q);
-            const float4 *pr = reinterpret_cast<const float4 *>(a.P32 + mat + (size_t)r * C + 8 * q);
-            const float4 a0 = ar[0], a1 = ar[1], p0 = pr[0], p1 = pr[1];
-            const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-            const float pv[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
-            st_split_chunk(sb + S_A, sb + S_A + 8192, r, q, av);
-            st_split_chunk(sb + S_P, sb + S_P + 8192, r, q, pv);
-        }
         // ---------------------------------------------------------------- P1: h^T (lane v) -> TMEM; KS, QS
         {
             const float *hc = a.hbuf + st_off + (size_t)(32 * hh) * DV + lrow;
@@ -324,8 +306,9 @@ k_tc_bwd_intra(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         }
         mma_sync();
         if (!ok) break;
-        tma_wait();  // dO and V tiles of this head
+        tma_wait();  // dO, V, A, P and the gate vectors of this head
         if (!ok) break;
+        if (t < 64) bg[t] = bet[t] * Gm[t];  // read after the next CTA barrier
         // ---------------------------------------------------------------- P2: R^T tile, dgam (scale Gam dO . QS)
         float Xr[16], KSr[16];  // (V - Gam KS) and KS at chunk rows c = 16 hh + i, value lrow
         {
@@ -752,9 +735,8 @@ k_tc_bwd_intra(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
 }  // namespace
 
 cudaError_t launch_tc_bwd_intra(const Plan &p, const void *q, const void *k, const void *v, const void *d_o,
-                                const float *g_cum, const float *beta, const float *A32, const float *P32,
-                                const float *hbuf, const float *dSe, void *dq, void *dk, void *dv, float *dbeta,
-                                float *dg, cudaStream_t st) {
+                                const unsigned char *tiles, const float *vecs, const float *hbuf, const float *dSe,
+                                void *dq, void *dk, void *dv, float *dbeta, float *dg, cudaStream_t st) {
     CUtensorMap tk, tq, tdo, tv;
     if (!make_head_map(&tk, k, p.Hq, p) || !make_head_map(&tq, q, p.Hq, p) || !make_head_map(&tdo, d_o, p.Hv, p) ||
         !make_head_map(&tv, v, p.Hv, p))
@@ -763,10 +745,8 @@ cudaError_t launch_tc_bwd_intra(const Plan &p, const void *q, const void *k, con
         cudaFuncSetAttribute(k_tc_bwd_intra, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
     if (e != cudaSuccess) return e;
     IntraArgs a;
-    a.g_cum = g_cum;
-    a.beta = beta;
-    a.A32 = A32;
-    a.P32 = P32;
+    a.tiles = tiles;
+    a.vecs = vecs;
     a.hbuf = hbuf;
     a.dSe = dSe;
     a.dq = static_cast<__nv_bfloat16 *>(dq);
