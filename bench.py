@@ -435,7 +435,13 @@ def run_reference(args, rank, world):
                     "d2h_bytes_per_step": 0}}
 
 
-TRAFFIC = {}  # kernel -> dram bytes per launch from the committed ncu capture (None until measured)
+# kernel -> DRAM bytes (read + write) per launch at the benchmark workload, from the committed ncu
+# capture (profiles/ncu_kernels_train_b1_t4096_h64.md): measured on the half-size training shape and
+# scaled by the 4x units of the full one (per-unit reads and writes do not depend on the unit count).
+# An entry is removed whenever its kernel changes.
+TRAFFIC = {
+    "bwd_intra_tc": 4 * (849.097216e6 + 105.029632e6),
+}
 
 
 def main():

@@ -87,6 +87,11 @@ WORKLOADS = {
     "train_b2_t8192_h64": Workload("train_b2_t8192_h64", B=2, T=8192, Hq=16, Hv=64, K=128, V=128,
                                    io_dtype=torch.bfloat16, seed=4, has_h0=True, has_dht=True,
                                    bwd=True, zero_g_frac=0.1),
+    # half of the training shape (same heads and distributions) for hardware-counter captures: its
+    # inputs still exceed the 129 MB L2 while the device footprint stays near 1 GB
+    "train_b1_t4096_h64": Workload("train_b1_t4096_h64", B=1, T=4096, Hq=16, Hv=64, K=128, V=128,
+                                   io_dtype=torch.bfloat16, seed=5, has_h0=True, has_dht=True,
+                                   bwd=True, zero_g_frac=0.1),
 }
 # positional order matches the workload list of the operator's test plan
 WORKLOAD_ORDER = ["tiny_fp32", "prefill_b4_t4096", "varlen_8seq_32k",
