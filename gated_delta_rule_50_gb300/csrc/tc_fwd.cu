@@ -68,8 +68,7 @@ constexpr uint32_t TM_EDH = 0, TM_EDL = 32, TM_KS = 64, TM_DL = 128, TM_U = 64, 
 
 enum {
     B_FULL0 = 0, B_FULL1, B_EMPTY0, B_EMPTY1, B_SSREADY, B_KSDONE, B_RTREADY, B_DLDONE, B_EDREADY, B_UPDDONE,
-    B_ODONE, B_EPIFREE0, B_EPIFREE1, B_FINAL, B_VFULL0, B_VFULL1, B_VEMPTY0, B_VEMPTY1, B_STAGED0, B_STAGED1,
-    B_COUNT
+    B_ODONE, B_EPIFREE0, B_EPIFREE1, B_FINAL, B_VFULL0, B_VFULL1, B_VEMPTY0, B_VEMPTY1, B_COUNT
 };
 
 constexpr uint32_t ID_N64 = idesc_bf16(128, 64, 0, 0);
@@ -151,7 +150,7 @@ k_tc_fwd(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
     float *h_out = outs ? a.h : nullptr;
 
     if (threadIdx.x == 0) {
-        const uint32_t counts[B_COUNT] = {1, 1, 1, 1, 256, 1, 256, 1, 256, 1, 1, 256, 256, 1, 1, 1, 256, 256, 256, 256};
+        const uint32_t counts[B_COUNT] = {1, 1, 1, 1, 256, 1, 256, 1, 256, 1, 1, 256, 256, 1, 1, 1, 256, 256};
         for (int i = 0; i < B_COUNT; ++i) mbar_init(bar(i), counts[i]);
         misc[1] = 0;
         fence_mbar_init();
@@ -277,8 +276,9 @@ k_tc_fwd(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
 #pragma unroll
         for (int i = 0; i < 64; ++i) S[i] = init ? init[(size_t)(64 * hh + i) * DV + v] : 0.f;
 
-        // o of chunk jj: scale (Gam QS + O) -> bf16, staged as [64 rows][128] in the v buffer of chunk jj
-        // (consumed: every state thread has passed R of chunk jj), then written with 16-byte stores
+        // o of chunk jj: scale (Gam QS + O) -> bf16.  Each warp stages its 32 rows x 32 values in a private
+        // 2 KB part of the v buffer of chunk jj (consumed: every state thread is past R of jj) and writes
+        // them back as 64-byte row segments with 16-byte stores; no CTA-wide barrier is involved.
         auto epilogue = [&](int jj) -> bool {
             const int tok0 = sr.tok0 + jj * C, n = min(C, sr.tok1 - tok0), b = jj & 1;
             const float *Gm = vecs(jj) + 64;
@@ -289,35 +289,29 @@ k_tc_fwd(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
             }
             if (!wwait(B_ODONE, jj & 1, jj)) return false;
             tc_fence_after();
-            __nv_bfloat16 *stg = reinterpret_cast<__nv_bfloat16 *>(sm + SM_V + b * V_STAGE);
-            uint32_t qs[16], oo[16];
+            __nv_bfloat16 *stg = reinterpret_cast<__nv_bfloat16 *>(sm + SM_V + b * V_STAGE + 2048 * (warp - W_STATE0));
+            uint32_t qs[32], oo[32];
+            float gm[32];  // loaded before any store (generic pointers: no reordering across stores)
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                tmem_ld16(trow + TM_QS + 64 * b + 32 * hh + 16 * half, qs);
-                tmem_ld16(trow + TM_O + 32 * hh + 16 * half, oo);
-                tmem_wait_ld();
-                if (half == 1) {
-                    tc_fence_before();
-                    mbar_arrive(bar(B_EPIFREE0 + b));
-                }
+            for (int i = 0; i < 32; ++i) gm[i] = Gm[32 * hh + i];
+            tmem_ld32(trow + TM_QS + 64 * b + 32 * hh, qs);
+            tmem_ld32(trow + TM_O + 32 * hh, oo);
+            tmem_wait_ld();
+            tc_fence_before();
+            mbar_arrive(bar(B_EPIFREE0 + b));
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const int c = 32 * hh + 16 * half + i;
-                    const float ov = p.scale * fmaf(Gm[c], __uint_as_float(qs[i]), __uint_as_float(oo[i]));
-                    stg[c * DV + v] = __float2bfloat16_rn(ov);
-                }
-            }
-            mbar_arrive(bar(B_STAGED0 + b));
-            if (!wwait(B_STAGED0 + b, (jj >> 1) & 1, jj)) return false;
-            {
-                const int ts = threadIdx.x - 32 * W_STATE0;
-                const uint4 *src = reinterpret_cast<const uint4 *>(stg);
+            for (int i = 0; i < 32; ++i)  // row i of this warp's 32, column lane
+                stg[i * 32 + lane] =
+                    __float2bfloat16_rn(p.scale * fmaf(gm[i], __uint_as_float(qs[i]), __uint_as_float(oo[i])));
+            __syncwarp();
+            const uint4 *src = reinterpret_cast<const uint4 *>(stg);
 #pragma unroll
-                for (int k4 = 0; k4 < 4; ++k4) {
-                    const int idx = ts + 256 * k4, r = idx >> 4, c16 = idx & 15;
-                    if (r < n)
-                        *reinterpret_cast<uint4 *>(o_out + ((size_t)(tok0 + r) * p.Hv + hv) * DV + 8 * c16) = src[idx];
-                }
+            for (int k4 = 0; k4 < 4; ++k4) {  // lane: row 8 k4 + lane / 4, 8 values at 8 (lane % 4)
+                const int ri = 8 * k4 + (lane >> 2), c = 32 * hh + ri;
+                const uint4 w = src[ri * 4 + (lane & 3)];
+                if (c < n)
+                    *reinterpret_cast<uint4 *>(o_out + ((size_t)(tok0 + c) * p.Hv + hv) * DV + 32 * (warp & 3) +
+                                               8 * (lane & 3)) = w;
             }
             mbar_arrive(bar(B_VEMPTY0 + b));
             return true;
@@ -336,12 +330,11 @@ k_tc_fwd(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
             }
             tc_fence_before();
             mbar_arrive(bar(B_SSREADY));
-            if (h_out) {
+            if (h_out) {  // while KS is computed: the chunk-entry state (backward recompute)
                 const size_t hb = ((size_t)(sr.c0 + j) * p.Hv + hv) * DK * DV;
 #pragma unroll
                 for (int i = 0; i < 64; ++i) h_out[hb + (size_t)(64 * hh + i) * DV + v] = S[i];
             }
-            if (j >= 1 && !(ok = epilogue(j - 1))) break;
             // (c) R^T = beta (V - Gam K S)^T
             if (!(ok = wwait(B_VFULL0 + (j & 1), (j >> 1) & 1, j))) break;
             if (!(ok = wwait(B_KSDONE, j & 1, j))) break;
@@ -353,38 +346,37 @@ k_tc_fwd(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
             // v at (row c, column v) of the swizzled tile (two 64-column boxes); rows past the chunk end
             // are finite (next tokens or zero fill) and meet beta = 0
             const unsigned char *vt = sm + SM_V + (j & 1) * V_STAGE + (v >> 6) * 8192;
+            // every operand is loaded before the first store (the stores are asm with a memory clobber,
+            // which would otherwise order each load behind the previous store)
+            float R[32];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                float R[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const int i = 8 * q + e, c = 32 * hh + i;
-                    const uint32_t vo = (uint32_t)c * 128u + ((uint32_t)(((v & 63) >> 3) ^ (c & 7)) << 4) + (uint32_t)(v & 7) * 2u;
-                    const float vv = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(vt + vo));
-                    R[e] = bet[c] * (vv - Gm[c] * __uint_as_float(raw[i]));
-                }
-                st_split_chunk(sb + SM_RT, sb + SM_RT + 16384, v, 4 * hh + q, R);
+            for (int i = 0; i < 32; ++i) {
+                const int c = 32 * hh + i;
+                const uint32_t vo = (uint32_t)c * 128u + ((uint32_t)(((v & 63) >> 3) ^ (c & 7)) << 4) + (uint32_t)(v & 7) * 2u;
+                const float vv = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(vt + vo));
+                R[i] = bet[c] * (vv - Gm[c] * __uint_as_float(raw[i]));
             }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) st_split_chunk(sb + SM_RT, sb + SM_RT + 16384, v, 4 * hh + q, R + 8 * q);
             tc_fence_before();
             fence_proxy_async_smem();
             mbar_arrive(bar(B_RTREADY));
+            // while Dl is computed: o of chunk j - 1
+            if (j >= 1 && !(ok = epilogue(j - 1))) break;
             // (e) Dl^T -> Dl^T tile (R region) and (E Dl)^T hi / lo pairs in TMEM
             if (!(ok = wwait(B_DLDONE, j & 1, j))) break;
             tc_fence_after();
             tmem_ld32(trow + TM_DL + 32 * hh, raw);
             tmem_wait_ld();
             {
-                float ED[32];
+                float ED[32], Dl[32];
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    float Dl[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        Dl[e] = __uint_as_float(raw[8 * q + e]);
-                        ED[8 * q + e] = Ev[32 * hh + 8 * q + e] * Dl[e];
-                    }
-                    st_split_chunk(sb + SM_RT, sb + SM_RT + 16384, v, 4 * hh + q, Dl);
+                for (int i = 0; i < 32; ++i) {
+                    Dl[i] = __uint_as_float(raw[i]);
+                    ED[i] = Ev[32 * hh + i] * Dl[i];
                 }
+#pragma unroll
+                for (int q = 0; q < 4; ++q) st_split_chunk(sb + SM_RT, sb + SM_RT + 16384, v, 4 * hh + q, Dl + 8 * q);
                 uint32_t ehi[16], elo[16];
                 split_pack16(ED, ehi, elo);
                 tmem_st16(trow + TM_EDH + 16 * hh, ehi);
