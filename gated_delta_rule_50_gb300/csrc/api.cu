@@ -70,8 +70,9 @@ gdn_status make_plan(const gdn_problem *pr, Plan *pl) {
 }
 
 struct FwdWs {
-    size_t err, chunk_off, gam64, A32, P32, tiles, vecs, serial, seg_states, total;
-    int seg_len, n_seg;  // n_seg > 1: sequence splitting with warmup is planned
+    size_t err, chunk_off, gam64, A32, P32, tiles, vecs, serial, seg_states, seg_h, seg_M, total;
+    int seg_len, n_seg;  // n_seg > 1: sequence splitting is planned
+    bool exact;          // exact split (transitions) rather than warmup
 };
 struct BwdWs {
     size_t err, chunk_off, gam64, A32, P32, tiles, vecs, hbuf, dSe, total;
@@ -80,6 +81,14 @@ struct BwdWs {
 // Sequence splitting with warmup runs when asked for, supported and triggered.
 bool warmup_split(const Plan &p) {
     if (p.cp_mode != GDN_CP_WARMUP || !tc_fwd_supported(p) || !cp_trigger(p)) return false;
+    int L, n;
+    cp_geometry(p, &L, &n);
+    return n > 1;
+}
+
+// Exact sequence splitting (segment transitions, no approximation) in the default mode.
+bool exact_split(const Plan &p) {
+    if (p.cp_mode != GDN_CP_AUTO || !tc_fwd_supported(p) || !cp_trigger(p) || p.K != p.V) return false;
     int L, n;
     cp_geometry(p, &L, &n);
     return n > 1;
@@ -103,11 +112,18 @@ FwdWs fwd_layout(const Plan &p) {
     w.vecs = c.take<float>(units * TC_VEC_FLOATS);
     w.seg_len = 0;
     w.n_seg = 1;
-    w.serial = w.seg_states = 0;
-    if (warmup_split(p)) {
+    w.serial = w.seg_states = w.seg_h = w.seg_M = 0;
+    w.exact = exact_split(p);
+    if (w.exact || warmup_split(p)) {
         cp_geometry(p, &w.seg_len, &w.n_seg);
-        w.serial = c.take<uint8_t>((size_t)p.n_seqs * p.Hv);
-        w.seg_states = c.take<float>((size_t)p.n_seqs * p.Hv * w.n_seg * p.K * p.V);
+        const size_t st = (size_t)p.n_seqs * p.Hv * w.n_seg * p.K * p.V;
+        w.seg_states = c.take<float>(st);
+        if (w.exact) {
+            w.seg_h = c.take<float>(st);
+            w.seg_M = c.take<float>(st);
+        } else {
+            w.serial = c.take<uint8_t>((size_t)p.n_seqs * p.Hv);
+        }
     }
     w.total = c.off;
     return w;
@@ -192,17 +208,29 @@ gdn_status gdn_fwd(const gdn_problem *p, const void *q, const void *k, const voi
     float *vecs = at<float>(workspace, w.vecs);
     if (tc_fwd_supported(pl))  // A, P and the gate vectors of every chunk, in parallel
         GDN_LAUNCH("fwd_prep_tc", launch_tc_prep(pl, q, k, g, false, beta, g_cum, A, nullptr, nullptr, tiles, vecs, st));
-    if (w.n_seg > 1) {  // sequence splitting with warmup
+    if (w.n_seg > 1) {  // sequence splitting
         CpSplit cs;
         cs.seg_len = w.seg_len;
         cs.n_seg = w.n_seg;
         cs.warm = pl.warmup_chunks;
-        cs.serial = at<uint8_t>(workspace, w.serial);
+        cs.serial = nullptr;
         cs.seg_states = at<float>(workspace, w.seg_states);
-        GDN_LAUNCH("cp_flags", launch_cp_flags(pl, g, cs.seg_len, cs.n_seg, cs.warm,
-                                               at<uint8_t>(workspace, w.serial), st));
-        cs.mode = CP_WARM;
-        GDN_LAUNCH("fwd_tc_warm", launch_tc_fwd(pl, q, k, v, tiles, vecs, nullptr, nullptr, nullptr, nullptr, st, &cs));
+        cs.seg_h = cs.seg_M = nullptr;
+        if (w.exact) {  // segment contributions and transitions, then the scan over segments
+            cs.seg_h = at<float>(workspace, w.seg_h);
+            cs.seg_M = at<float>(workspace, w.seg_M);
+            cs.mode = CP_SEG;
+            GDN_LAUNCH("fwd_tc_seg", launch_tc_fwd(pl, q, k, v, tiles, vecs, nullptr, nullptr, nullptr, nullptr, st, &cs));
+            GDN_LAUNCH("cp_combine", launch_cp_combine(pl, h0, cs.seg_h, cs.seg_M, cs.seg_len, cs.n_seg, cs.seg_states,
+                                                       st));
+        } else {  // warmup: each segment after the first starts from a zero-state run over its window
+            uint8_t *serial = at<uint8_t>(workspace, w.serial);
+            cs.serial = serial;
+            GDN_LAUNCH("cp_flags", launch_cp_flags(pl, g, cs.seg_len, cs.n_seg, cs.warm, serial, st));
+            cs.mode = CP_WARM;
+            GDN_LAUNCH("fwd_tc_warm",
+                       launch_tc_fwd(pl, q, k, v, tiles, vecs, nullptr, nullptr, nullptr, nullptr, st, &cs));
+        }
         cs.mode = CP_MAIN;
         GDN_LAUNCH("fwd_tc", launch_tc_fwd(pl, q, k, v, tiles, vecs, h0, o, h, final_state, st, &cs));
         return GDN_OK;
@@ -273,7 +301,7 @@ int gdn_cp_plan(const gdn_problem *p, int *seg_len, int *n_seg) {
     Plan pl;
     if (make_plan(p, &pl) != GDN_OK) return -1;
     int L = 0, n = 1;
-    const int on = warmup_split(pl) ? 1 : 0;
+    const int on = (warmup_split(pl) || exact_split(pl)) ? 1 : 0;
     if (on) cp_geometry(pl, &L, &n);
     if (seg_len) *seg_len = on ? L : 0;
     if (n_seg) *n_seg = on ? n : 1;

@@ -25,15 +25,21 @@ cudaError_t launch_simt_bwd_intra(const Plan &p, const void *q, const void *k, c
                                   const float *P32, const float *hbuf, const float *dSe, void *dq, void *dk,
                                   void *dv, float *dbeta, float *dg, cudaStream_t st);
 
-// Sequence splitting with warmup: each sequence is cut into n_seg segments of
-// seg_len chunks; a CP_WARM launch computes every segment's starting state by
-// running `warm` chunks from a zero state, a CP_MAIN launch runs the segments.
-enum { CP_WARM = 1, CP_MAIN = 2 };
+// Sequence splitting: each sequence is cut into n_seg segments of
+// seg_len chunks.  Warmup: a CP_WARM launch computes every segment's starting state by running `warm`
+// chunks from a zero state.  Exact: a CP_SEG launch runs every segment twice -- from a zero state with
+// the real v (its contribution h_p) and with v = 0 from the identity (its transition M_p, since the
+// recurrence is linear in (v, S)) -- and launch_cp_combine scans S_(p+1) = M_p S_p + h_p.  A CP_MAIN
+// launch then runs the segments from their starting states.
+enum { CP_WARM = 1, CP_MAIN = 2, CP_SEG = 3 };
 struct CpSplit {
     int seg_len, n_seg, warm, mode;
-    const uint8_t *serial;  // [n_seqs][Hv] heads whose warmup windows do not decay enough
+    const uint8_t *serial;  // [n_seqs][Hv] heads whose warmup windows do not decay enough (warmup only)
     float *seg_states;      // [n_seqs][Hv][n_seg][K][V]
+    float *seg_h, *seg_M;   // exact: [n_seqs][Hv][n_seg][K][V] contributions and [..][K][K] transitions
 };
+cudaError_t launch_cp_combine(const Plan &p, const float *h0, const float *seg_h, const float *seg_M, int seg_len,
+                              int n_seg, float *seg_states, cudaStream_t st);
 bool cp_trigger(const Plan &p);                  // the pages' small batch x heads rule
 void cp_geometry(const Plan &p, int *seg_len, int *n_seg);
 cudaError_t launch_cp_flags(const Plan &p, const float *g, int seg_len, int n_seg, int warm, uint8_t *serial,

@@ -80,10 +80,11 @@ struct FwdArgs {
     const float *h0;
     __nv_bfloat16 *o;
     float *h, *ht;
-    // sequence splitting with warmup (see cp.cu): seg_len > 0 enables it
-    int seg_len, n_seg, warm, mode;  // mode: CP_WARM or CP_MAIN
-    const uint8_t *serial;           // [n_seqs][Hv]: 1 = this head runs unsplit
-    float *seg_states;               // [n_seqs][Hv][n_seg][K][V] warmup states
+    // sequence splitting (see cp.cu and launch.h): seg_len > 0 enables it
+    int seg_len, n_seg, warm, mode;  // mode: CP_WARM, CP_MAIN or CP_SEG
+    const uint8_t *serial;           // [n_seqs][Hv]: 1 = this head runs unsplit (warmup only; may be null)
+    float *seg_states;               // [n_seqs][Hv][n_seg][K][V] segment starting states
+    float *seg_h, *seg_M;            // CP_SEG outputs: segment contributions and transitions
 };
 
 // Records the first expired wait: err[1] = barrier + 1, err[2] = chunk,
@@ -110,8 +111,11 @@ k_tc_fwd(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
     auto bar = [&](int i) { return sb + SM_BAR + 8u * (uint32_t)i; };
 
     const int hv = blockIdx.y, hq = hv / p.G;
-    const int s = a.seg_len > 0 ? (int)blockIdx.x / a.n_seg : (int)blockIdx.x;
-    const int pseg = a.seg_len > 0 ? (int)blockIdx.x % a.n_seg : 0;
+    // CP_SEG: two CTAs per segment, the second runs the transition (v = 0, identity start)
+    const int cps = a.mode == CP_SEG ? 2 : 1;
+    const int s = a.seg_len > 0 ? (int)blockIdx.x / (a.n_seg * cps) : (int)blockIdx.x;
+    const int pseg = a.seg_len > 0 ? ((int)blockIdx.x / cps) % a.n_seg : 0;
+    const bool v_zero = a.mode == CP_SEG && (blockIdx.x & 1);
     SeqRange sr = seq_range(p, s);
     // chunk range of this CTA, its initial / final state and whether it writes the outputs
     const int nseq_ck = sr.c1 - sr.c0;
@@ -120,8 +124,9 @@ k_tc_fwd(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
     const float *init = a.h0 ? a.h0 + st_base : nullptr;
     float *fin = a.ht ? a.ht + st_base : nullptr;
     bool outs = true;
+    bool init_identity = false;
     if (a.seg_len > 0) {
-        const bool serial = a.serial[(size_t)s * p.Hv + hv] != 0;
+        const bool serial = a.serial && a.serial[(size_t)s * p.Hv + hv] != 0;
         const int L = a.seg_len;
         float *segst = a.seg_states + (((size_t)s * p.Hv + hv) * a.n_seg + pseg) * DK * DV;
         if (a.mode == CP_WARM) {  // state after the warmup window that precedes segment pseg, from zero
@@ -130,17 +135,28 @@ k_tc_fwd(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
             fin = segst;
             if (serial || pseg == 0 || pseg * L >= nseq_ck) jb = je = 0;
             else { jb = max(0, pseg * L - a.warm); je = pseg * L; }
-        } else {  // CP_MAIN
+        } else if (a.mode == CP_SEG) {  // segment pseg alone (not the last one): h_p or M_p
+            outs = false;
+            init = nullptr;
+            init_identity = v_zero;
+            const size_t so = (((size_t)s * p.Hv + hv) * a.n_seg + pseg) * DK * DV;
+            fin = (v_zero ? a.seg_M : a.seg_h) + so;
+            jb = min(pseg * L, nseq_ck);
+            je = min(nseq_ck, (pseg + 1) * L);
+            if (je >= nseq_ck) jb = je = 0;  // the last segment feeds no other
+        } else {  // CP_MAIN: exactly one segment owns the sequence end (segment 0 of an empty sequence)
             if (serial) {
-                if (pseg != 0) jb = je = 0;
+                if (pseg != 0) { jb = je = 0; fin = nullptr; }
             } else {
                 jb = min(pseg * L, nseq_ck);
                 je = min(nseq_ck, (pseg + 1) * L);
                 if (pseg > 0) init = segst;
-                if (je < nseq_ck) fin = nullptr;
+                const bool owns_end = nseq_ck == 0 ? pseg == 0 : (jb < je && je == nseq_ck);
+                if (!owns_end) fin = nullptr;
+                if (jb >= je) jb = je = 0;
             }
         }
-        if (jb >= je) { jb = je = 0; fin = nullptr; }
+        if (a.mode != CP_MAIN && jb >= je) { jb = je = 0; fin = nullptr; }
     }
     sr.tok0 += jb * C;
     sr.c0 += jb;
@@ -191,9 +207,11 @@ k_tc_fwd(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
                     record_timeout(p, B_VEMPTY0 + st, j);
                     break;
                 }
-                mbar_arrive_expect_tx(bar(B_VFULL0 + st), 16384 + 1024);
-                tma_load_3d(sb + SM_V + st * V_STAGE, &tm_v, bar(B_VFULL0 + st), 0, hv, tok0);
-                tma_load_3d(sb + SM_V + st * V_STAGE + 8192, &tm_v, bar(B_VFULL0 + st), 64, hv, tok0);
+                mbar_arrive_expect_tx(bar(B_VFULL0 + st), (v_zero ? 0 : 16384) + 1024);
+                if (!v_zero) {
+                    tma_load_3d(sb + SM_V + st * V_STAGE, &tm_v, bar(B_VFULL0 + st), 0, hv, tok0);
+                    tma_load_3d(sb + SM_V + st * V_STAGE + 8192, &tm_v, bar(B_VFULL0 + st), 64, hv, tok0);
+                }
                 bulk_load(sb + SM_V + st * V_STAGE + VEC_OFF, a.vecs + unit * 256, 1024, bar(B_VFULL0 + st));
                 vissued = j + 1;
             }
@@ -274,7 +292,8 @@ k_tc_fwd(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
         auto vecs = [&](int jj) { return reinterpret_cast<const float *>(sm + SM_V + (jj & 1) * V_STAGE + VEC_OFF); };
         float S[64];
 #pragma unroll
-        for (int i = 0; i < 64; ++i) S[i] = init ? init[(size_t)(64 * hh + i) * DV + v] : 0.f;
+        for (int i = 0; i < 64; ++i)
+            S[i] = init ? init[(size_t)(64 * hh + i) * DV + v] : (init_identity && 64 * hh + i == v ? 1.f : 0.f);
 
         // o of chunk jj: scale (Gam QS + O) -> bf16.  Each warp stages its 32 rows x 32 values in a private
         // 2 KB part of the v buffer of chunk jj (consumed: every state thread is past R of jj) and writes
@@ -353,7 +372,7 @@ k_tc_fwd(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
             for (int i = 0; i < 32; ++i) {
                 const int c = 32 * hh + i;
                 const uint32_t vo = (uint32_t)c * 128u + ((uint32_t)(((v & 63) >> 3) ^ (c & 7)) << 4) + (uint32_t)(v & 7) * 2u;
-                const float vv = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(vt + vo));
+                const float vv = v_zero ? 0.f : __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(vt + vo));
                 R[i] = bet[c] * (vv - Gm[c] * __uint_as_float(raw[i]));
             }
 #pragma unroll
@@ -465,6 +484,7 @@ cudaError_t launch_tc_fwd(const Plan &p, const void *q, const void *k, const voi
     a.mode = 0;
     a.serial = nullptr;
     a.seg_states = nullptr;
+    a.seg_h = a.seg_M = nullptr;
     if (cp) {
         a.seg_len = cp->seg_len;
         a.n_seg = cp->n_seg;
@@ -472,8 +492,10 @@ cudaError_t launch_tc_fwd(const Plan &p, const void *q, const void *k, const voi
         a.mode = cp->mode;
         a.serial = cp->serial;
         a.seg_states = cp->seg_states;
+        a.seg_h = cp->seg_h;
+        a.seg_M = cp->seg_M;
     }
-    dim3 grid(p.n_seqs * a.n_seg, p.Hv);
+    dim3 grid(p.n_seqs * a.n_seg * (a.mode == CP_SEG ? 2 : 1), p.Hv);
     k_tc_fwd<<<grid, NUM_THREADS, SMEM_BYTES, st>>>(tk, tq, tv, p, a);
     return cudaGetLastError();
 }

@@ -71,7 +71,8 @@ typedef enum {
 typedef enum { GDN_F32 = 0, GDN_BF16 = 1 } gdn_dtype;
 
 typedef enum {
-    GDN_CP_AUTO = 0,   /* exact path; sequence splitting only where it is exact   */
+    GDN_CP_AUTO = 0,   /* exact; when the pages' trigger fires, sequences are
+                          split and joined through segment transitions (gdn_fwd) */
     GDN_CP_OFF = 1,    /* one serial scan per (sequence, value head)             */
     GDN_CP_WARMUP = 2  /* approximate: segments start from a warmup state, see
                           gdn_fwd; used only when the page's trigger rule fires   */
@@ -111,6 +112,13 @@ size_t gdn_bwd_workspace_bytes(const gdn_problem *p);
  * state at the window start.  A value head whose gate sum over some warmup
  * window is above ln(1e-4) runs unsplit (exact) in that sequence.  g_cum, A
  * and h are as in the exact path; final_state comes from the last segment.
+ * GDN_CP_AUTO with the trigger on (the pages' AutoCP, news page "FlashQLA's
+ * core advantages"; here without approximation): the same segments; each is
+ * run from a zero state and, with v = 0, from the identity, which gives its
+ * contribution h_p and transition M_p (the recurrence is linear in v and S);
+ * the segment starting states S_(p+1) = M_p S_p + h_p are scanned in fp32 and
+ * every segment is then run from its own.  The result equals the unsplit one
+ * up to rounding.
  */
 gdn_status gdn_fwd(const gdn_problem *p,
                    const void *q, const void *k, const void *v,
@@ -168,8 +176,8 @@ gdn_status gdn_fwd_noalloc(const gdn_problem *p,
  * gdn_cp_trigger: 1 iff the pages' rule turns splitting on for n_seqs
  *   sequences of up to seq_len tokens and n_heads value heads
  *   (n_seqs * n_heads <= 40, or <= 56 with seq_len >= 8192).
- * gdn_cp_plan: 1 iff gdn_fwd would split this problem (cp_mode ==
- *   GDN_CP_WARMUP, bf16 with K = V = 128, trigger on, more than one segment);
+ * gdn_cp_plan: 1 iff gdn_fwd would split this problem (cp_mode GDN_CP_AUTO
+ *   or GDN_CP_WARMUP, bf16 with K = V = 128, trigger on, more than one segment);
  *   then *seg_len = L = round(sqrt(N)) chunks for N chunks of the longest
  *   sequence and *n_seg = ceil(N / L).  Returns 0 otherwise, -1 on a bad problem.
  */

@@ -124,8 +124,12 @@ def test_cp_plan_geometry(lib):
     assert lib.gdn_cp_plan(ctypes.byref(p), ctypes.byref(L), ctypes.byref(n)) == 1
     assert (L.value, n.value) == (23, 23)
     assert lib.gdn_fwd_workspace_bytes(ctypes.byref(p)) > 8 * 23 * 128 * 128 * 4
-    # exact mode, or a batch x heads product above the rule: no splitting
+    # the default (exact) mode splits through segment transitions
     p.cp_mode = 0
+    assert lib.gdn_cp_plan(ctypes.byref(p), ctypes.byref(L), ctypes.byref(n)) == 1
+    assert (L.value, n.value) == (23, 23)
+    # no splitting when turned off, or with a batch x heads product above the rule
+    p.cp_mode = 1
     assert lib.gdn_cp_plan(ctypes.byref(p), ctypes.byref(L), ctypes.byref(n)) == 0
     p = _prob(B=2, T=8192, Hq=16, Hv=64, n_seqs=2, cp_mode=2)
     assert lib.gdn_cp_plan(ctypes.byref(p), ctypes.byref(L), ctypes.byref(n)) == 0

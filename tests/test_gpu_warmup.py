@@ -75,3 +75,38 @@ def test_warmup_full_size_sampled():
     _, o, ht, o_ref, ht_ref, _ = run(x, warm=8, groups=[1])
     check("o", o, o_ref, torch.bfloat16, torch.bfloat16)
     check("final_state", ht, ht_ref, torch.bfloat16, torch.float32)
+
+
+# ------------------------------------------------------------------ exact split (default mode)
+def run_exact(x):
+    d = to_dev(x)
+    plan = gdn.cp_plan(d["q"], d["v"], cu_seqlens=d["cu_seqlens"], cp_mode="auto")
+    assert plan is not None
+    _, _, o, _, ht = gdn.chunk_gated_delta_rule_fwd(
+        d["q"], d["k"], d["v"], d["g"], d["beta"], scale=x["scale"], initial_state=d["h0"],
+        cu_seqlens=d["cu_seqlens"], output_final_state=True, cp_mode="auto")
+    torch.cuda.synchronize()
+    o_ref, ht_ref = oracle.oracle_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["scale"], x["h0"],
+                                      cu_seqlens=x["cu_seqlens"])
+    return plan, o, ht, o_ref, ht_ref
+
+
+def test_exact_split_matches_unsplit_with_non_decaying_heads():
+    """Default mode on a shape the trigger splits: exact even for g = 0 heads, where warmup is invalid."""
+    x = make_inputs(workload("longseq_b1_t32k_h8").scaled(T=8192 + 100, Hq=2, Hv=4, seed=43))
+    x["g"][..., 1] = 0.0
+    x["g"][..., 2] *= 0.02
+    plan, o, ht, o_ref, ht_ref = run_exact(x)
+    assert plan == (11, 12)
+    check("o", o, o_ref, torch.bfloat16, torch.bfloat16)
+    check("final_state", ht, ht_ref, torch.bfloat16, torch.float32)
+
+
+def test_exact_split_varlen_no_h0():
+    x = make_inputs(workload("varlen_8seq_32k").scaled(T=2500, Hq=1, Hv=2, seed=44, n_varlen=3))
+    x["cu_seqlens"] = torch.tensor([0, 700, 2200, 2500], dtype=torch.int32)
+    x["h0"] = None
+    plan, o, ht, o_ref, ht_ref = run_exact(x)
+    assert plan == (5, 5)
+    check("o", o, o_ref, torch.bfloat16, torch.bfloat16)
+    check("final_state", ht, ht_ref, torch.bfloat16, torch.float32)

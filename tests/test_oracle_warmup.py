@@ -51,3 +51,22 @@ def test_non_decaying_head_runs_unsplit():
     o, ht = oracle.oracle_fwd(q, k, v, g, beta, 0.5, h0)
     ow, hw = oracle.oracle_fwd_warmup(q, k, v, g, beta, 0.5, h0, seg_len=2, warm=1, chunk=32)
     assert np.allclose(ow[:, :, 1], o[:, :, 1], atol=1e-12) and np.allclose(hw[:, 1], ht[:, 1], atol=1e-12)
+
+
+def test_segment_transition_identity():
+    """The exact split rests on linearity in (v, S): a run from X equals M X + h, with h the run from a
+    zero state and M the run with v = 0 from the identity (K = V)."""
+    q, k, v, g, beta, h0 = rand_problem(35, B=1, T=90, Hq=1, Hv=1, K=6, V=6)
+    _, hx = oracle.oracle_fwd(q, k, v, g, beta, 0.4, h0)
+    _, h = oracle.oracle_fwd(q, k, v, g, beta, 0.4, None)
+    _, M = oracle.oracle_fwd(q, k, np.zeros_like(v), g, beta, 0.4, np.eye(6)[None, None])
+    assert np.allclose(hx[0, 0], M[0, 0] @ h0[0, 0] + h[0, 0], atol=1e-12)
+    # and a two-segment scan reproduces the end state of one run
+    _, h1 = oracle.oracle_fwd(q[:, :40], k[:, :40], v[:, :40], g[:, :40], beta[:, :40], 0.4, None)
+    _, M1 = oracle.oracle_fwd(q[:, :40], k[:, :40], np.zeros_like(v[:, :40]), g[:, :40], beta[:, :40], 0.4,
+                              np.eye(6)[None, None])
+    _, h2 = oracle.oracle_fwd(q[:, 40:], k[:, 40:], v[:, 40:], g[:, 40:], beta[:, 40:], 0.4, None)
+    _, M2 = oracle.oracle_fwd(q[:, 40:], k[:, 40:], np.zeros_like(v[:, 40:]), g[:, 40:], beta[:, 40:], 0.4,
+                              np.eye(6)[None, None])
+    s1 = M1[0, 0] @ h0[0, 0] + h1[0, 0]
+    assert np.allclose(M2[0, 0] @ s1 + h2[0, 0], hx[0, 0], atol=1e-12)
