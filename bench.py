@@ -317,9 +317,41 @@ def run_ours(args, rank, world, local_rank):
     }
     if not args.no_e2e:
         res["e2e"] = run_e2e(args, w, x, dev, gdn, world)
+    if not args.no_autocp and rank == 0:
+        res["autocp"] = run_autocp(dev, gdn)
     if rank == 0 and not args.no_cpu_baseline and world == 1:
         res["cpu_baseline"] = cpu_baseline(w, x, budget_s=args.cpu_budget)
     return res
+
+
+def run_autocp(dev, gdn, steps=10, warmup=3):
+    """Forward of the small-head long-sequence workload (B x Hv = 8 meets the AutoCP
+    trigger) in the three split modes: unsplit, exact split, warmup split (8 chunks).
+    Inputs resident in HBM, CUDA events on the current stream; larger than L2."""
+    aw = workload("longseq_b1_t32k_h8")
+    ax = make_inputs(aw)
+    d = {k: (t.to(dev) if isinstance(t, torch.Tensor) else t) for k, t in ax.items()}
+    out = {"workload": f"{aw.name}: B={aw.B} T={aw.T} Hq={aw.Hq} Hv={aw.Hv} K={aw.K} V={aw.V}, forward"}
+    plan = gdn.cp_plan(d["q"], d["v"], cp_mode="auto")
+    out["segments"] = {"seg_len_chunks": plan[0], "n_seg": plan[1]} if plan else None
+    for mode in ("off", "auto", "warmup"):
+        def f():
+            return gdn.chunk_gated_delta_rule_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], scale=ax["scale"],
+                                                  initial_state=d["h0"], output_final_state=True, cp_mode=mode,
+                                                  warmup_chunks=8)
+        for _ in range(warmup):
+            f()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(steps):
+            f()
+        e1.record()
+        torch.cuda.synchronize(dev)
+        ms = e0.elapsed_time(e1) / steps
+        key = {"off": "unsplit", "auto": "exact_split", "warmup": "warmup_split_8"}[mode]
+        out[key] = {"ms": round(ms, 4), "tokens_per_s": round(aw.tokens / (ms / 1e3), 1)}
+    return out
 
 
 def run_e2e(args, w, x, dev, gdn, world):
@@ -453,6 +485,7 @@ def main():
     ap.add_argument("--workload", default=WORKLOAD)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-autocp", action="store_true", help="skip the split-mode forward timings")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     args = ap.parse_args()
     rank = int(os.environ.get("RANK", 0))
