@@ -325,8 +325,8 @@ def run_ours(args, rank, world, local_rank):
 
 
 def run_autocp(dev, gdn, steps=10, warmup=3):
-    """Forward of the small-head long-sequence workload (B x Hv = 8 meets the AutoCP
-    trigger) in the three split modes: unsplit, exact split, warmup split (8 chunks).
+    """The small-head long-sequence workload (B x Hv = 8 meets the AutoCP trigger): forward
+    unsplit, exact split and warmup split (8 chunks); backward unsplit and exact split.
     Inputs resident in HBM, CUDA events on the current stream; larger than L2."""
     aw = workload("longseq_b1_t32k_h8")
     ax = make_inputs(aw)
@@ -350,6 +350,26 @@ def run_autocp(dev, gdn, steps=10, warmup=3):
         torch.cuda.synchronize(dev)
         ms = e0.elapsed_time(e1) / steps
         key = {"off": "unsplit", "auto": "exact_split", "warmup": "warmup_split_8"}[mode]
+        out[key] = {"ms": round(ms, 4), "tokens_per_s": round(aw.tokens / (ms / 1e3), 1)}
+    # backward: unsplit vs exact split of both chains (warmup does not apply to the backward)
+    g_cum, A, _, _, _ = gdn.chunk_gated_delta_rule_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"],
+                                                       scale=ax["scale"], initial_state=d["h0"])
+    for mode in ("off", "auto"):
+        def b():
+            return gdn.chunk_gated_delta_rule_bwd(d["q"], d["k"], d["v"], g_cum, d["beta"], A, d["do"],
+                                                  dht=d["dht"], scale=ax["scale"], initial_state=d["h0"],
+                                                  cp_mode=mode)
+        for _ in range(warmup):
+            b()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(max(3, steps // 2)):
+            b()
+        e1.record()
+        torch.cuda.synchronize(dev)
+        ms = e0.elapsed_time(e1) / max(3, steps // 2)
+        key = {"off": "bwd_unsplit", "auto": "bwd_exact_split"}[mode]
         out[key] = {"ms": round(ms, 4), "tokens_per_s": round(aw.tokens / (ms / 1e3), 1)}
     return out
 

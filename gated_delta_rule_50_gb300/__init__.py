@@ -208,9 +208,11 @@ def chunk_gated_delta_rule_fwd(q, k, v, g, beta, scale=None, initial_state=None,
 
 def chunk_gated_delta_rule_bwd(q, k, v, g, beta, A, do, dht=None, scale=None, initial_state=None,
                                cu_seqlens=None, cu_seqlens_cpu=None,
-                               workspace: Optional[torch.Tensor] = None):
+                               workspace: Optional[torch.Tensor] = None, cp_mode="auto"):
     """``g`` is the forward's returned chunk-local cumsum.  Returns
-    (dq, dk, dv, db, dg, dh0); dg is the gradient of the raw gate."""
+    (dq, dk, dv, db, dg, dh0); dg is the gradient of the raw gate.  ``cp_mode``
+    "auto" splits long sequences of small batch x heads exactly; any other mode
+    runs the backward unsplit."""
     lib = load_library()
     io = q.dtype
     q, k, v = _cuda(q, "q", io), _cuda(k, "k", io), _cuda(v, "v", io)
@@ -220,7 +222,7 @@ def chunk_gated_delta_rule_bwd(q, k, v, g, beta, A, do, dht=None, scale=None, in
     h0 = _cuda(initial_state, "initial_state", torch.float32)
     dht = _cuda(dht, "dht", torch.float32)
     cu, host = _cu(cu_seqlens, cu_seqlens_cpu)
-    pr = _problem(q, v, scale, cu, host, "auto", 8)
+    pr = _problem(q, v, scale, cu, host, cp_mode, 8)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     db = torch.empty_like(beta)
     dg = torch.empty_like(g)

@@ -75,7 +75,8 @@ struct FwdWs {
     bool exact;          // exact split (transitions) rather than warmup
 };
 struct BwdWs {
-    size_t err, chunk_off, gam64, A32, P32, tiles, vecs, hbuf, dSe, total;
+    size_t err, chunk_off, gam64, A32, P32, tiles, vecs, hbuf, dSe, seg_states, seg_h, seg_M, total;
+    int seg_len, n_seg;  // n_seg > 1: both backward chains are split exactly
 };
 
 // Sequence splitting with warmup runs when asked for, supported and triggered.
@@ -146,6 +147,16 @@ BwdWs bwd_layout(const Plan &p) {
     w.vecs = c.take<float>(units * TC_VEC_FLOATS);
     w.hbuf = c.take<float>(states);
     w.dSe = c.take<float>(states);
+    w.seg_len = 0;
+    w.n_seg = 1;
+    w.seg_states = w.seg_h = w.seg_M = 0;
+    if (exact_split(p)) {  // segment buffers, used in turn by the state recompute and the dS scan
+        cp_geometry(p, &w.seg_len, &w.n_seg);
+        const size_t st = (size_t)p.n_seqs * p.Hv * w.n_seg * p.K * p.V;
+        w.seg_states = c.take<float>(st);
+        w.seg_h = c.take<float>(st);
+        w.seg_M = c.take<float>(st);
+    }
     w.total = c.off;
     return w;
 }
@@ -276,13 +287,40 @@ gdn_status gdn_bwd(const gdn_problem *p, const void *q, const void *k, const voi
         float *vecs = at<float>(workspace, w.vecs);
         GDN_LAUNCH("bwd_prep_tc", launch_tc_prep(pl, q, k, g_cum, true, beta, nullptr, nullptr, nullptr, nullptr,
                                                  tiles, vecs, st));
-        GDN_LAUNCH("bwd_state_tc", launch_tc_fwd(pl, q, k, v, tiles, vecs, h0, nullptr, hbuf, nullptr, st));
+        if (w.n_seg > 1) {  // exact split: segment contributions and transitions, scan, then the segments
+            CpSplit cs;
+            cs.seg_len = w.seg_len;
+            cs.n_seg = w.n_seg;
+            cs.warm = 0;
+            cs.serial = nullptr;
+            cs.seg_states = at<float>(workspace, w.seg_states);
+            cs.seg_h = at<float>(workspace, w.seg_h);
+            cs.seg_M = at<float>(workspace, w.seg_M);
+            cs.mode = CP_SEG;
+            GDN_LAUNCH("bwd_state_seg", launch_tc_fwd(pl, q, k, v, tiles, vecs, nullptr, nullptr, nullptr, nullptr, st,
+                                                      &cs));
+            GDN_LAUNCH("cp_combine", launch_cp_combine(pl, h0, cs.seg_h, cs.seg_M, cs.seg_len, cs.n_seg,
+                                                       cs.seg_states, st));
+            cs.mode = CP_MAIN;
+            GDN_LAUNCH("bwd_state_tc", launch_tc_fwd(pl, q, k, v, tiles, vecs, h0, nullptr, hbuf, nullptr, st, &cs));
+            cs.mode = CP_SEG;  // the dS scan, segments counted from the sequence end
+            GDN_LAUNCH("bwd_dscan_seg", launch_tc_dscan(pl, q, k, d_o, g_cum, beta, tiles, nullptr, nullptr, nullptr,
+                                                        st, &cs));
+            GDN_LAUNCH("cp_combine", launch_cp_combine(pl, dht, cs.seg_h, cs.seg_M, cs.seg_len, cs.n_seg,
+                                                       cs.seg_states, st));
+            cs.mode = CP_MAIN;
+            GDN_LAUNCH("bwd_dscan_tc", launch_tc_dscan(pl, q, k, d_o, g_cum, beta, tiles, dht, dSe, dh0, st, &cs));
+        } else {
+            GDN_LAUNCH("bwd_state_tc", launch_tc_fwd(pl, q, k, v, tiles, vecs, h0, nullptr, hbuf, nullptr, st));
+        }
     } else if (pl.total_chunks > 0) {
         GDN_LAUNCH("bwd_prep", launch_simt_prep(pl, q, k, g_cum, 1, beta, nullptr, nullptr, gam64, A32, P32, st));
         GDN_LAUNCH("bwd_state", launch_simt_scan(pl, q, k, v, beta, gam64, A32, P32, h0, nullptr, hbuf, nullptr,
                                                  st));
     }
-    if (tc_fwd_supported(pl))
+    if (tc_fwd_supported(pl) && w.n_seg > 1) {
+        // split dS scan launched above
+    } else if (tc_fwd_supported(pl))
         GDN_LAUNCH("bwd_dscan_tc", launch_tc_dscan(pl, q, k, d_o, g_cum, beta, at<unsigned char>(workspace, w.tiles), dht,
                                                    dSe, dh0, st));
     else

@@ -62,7 +62,7 @@ bool make_head_map(CUtensorMap *m, const void *ptr, int heads, const Plan &p);
 // tensor-core reverse scan of the state gradient: bf16 io, K = V = 128
 cudaError_t launch_tc_dscan(const Plan &p, const void *q, const void *k, const void *d_o, const float *g_cum,
                             const float *beta, const unsigned char *tiles, const float *dht, float *dSe, float *dh0,
-                            cudaStream_t st);
+                            cudaStream_t st, const CpSplit *cp = nullptr);
 
 // tensor-core per-chunk gradients (dq, dk, dv, dbeta, dg): bf16 io, K = V = 128
 cudaError_t launch_tc_bwd_intra(const Plan &p, const void *q, const void *k, const void *v, const void *d_o,

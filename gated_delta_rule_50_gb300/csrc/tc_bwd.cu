@@ -71,6 +71,10 @@ struct DscanArgs {
     const float *g_cum, *beta, *dht;
     const unsigned char *tiles;  // [chunks][Hv] x 32 KB: A hi / lo, P hi / lo operand images
     float *dSe, *dh0;
+    // sequence splitting (see launch.h), segments counted from the sequence end: seg_len > 0 enables it
+    int seg_len, n_seg, mode;
+    const float *seg_states;  // [n_seqs][Hv][n_seg][K][V] state gradient entering each segment from the right
+    float *seg_h, *seg_M;     // CP_SEG outputs: segment contributions and transitions
 };
 
 __device__ void record_timeout(const Plan &p, int bar_id, int chunk) {
@@ -94,9 +98,45 @@ k_tc_dscan(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
     volatile int *abort_flag = reinterpret_cast<volatile int *>(misc + 1);
     auto bar = [&](int i) { return sb + SM_BAR + 8u * (uint32_t)i; };
 
-    const int s = blockIdx.x, hv = blockIdx.y, hq = hv / p.G;
-    const SeqRange sr = seq_range(p, s);
-    const int nck = sr.c1 - sr.c0;
+    const int hv = blockIdx.y, hq = hv / p.G;
+    // CP_SEG: two CTAs per segment, the second runs the transition (dO = 0, identity start)
+    const int cps = a.mode == CP_SEG ? 2 : 1;
+    const int s = a.seg_len > 0 ? (int)blockIdx.x / (a.n_seg * cps) : (int)blockIdx.x;
+    const int pr = a.seg_len > 0 ? ((int)blockIdx.x / cps) % a.n_seg : 0;  // segment index from the end
+    const bool do_zero = a.mode == CP_SEG && (blockIdx.x & 1);
+    SeqRange sr = seq_range(p, s);
+    const int nseq_ck = sr.c1 - sr.c0;
+    int jb = 0, je = nseq_ck;
+    const size_t st_base = ((size_t)s * p.Hv + hv) * DK * DV;
+    const float *init = a.dht ? a.dht + st_base : nullptr;
+    float *fin = a.dh0 ? a.dh0 + st_base : nullptr;
+    bool init_identity = false, outs = true;
+    if (a.seg_len > 0) {
+        const int L = a.seg_len, P = (nseq_ck + L - 1) / L, ps = P - 1 - pr;  // forward segment index
+        const size_t so = (((size_t)s * p.Hv + hv) * a.n_seg + pr) * DK * DV;
+        if (pr < P) {
+            jb = ps * L;
+            je = min(nseq_ck, (ps + 1) * L);
+        } else {
+            jb = je = 0;
+        }
+        if (a.mode == CP_SEG) {  // every segment but the sequence's first: contribution or transition
+            outs = false;
+            init = nullptr;
+            init_identity = do_zero;
+            fin = (do_zero ? a.seg_M : a.seg_h) + so;
+            if (pr >= P || ps == 0) { jb = je = 0; fin = nullptr; }
+        } else {  // CP_MAIN: the segment holding the sequence start (segment 0 of an empty one) writes dh0
+            if (pr > 0) init = a.seg_states + so;
+            const bool owns_start = nseq_ck == 0 ? pr == 0 : (pr < P && ps == 0);
+            if (!owns_start) fin = nullptr;
+        }
+    }
+    sr.tok0 += jb * C;
+    sr.c0 += jb;
+    sr.c1 = sr.c0 + (je - jb);
+    const int nck = je - jb;
+    float *dSe_out = outs ? a.dSe : nullptr;
     // step t handles chunk j = nck - 1 - t
     auto chunk_tok0 = [&](int t) { return sr.tok0 + (nck - 1 - t) * C; };
 
@@ -110,6 +150,11 @@ k_tc_dscan(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
     if (warp == W_TMA && lane == 0) {
         prefetch_tmap(&tm_k);
         prefetch_tmap(&tm_do);
+    }
+    if (do_zero) {  // the transition run: both dO stages hold zeros and are never loaded
+        for (int i = threadIdx.x; i < 2 * 16384 / 16; i += NUM_THREADS)
+            reinterpret_cast<uint4 *>(sm + SM_DO)[i] = make_uint4(0, 0, 0, 0);
+        fence_proxy_async_smem();
     }
     tc_fence_before();
     __syncthreads();
@@ -127,11 +172,13 @@ k_tc_dscan(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
                     break;
                 }
                 const int tok0 = chunk_tok0(t);
-                mbar_arrive_expect_tx(bar(B_FULL0 + st), 32768);
+                mbar_arrive_expect_tx(bar(B_FULL0 + st), do_zero ? 16384 : 32768);
                 tma_load_3d(sb + SM_K + st * 16384, &tm_k, bar(B_FULL0 + st), 0, hq, tok0);
                 tma_load_3d(sb + SM_K + st * 16384 + 8192, &tm_k, bar(B_FULL0 + st), 64, hq, tok0);
-                tma_load_3d(sb + SM_DO + st * 16384, &tm_do, bar(B_FULL0 + st), 0, hv, tok0);
-                tma_load_3d(sb + SM_DO + st * 16384 + 8192, &tm_do, bar(B_FULL0 + st), 64, hv, tok0);
+                if (!do_zero) {
+                    tma_load_3d(sb + SM_DO + st * 16384, &tm_do, bar(B_FULL0 + st), 0, hv, tok0);
+                    tma_load_3d(sb + SM_DO + st * 16384 + 8192, &tm_do, bar(B_FULL0 + st), 64, hv, tok0);
+                }
                 issued = t + 1;
             }
             for (int t = (issued > 2 ? issued - 2 : 0); t < issued; ++t) mbar_drain(bar(B_FULL0 + (t & 1)), (t >> 1) & 1);
@@ -274,7 +321,6 @@ k_tc_dscan(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
         const int sw = warp - W_STATE0, hh = sw >> 2;
         const uint32_t trow = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
         float *wv = reinterpret_cast<float *>(sm + SM_VEC) + sw * 64;  // E[32], beta Gam[32] of this warp's rows
-        const size_t st_base = ((size_t)s * p.Hv + hv) * DK * DV;
         int failed = -1, fj = 0;
         auto wwait = [&](int id, uint32_t par, int t) {
             bool w = mbar_wait_warp(bar(id), par, abort_flag);
@@ -283,7 +329,8 @@ k_tc_dscan(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
         };
         float S[64];  // dS^T[v][64 hh .. 64 hh + 63]
 #pragma unroll
-        for (int i = 0; i < 64; ++i) S[i] = a.dht ? a.dht[st_base + (size_t)(64 * hh + i) * DV + v] : 0.f;
+        for (int i = 0; i < 64; ++i)
+            S[i] = init ? init[(size_t)(64 * hh + i) * DV + v] : (init_identity && 64 * hh + i == v ? 1.f : 0.f);
         bool ok = true;
         for (int t = 0; t < nck && ok; ++t) {
             const int j = nck - 1 - t, gc = sr.c0 + j, tok0 = chunk_tok0(t), n = min(C, sr.tok1 - tok0);
@@ -304,8 +351,8 @@ k_tc_dscan(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
             }
             tc_fence_before();
             mbar_arrive(bar(B_DSREADY));
-            {
-                float *dst = a.dSe + ((size_t)gc * p.Hv + hv) * DK * DV + (size_t)(64 * hh) * DV + v;
+            if (dSe_out) {
+                float *dst = dSe_out + ((size_t)gc * p.Hv + hv) * DK * DV + (size_t)(64 * hh) * DV + v;
 #pragma unroll
                 for (int i = 0; i < 64; ++i) dst[(size_t)i * DV] = S[i];
             }
@@ -375,9 +422,9 @@ k_tc_dscan(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
             tc_fence_before();
             __syncwarp();
         }
-        if (ok && a.dh0) {
+        if (ok && fin) {
 #pragma unroll
-            for (int i = 0; i < 64; ++i) a.dh0[st_base + (size_t)(64 * hh + i) * DV + v] = S[i];
+            for (int i = 0; i < 64; ++i) fin[(size_t)(64 * hh + i) * DV + v] = S[i];
         }
         if (failed >= 0) record_timeout(p, failed, fj);
     }
@@ -391,7 +438,7 @@ k_tc_dscan(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
 
 cudaError_t launch_tc_dscan(const Plan &p, const void *q, const void *k, const void *d_o, const float *g_cum,
                             const float *beta, const unsigned char *tiles, const float *dht, float *dSe, float *dh0,
-                            cudaStream_t st) {
+                            cudaStream_t st, const CpSplit *cp) {
     CUtensorMap tk, tdo;
     if (!make_head_map(&tk, k, p.Hq, p) || !make_head_map(&tdo, d_o, p.Hv, p)) return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(k_tc_dscan, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
@@ -404,7 +451,20 @@ cudaError_t launch_tc_dscan(const Plan &p, const void *q, const void *k, const v
     a.dht = dht;
     a.dSe = dSe;
     a.dh0 = dh0;
-    dim3 grid(p.n_seqs, p.Hv);
+    a.seg_len = 0;
+    a.n_seg = 1;
+    a.mode = 0;
+    a.seg_states = nullptr;
+    a.seg_h = a.seg_M = nullptr;
+    if (cp) {
+        a.seg_len = cp->seg_len;
+        a.n_seg = cp->n_seg;
+        a.mode = cp->mode;
+        a.seg_states = cp->seg_states;
+        a.seg_h = cp->seg_h;
+        a.seg_M = cp->seg_M;
+    }
+    dim3 grid(p.n_seqs * a.n_seg * (a.mode == CP_SEG ? 2 : 1), p.Hv);
     k_tc_dscan<<<grid, NUM_THREADS, SMEM_BYTES, st>>>(tk, tdo, p, a);
     return cudaGetLastError();
 }

@@ -110,3 +110,13 @@ def test_exact_split_varlen_no_h0():
     assert plan == (5, 5)
     check("o", o, o_ref, torch.bfloat16, torch.bfloat16)
     check("final_state", ht, ht_ref, torch.bfloat16, torch.float32)
+
+
+def test_exact_split_backward():
+    """Both backward chains split through segment transitions (default mode, trigger on)."""
+    from gpu_cases import run_bwd_case
+    x = make_inputs(workload("longseq_b1_t32k_h8").scaled(T=4096 + 100, Hq=2, Hv=4, seed=45))
+    x["g"][..., 1] = 0.0
+    d = to_dev(x)
+    assert gdn.cp_plan(d["q"], d["v"], cp_mode="auto") == (8, 9)
+    run_bwd_case(x)
