@@ -496,6 +496,65 @@ TRAFFIC = {
 }
 
 
+def time_cuda(fn, dev, steps, warmup):
+    """Mean milliseconds of fn() over `steps` calls after `warmup`, CUDA events on the current stream."""
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        fn()
+    e1.record()
+    torch.cuda.synchronize(dev)
+    return e0.elapsed_time(e1) / steps
+
+
+def run_sweep(args):
+    """The pages' benchmark shapes on synthetic data (FlashQLA README, "Benchmark"): value-head counts
+    {64, 48, 32, 24, 16, 8} (tensor parallelism 1 to 8; q/k heads = value heads / 4 as in the
+    training-shaped workload), forward latency over batch lengths at 32768 tokens per batch, and backward
+    latency over the total token count.  One JSON line per shape; inputs resident in HBM."""
+    import gated_delta_rule_50_gb300 as gdn
+    from synth import Workload
+    dev = torch.device("cuda", 0)
+    rows = []
+    heads = (64, 48, 32, 24, 16, 8)
+    for hv in heads:
+        for T in (2048, 8192, 32768):
+            B = 32768 // T
+            w = Workload(f"sweep_fwd_h{hv}_t{T}", B=B, T=T, Hq=hv // 4, Hv=hv, K=128, V=128,
+                         io_dtype=torch.bfloat16, seed=7, has_h0=True, has_dht=False, bwd=False)
+            x = make_inputs(w)
+            d = {k: (t.to(dev) if isinstance(t, torch.Tensor) else t) for k, t in x.items()}
+            ms = time_cuda(lambda: gdn.chunk_gated_delta_rule_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"],
+                                                                   initial_state=d["h0"], output_final_state=True),
+                           dev, args.steps, args.warmup)
+            plan = gdn.cp_plan(d["q"], d["v"], cp_mode="auto")
+            rows.append({"sweep": "fwd", "Hv": hv, "Hq": hv // 4, "B": B, "T": T, "ms": round(ms, 4),
+                         "tokens_per_s": round(B * T / (ms / 1e3), 1),
+                         "split": {"seg_len": plan[0], "n_seg": plan[1]} if plan else None})
+            del d, x
+    for hv in (64, 16, 8):
+        for tokens in (8192, 32768, 65536):
+            T = min(tokens, 32768)
+            B = tokens // T
+            w = Workload(f"sweep_bwd_h{hv}_n{tokens}", B=B, T=T, Hq=hv // 4, Hv=hv, K=128, V=128,
+                         io_dtype=torch.bfloat16, seed=8, has_h0=True, has_dht=True, bwd=True)
+            x = make_inputs(w)
+            d = {k: (t.to(dev) if isinstance(t, torch.Tensor) else t) for k, t in x.items()}
+            g_cum, A, _, _, _ = gdn.chunk_gated_delta_rule_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"],
+                                                               initial_state=d["h0"])
+            ms = time_cuda(lambda: gdn.chunk_gated_delta_rule_bwd(d["q"], d["k"], d["v"], g_cum, d["beta"], A,
+                                                                   d["do"], dht=d["dht"], initial_state=d["h0"]),
+                           dev, max(3, args.steps // 2), args.warmup)
+            rows.append({"sweep": "bwd", "Hv": hv, "Hq": hv // 4, "B": B, "T": T, "tokens": tokens,
+                         "ms": round(ms, 4), "tokens_per_s": round(tokens / (ms / 1e3), 1)})
+            del d, x
+    for r in rows:
+        print(json.dumps(r), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -507,7 +566,12 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-autocp", action="store_true", help="skip the split-mode forward timings")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--sweep", action="store_true",
+                    help="the pages' head-count / batch-length / token-count sweep (one JSON line per shape)")
     args = ap.parse_args()
+    if args.sweep:
+        run_sweep(args)
+        return
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", 1))
     local_rank = int(os.environ.get("LOCAL_RANK", 0))
