@@ -34,13 +34,15 @@ using namespace tc;
 constexpr int DK = 128;
 constexpr int NT = 128;
 
+// The k / q tiles are dead once K K^T and Q K^T are in TMEM, so the fp32 scratch reuses their space.
 constexpr uint32_t S_KQ = 0;                          // [kb0: K 8K, Q 8K][kb1: K 8K, Q 8K]
-constexpr uint32_t S_LM = 32768;                      // fp32 [64][65]: L, then A in place
+constexpr uint32_t S_LM = 0;                          // fp32 [64][65]: L, then A in place
 constexpr uint32_t S_TB = S_LM + 64 * 65 * 4;         // fp32 3 x [16][17]
 constexpr uint32_t S_VEC = S_TB + 3 * 16 * 17 * 4;    // gam, Gam, E, beta (64 each)
-constexpr uint32_t S_BAR = S_VEC + 4 * 64 * 4;
+constexpr uint32_t S_BAR = 32768;
 constexpr uint32_t S_MISC = S_BAR + 16;
 constexpr uint32_t SMEM_BYTES = S_MISC + 32 + 1024;
+static_assert(S_VEC + 4 * 64 * 4 <= S_BAR, "scratch fits in the k / q tile space");
 
 constexpr uint32_t ID_N64 = idesc_bf16(128, 64, 0, 0);
 
@@ -122,7 +124,7 @@ __device__ __forceinline__ void put_split_chunk(unsigned char *hi_tile, unsigned
         make_uint4(pack_bf16(l[0], l[1]), pack_bf16(l[2], l[3]), pack_bf16(l[4], l[5]), pack_bf16(l[6], l[7]));
 }
 
-__global__ void __launch_bounds__(NT, 4)
+__global__ void __launch_bounds__(NT, 6)
 k_tc_prep(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q, Plan p, PrepArgs a) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char *sm = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -169,20 +171,8 @@ k_tc_prep(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
         mma_commit(bar_mma);
     }
     if (ok && warp == 0) ok = mbar_wait_warp(bar_mma, 0, abort_flag);
-    ok = __syncthreads_and(ok) != 0;
+    ok = __syncthreads_and(ok) != 0;  // the MMA has read the k / q tiles: their space is scratch from here
     tc_fence_after();
-    uint32_t raw[64];  // this thread's row of K K^T (t < 64) or Q K^T (t >= 64)
-    if (ok) {
-        uint32_t r0[32], r1[32];
-        tmem_ld32(tmem + ((uint32_t)(32 * warp) << 16), r0);
-        tmem_ld32(tmem + ((uint32_t)(32 * warp) << 16) + 32, r1);
-        tmem_wait_ld();
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            raw[i] = r0[i];
-            raw[32 + i] = r1[i];
-        }
-    }
     for (int g = 0; ok && g < p.G; ++g) {
         const int hv = hq * p.G + g;
         const size_t unit = (size_t)gc * p.Hv + hv;
@@ -217,6 +207,18 @@ k_tc_prep(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
             Ev[t] = t < n ? __expf(glast - gam[t]) : 0.f;
         }
         unsigned char *img = a.tiles + unit * 32768;
+        uint32_t raw[64];  // this thread's row of K K^T (t < 64) or Q K^T (t >= 64), read from TMEM
+        {
+            uint32_t r0[32], r1[32];
+            tmem_ld32(tmem + ((uint32_t)(32 * warp) << 16), r0);
+            tmem_ld32(tmem + ((uint32_t)(32 * warp) << 16) + 32, r1);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                raw[i] = r0[i];
+                raw[32 + i] = r1[i];
+            }
+        }
         if (t < 64) {  // L = beta D o K K^T, strictly lower
             const int r = t;
             const float gr = gam[r], br = bet[r];
