@@ -28,7 +28,7 @@
 //   warp 0      producer: k, q (TMA) and the A / P operand image (bulk copy), 2 stages;
 //               v (TMA) and the gate vectors (bulk copy), 2 stages
 //   warp 1      TMEM allocator and single-thread MMA issuer
-//   warps 2-9   state: S in registers (written to TMEM as the A operand of the
+//   warps 2-17  state: S in registers (written to TMEM as the A operand of the
 //               KS / QS products), R, E Dl, state update, o epilogue (staged in
 //               the consumed v tile, written with 16-byte stores)
 #include <cuda.h>
@@ -44,8 +44,9 @@ namespace {
 using namespace tc;
 
 constexpr int DK = 128, DV = 128;
-constexpr int NUM_THREADS = 320;
+constexpr int NUM_THREADS = 576;
 constexpr int W_TMA = 0, W_MMA = 1, W_STATE0 = 2;
+constexpr uint32_t NSTATE = NUM_THREADS - 64;  // state threads: 16 warps, four per TMEM lane quarter
 
 // shared memory map (bytes from a 1024-aligned base)
 constexpr uint32_t SM_KQ = 0;             // 2 stages x {[kb0: K 8K, Q 8K][kb1: K 8K, Q 8K], A hi / lo, P hi / lo}
@@ -166,7 +167,8 @@ k_tc_fwd(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
     float *h_out = outs ? a.h : nullptr;
 
     if (threadIdx.x == 0) {
-        const uint32_t counts[B_COUNT] = {1, 1, 1, 1, 256, 1, 256, 1, 256, 1, 1, 256, 256, 1, 1, 1, 256, 256};
+        const uint32_t counts[B_COUNT] = {1,      1, 1, 1,      NSTATE, 1, NSTATE, 1,      NSTATE, 1,
+                                          1,      NSTATE, NSTATE, 1, 1,      1, NSTATE, NSTATE};
         for (int i = 0; i < B_COUNT; ++i) mbar_init(bar(i), counts[i]);
         misc[1] = 0;
         fence_mbar_init();
@@ -280,8 +282,10 @@ k_tc_fwd(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
         __syncwarp();
     } else {
         // ------------------------------------------------------------------ state warps
+        // 16 warps: lane quarter warp & 3 holds value columns v; quarter index hh = 0..3 of the warp
+        // within its lane quarter picks keys 32 hh .. 32 hh + 31 and chunk rows 16 hh .. 16 hh + 15.
         const int v = 32 * (warp & 3) + lane;          // value column = TMEM lane
-        const int hh = (warp - W_STATE0) >> 2;         // key half / chunk-row half
+        const int hh = (warp - W_STATE0) >> 2;
         const uint32_t trow = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
         int failed = -1, fj = 0;
         auto wwait = [&](int id, uint32_t par, int j) {  // warp-uniform bounded wait
@@ -290,13 +294,13 @@ k_tc_fwd(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
             return w;
         };
         auto vecs = [&](int jj) { return reinterpret_cast<const float *>(sm + SM_V + (jj & 1) * V_STAGE + VEC_OFF); };
-        float S[64];
+        float S[32];  // S^T[v][32 hh + i]
 #pragma unroll
-        for (int i = 0; i < 64; ++i)
-            S[i] = init ? init[(size_t)(64 * hh + i) * DV + v] : (init_identity && 64 * hh + i == v ? 1.f : 0.f);
+        for (int i = 0; i < 32; ++i)
+            S[i] = init ? init[(size_t)(32 * hh + i) * DV + v] : (init_identity && 32 * hh + i == v ? 1.f : 0.f);
 
-        // o of chunk jj: scale (Gam QS + O) -> bf16.  Each warp stages its 32 rows x 32 values in a private
-        // 2 KB part of the v buffer of chunk jj (consumed: every state thread is past R of jj) and writes
+        // o of chunk jj: scale (Gam QS + O) -> bf16.  Each warp stages its 16 rows x 32 values in a private
+        // 1 KB part of the v buffer of chunk jj (consumed: every state thread is past R of jj) and writes
         // them back as 64-byte row segments with 16-byte stores; no CTA-wide barrier is involved.
         auto epilogue = [&](int jj) -> bool {
             const int tok0 = sr.tok0 + jj * C, n = min(C, sr.tok1 - tok0), b = jj & 1;
@@ -308,25 +312,25 @@ k_tc_fwd(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
             }
             if (!wwait(B_ODONE, jj & 1, jj)) return false;
             tc_fence_after();
-            __nv_bfloat16 *stg = reinterpret_cast<__nv_bfloat16 *>(sm + SM_V + b * V_STAGE + 2048 * (warp - W_STATE0));
-            uint32_t qs[32], oo[32];
-            float gm[32];  // loaded before any store (generic pointers: no reordering across stores)
+            __nv_bfloat16 *stg = reinterpret_cast<__nv_bfloat16 *>(sm + SM_V + b * V_STAGE + 1024 * (warp - W_STATE0));
+            uint32_t qs[16], oo[16];
+            float gm[16];  // loaded before any store (generic pointers: no reordering across stores)
 #pragma unroll
-            for (int i = 0; i < 32; ++i) gm[i] = Gm[32 * hh + i];
-            tmem_ld32(trow + TM_QS + 64 * b + 32 * hh, qs);
-            tmem_ld32(trow + TM_O + 32 * hh, oo);
+            for (int i = 0; i < 16; ++i) gm[i] = Gm[16 * hh + i];
+            tmem_ld16(trow + TM_QS + 64 * b + 16 * hh, qs);
+            tmem_ld16(trow + TM_O + 16 * hh, oo);
             tmem_wait_ld();
             tc_fence_before();
             mbar_arrive(bar(B_EPIFREE0 + b));
 #pragma unroll
-            for (int i = 0; i < 32; ++i)  // row i of this warp's 32, column lane
+            for (int i = 0; i < 16; ++i)  // row i of this warp's 16, column lane
                 stg[i * 32 + lane] =
                     __float2bfloat16_rn(p.scale * fmaf(gm[i], __uint_as_float(qs[i]), __uint_as_float(oo[i])));
             __syncwarp();
             const uint4 *src = reinterpret_cast<const uint4 *>(stg);
 #pragma unroll
-            for (int k4 = 0; k4 < 4; ++k4) {  // lane: row 8 k4 + lane / 4, 8 values at 8 (lane % 4)
-                const int ri = 8 * k4 + (lane >> 2), c = 32 * hh + ri;
+            for (int k2 = 0; k2 < 2; ++k2) {  // lane: row 8 k2 + lane / 4, 8 values at 8 (lane % 4)
+                const int ri = 8 * k2 + (lane >> 2), c = 16 * hh + ri;
                 const uint4 w = src[ri * 4 + (lane & 3)];
                 if (c < n)
                     *reinterpret_cast<uint4 *>(o_out + ((size_t)(tok0 + c) * p.Hv + hv) * DV + 32 * (warp & 3) +
@@ -339,12 +343,12 @@ k_tc_fwd(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
         bool ok = true;
         for (int j = 0; j < nck && ok; ++j) {
             const int tok0 = sr.tok0 + j * C, n = min(C, sr.tok1 - tok0);
-            // (a) S^T row -> hi / lo bf16 pairs in TMEM (keys 64hh .. 64hh + 63: columns 32hh ..)
+            // (a) S^T row -> hi / lo bf16 pairs in TMEM (keys 32hh .. 32hh + 31: columns 16hh ..)
             {
-                uint32_t shi[32], slo[32];
-                split_pack32(S, shi, slo);
-                tmem_st32(trow + TM_SH + 32 * hh, shi);
-                tmem_st32(trow + TM_SL + 32 * hh, slo);
+                uint32_t shi[16], slo[16];
+                split_pack16(S, shi, slo);
+                tmem_st16(trow + TM_SH + 16 * hh, shi);
+                tmem_st16(trow + TM_SL + 16 * hh, slo);
                 tmem_wait_st();
             }
             tc_fence_before();
@@ -352,7 +356,7 @@ k_tc_fwd(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
             if (h_out) {  // while KS is computed: the chunk-entry state (backward recompute)
                 const size_t hb = ((size_t)(sr.c0 + j) * p.Hv + hv) * DK * DV;
 #pragma unroll
-                for (int i = 0; i < 64; ++i) h_out[hb + (size_t)(64 * hh + i) * DV + v] = S[i];
+                for (int i = 0; i < 32; ++i) h_out[hb + (size_t)(32 * hh + i) * DV + v] = S[i];
             }
             // (c) R^T = beta (V - Gam K S)^T
             if (!(ok = wwait(B_VFULL0 + (j & 1), (j >> 1) & 1, j))) break;
@@ -360,23 +364,23 @@ k_tc_fwd(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
             tc_fence_after();
             const float *vj = vecs(j), *Gm = vj + 64, *Ev = vj + 128, *bet = vj + 192;
             uint32_t raw[32];
-            tmem_ld32(trow + TM_KS + 32 * hh, raw);
+            tmem_ld16(trow + TM_KS + 16 * hh, *reinterpret_cast<uint32_t(*)[16]>(raw));
             tmem_wait_ld();
             // v at (row c, column v) of the swizzled tile (two 64-column boxes); rows past the chunk end
             // are finite (next tokens or zero fill) and meet beta = 0
             const unsigned char *vt = sm + SM_V + (j & 1) * V_STAGE + (v >> 6) * 8192;
             // every operand is loaded before the first store (the stores are asm with a memory clobber,
             // which would otherwise order each load behind the previous store)
-            float R[32];
+            float R[16];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                const int c = 32 * hh + i;
+            for (int i = 0; i < 16; ++i) {
+                const int c = 16 * hh + i;
                 const uint32_t vo = (uint32_t)c * 128u + ((uint32_t)(((v & 63) >> 3) ^ (c & 7)) << 4) + (uint32_t)(v & 7) * 2u;
                 const float vv = v_zero ? 0.f : __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(vt + vo));
                 R[i] = bet[c] * (vv - Gm[c] * __uint_as_float(raw[i]));
             }
 #pragma unroll
-            for (int q = 0; q < 4; ++q) st_split_chunk(sb + SM_RT, sb + SM_RT + 16384, v, 4 * hh + q, R + 8 * q);
+            for (int q = 0; q < 2; ++q) st_split_chunk(sb + SM_RT, sb + SM_RT + 16384, v, 2 * hh + q, R + 8 * q);
             tc_fence_before();
             fence_proxy_async_smem();
             mbar_arrive(bar(B_RTREADY));
@@ -385,21 +389,28 @@ k_tc_fwd(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
             // (e) Dl^T -> Dl^T tile (R region) and (E Dl)^T hi / lo pairs in TMEM
             if (!(ok = wwait(B_DLDONE, j & 1, j))) break;
             tc_fence_after();
-            tmem_ld32(trow + TM_DL + 32 * hh, raw);
+            tmem_ld16(trow + TM_DL + 16 * hh, *reinterpret_cast<uint32_t(*)[16]>(raw));
             tmem_wait_ld();
             {
-                float ED[32], Dl[32];
+                float ED[16], Dl[16];
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
+                for (int i = 0; i < 16; ++i) {
                     Dl[i] = __uint_as_float(raw[i]);
-                    ED[i] = Ev[32 * hh + i] * Dl[i];
+                    ED[i] = Ev[16 * hh + i] * Dl[i];
                 }
 #pragma unroll
-                for (int q = 0; q < 4; ++q) st_split_chunk(sb + SM_RT, sb + SM_RT + 16384, v, 4 * hh + q, Dl + 8 * q);
-                uint32_t ehi[16], elo[16];
-                split_pack16(ED, ehi, elo);
-                tmem_st16(trow + TM_EDH + 16 * hh, ehi);
-                tmem_st16(trow + TM_EDL + 16 * hh, elo);
+                for (int q = 0; q < 2; ++q) st_split_chunk(sb + SM_RT, sb + SM_RT + 16384, v, 2 * hh + q, Dl + 8 * q);
+                uint32_t ehi[8], elo[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    float h0, l0, h1, l1;
+                    split2(ED[2 * i], h0, l0);
+                    split2(ED[2 * i + 1], h1, l1);
+                    ehi[i] = pack_bf16(h0, h1);
+                    elo[i] = pack_bf16(l0, l1);
+                }
+                tmem_st8(trow + TM_EDH + 8 * hh, ehi);
+                tmem_st8(trow + TM_EDL + 8 * hh, elo);
                 tmem_wait_st();
             }
             tc_fence_before();
@@ -409,20 +420,16 @@ k_tc_fwd(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
             if (!(ok = wwait(B_UPDDONE, j & 1, j))) break;
             tc_fence_after();
             const float gl = Gm[n - 1];
-            tmem_ld32(trow + TM_U + 64 * hh, raw);
+            tmem_ld32(trow + TM_U + 32 * hh, raw);
             tmem_wait_ld();
 #pragma unroll
             for (int i = 0; i < 32; ++i) S[i] = fmaf(gl, S[i], __uint_as_float(raw[i]));
-            tmem_ld32(trow + TM_U + 64 * hh + 32, raw);
-            tmem_wait_ld();
-#pragma unroll
-            for (int i = 0; i < 32; ++i) S[32 + i] = fmaf(gl, S[32 + i], __uint_as_float(raw[i]));
             tc_fence_before();
         }
         if (ok && nck > 0) ok = epilogue(nck - 1);
         if (ok && fin) {
 #pragma unroll
-            for (int i = 0; i < 64; ++i) fin[(size_t)(64 * hh + i) * DV + v] = S[i];
+            for (int i = 0; i < 32; ++i) fin[(size_t)(32 * hh + i) * DV + v] = S[i];
         }
         if (failed >= 0) record_timeout(p, failed, fj);
     }
