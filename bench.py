@@ -204,16 +204,27 @@ def run_ours(args, rank, world, local_rank):
                        device=dev)
     ws_b = torch.empty(gdn.workspace_bytes("bwd", d["q"], d["v"], d["cu_seqlens"], cu_cpu), dtype=torch.uint8,
                        device=dev)
+    ws_bs = torch.empty(gdn.workspace_bytes("bwd_saved", d["q"], d["v"], d["cu_seqlens"], cu_cpu),
+                        dtype=torch.uint8, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
+    # The training step: the forward keeps its operand images and chunk-entry states for the backward
+    # (the save-for-backward pair, as the autograd function uses it).
     def fwd():
-        return gdn.chunk_gated_delta_rule_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], scale=d["scale"],
-                                              initial_state=d["h0"], cu_seqlens=d["cu_seqlens"],
-                                              cu_seqlens_cpu=cu_cpu, output_final_state=True,
-                                              workspace=ws_f)
+        return gdn.chunk_gated_delta_rule_fwd_saved(d["q"], d["k"], d["v"], d["g"], d["beta"], scale=d["scale"],
+                                                    initial_state=d["h0"], cu_seqlens=d["cu_seqlens"],
+                                                    cu_seqlens_cpu=cu_cpu, output_final_state=True,
+                                                    workspace=ws_f)
 
     def bwd(f):
+        g_cum, A, saved = f[0], f[1], f[4]
+        return gdn.chunk_gated_delta_rule_bwd_saved(d["q"], d["k"], d["v"], g_cum, d["beta"], A, d["do"], saved,
+                                                    dht=d["dht"], scale=d["scale"], initial_state=d["h0"],
+                                                    cu_seqlens=d["cu_seqlens"], cu_seqlens_cpu=cu_cpu,
+                                                    workspace=ws_bs)
+
+    def bwd_recompute(f):  # the pages' backward interface: recomputes A, P and the chunk states
         g_cum, A = f[0], f[1]
         return gdn.chunk_gated_delta_rule_bwd(d["q"], d["k"], d["v"], g_cum, d["beta"], A, d["do"],
                                               dht=d["dht"], scale=d["scale"], initial_state=d["h0"],
@@ -248,6 +259,17 @@ def run_ours(args, rank, world, local_rank):
     clocks = sampler.stop()
     fwd_ms = sum(a.elapsed_time(b) for a, b, _ in evs) / args.steps
     bwd_ms = sum(b.elapsed_time(c) for _, b, c in evs) / args.steps
+    # the recomputing backward, timed alone on the same forward output (reported beside the step)
+    f_last = fwd()
+    rec_ms = 0.0
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        bwd_recompute(f_last)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        rec_ms += e0.elapsed_time(e1) / args.steps
     step_ms = fwd_ms + bwd_ms
     if world > 1:
         t = torch.tensor([step_ms, fwd_ms, bwd_ms], device=dev)
@@ -306,7 +328,10 @@ def run_ours(args, rank, world, local_rank):
         "fwd": {"ms": round(fwd_ms, 4), "tokens_per_s": round(world * tokens / (fwd_ms / 1e3), 1),
                 "roofline_frac": round(t_roof_f / (fwd_ms / 1e3), 4)},
         "bwd": {"ms": round(bwd_ms, 4), "tokens_per_s": round(world * tokens / (bwd_ms / 1e3), 1),
-                "roofline_frac": round(t_roof_b / (bwd_ms / 1e3), 4)},
+                "roofline_frac": round(t_roof_b / (bwd_ms / 1e3), 4),
+                "reuses": "the forward's A / P operand images and chunk-entry states (save for backward)"},
+        "bwd_recompute": {"ms": round(rec_ms, 4), "tokens_per_s": round(world * tokens / (rec_ms / 1e3), 1),
+                          "note": "backward with the pages' interface (recomputes A, P and the chunk states)"},
         "step_roofline_frac": round((t_roof_f + t_roof_b) / (step_ms / 1e3), 4),
         "roofline": roof,
         "kernels": {k: {"launches": c, "ms_total": round(t, 4)} for k, (c, t) in sorted(kprof.items())},
@@ -387,12 +412,12 @@ def run_e2e(args, w, x, dev, gdn, world):
     def step():
         nonlocal outs_host
         d = {k: t.to(dev, non_blocking=True) for k, t in host.items()}
-        g_cum, A, o, _, ht = gdn.chunk_gated_delta_rule_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"],
-                                                            scale=x["scale"], initial_state=d.get("h0"),
-                                                            output_final_state=True, cu_seqlens_cpu=cu_cpu)
-        grads = gdn.chunk_gated_delta_rule_bwd(d["q"], d["k"], d["v"], g_cum, d["beta"], A, d["do"],
-                                               dht=d.get("dht"), scale=x["scale"], initial_state=d.get("h0"),
-                                               cu_seqlens_cpu=cu_cpu)
+        g_cum, A, o, ht, saved = gdn.chunk_gated_delta_rule_fwd_saved(
+            d["q"], d["k"], d["v"], d["g"], d["beta"], scale=x["scale"], initial_state=d.get("h0"),
+            output_final_state=True, cu_seqlens_cpu=cu_cpu)
+        grads = gdn.chunk_gated_delta_rule_bwd_saved(d["q"], d["k"], d["v"], g_cum, d["beta"], A, d["do"], saved,
+                                                     dht=d.get("dht"), scale=x["scale"],
+                                                     initial_state=d.get("h0"), cu_seqlens_cpu=cu_cpu)
         outs = [o, ht] + [t for t in grads if t is not None]
         if outs_host is None:
             outs_host = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]

@@ -27,7 +27,8 @@ import torch
 from . import build as _build
 
 __all__ = ["chunk_gated_delta_rule", "chunk_gated_delta_rule_fwd", "chunk_gated_delta_rule_bwd",
-           "GdnError", "load_library", "library_path", "workspace_bytes", "CHUNK"]
+           "chunk_gated_delta_rule_fwd_saved", "chunk_gated_delta_rule_bwd_saved", "SavedForward",
+           "cp_plan", "cp_trigger", "GdnError", "load_library", "library_path", "workspace_bytes", "CHUNK"]
 
 CHUNK = 64
 GDN_F32, GDN_BF16 = 0, 1
@@ -76,6 +77,10 @@ def load_library():
             lib.gdn_fwd.restype = ctypes.c_int
             lib.gdn_bwd.argtypes = [pp] + [P] * 15 + [P, SZ, P]
             lib.gdn_bwd.restype = ctypes.c_int
+            lib.gdn_bwd_saved_workspace_bytes.argtypes = [pp]
+            lib.gdn_bwd_saved_workspace_bytes.restype = SZ
+            lib.gdn_bwd_saved.argtypes = [pp] + [P] * 10 + [P, SZ] + [P] * 6 + [P, SZ, P]
+            lib.gdn_bwd_saved.restype = ctypes.c_int
             lib.gdn_workspace_error.argtypes = [P, P]
             lib.gdn_workspace_error.restype = ctypes.c_int
             lib.gdn_status_str.argtypes = [ctypes.c_int]
@@ -144,7 +149,8 @@ def workspace_bytes(kind: str, q, v, cu_seqlens=None, cu_seqlens_cpu=None, cp_mo
     lib = load_library()
     cu, host = _cu(cu_seqlens, cu_seqlens_cpu)
     pr = _problem(q, v, None, cu, host, cp_mode, warmup_chunks)
-    fn = lib.gdn_fwd_workspace_bytes if kind == "fwd" else lib.gdn_bwd_workspace_bytes
+    fn = {"fwd": lib.gdn_fwd_workspace_bytes, "bwd": lib.gdn_bwd_workspace_bytes,
+          "bwd_saved": lib.gdn_bwd_saved_workspace_bytes}[kind]
     return int(fn(ctypes.byref(pr)))
 
 
@@ -240,13 +246,75 @@ def chunk_gated_delta_rule_bwd(q, k, v, g, beta, A, do, dht=None, scale=None, in
     return dq, dk, dv, db, dg, dh0
 
 
+class SavedForward:
+    """What a forward leaves for its backward: the workspace (operand images and gate vectors of every
+    chunk) and the chunk-entry states h.  Valid while the forward's inputs are unchanged."""
+
+    def __init__(self, workspace: torch.Tensor, h: torch.Tensor):
+        self.workspace = workspace
+        self.h = h
+
+
+def chunk_gated_delta_rule_fwd_saved(q, k, v, g, beta, scale=None, initial_state=None, cu_seqlens=None,
+                                     output_final_state=True, cp_mode="auto", cu_seqlens_cpu=None,
+                                     workspace: Optional[torch.Tensor] = None):
+    """Forward that keeps what its backward needs.  Returns (g_cum, A, o, final_state, saved); pass
+    ``saved`` to chunk_gated_delta_rule_bwd_saved, which then skips the backward's recompute passes.
+    A given ``workspace`` (large enough) is used and must stay untouched until that backward."""
+    lib = load_library()
+    cu, host = _cu(cu_seqlens, cu_seqlens_cpu)
+    pr = _problem(_cuda(q, "q", q.dtype), v, scale, cu, host, cp_mode, 8)
+    need = int(lib.gdn_fwd_workspace_bytes(ctypes.byref(pr)))
+    ws = workspace if workspace is not None and workspace.numel() >= need else _workspace(need, q.device)
+    g_cum, A, o, h, ht = chunk_gated_delta_rule_fwd(
+        q, k, v, g, beta, scale=scale, initial_state=initial_state, cu_seqlens=cu_seqlens,
+        output_final_state=output_final_state, output_h=True, cp_mode=cp_mode, cu_seqlens_cpu=host,
+        workspace=ws)
+    return g_cum, A, o, ht, SavedForward(ws, h)
+
+
+def chunk_gated_delta_rule_bwd_saved(q, k, v, g, beta, A, do, saved: SavedForward, dht=None, scale=None,
+                                     initial_state=None, cu_seqlens=None, cu_seqlens_cpu=None, cp_mode="auto",
+                                     workspace: Optional[torch.Tensor] = None):
+    """Backward from a chunk_gated_delta_rule_fwd_saved forward on the same inputs (g = its g_cum).
+    Returns (dq, dk, dv, db, dg, dh0), equal to chunk_gated_delta_rule_bwd's up to rounding."""
+    lib = load_library()
+    io = q.dtype
+    q, k, v = _cuda(q, "q", io), _cuda(k, "k", io), _cuda(v, "v", io)
+    do = _cuda(do, "do", io)
+    g, beta = _cuda(g, "g", torch.float32), _cuda(beta, "beta", torch.float32)
+    A = _cuda(A, "A", io)
+    h0 = _cuda(initial_state, "initial_state", torch.float32)
+    dht = _cuda(dht, "dht", torch.float32)
+    cu, host = _cu(cu_seqlens, cu_seqlens_cpu)
+    pr = _problem(q, v, scale, cu, host, cp_mode, 8)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    db = torch.empty_like(beta)
+    dg = torch.empty_like(g)
+    dh0 = torch.empty_like(h0) if h0 is not None else None
+    need = int(lib.gdn_bwd_saved_workspace_bytes(ctypes.byref(pr)))
+    if need == 0:
+        raise GdnError(1, "gdn_bwd_saved_workspace_bytes")
+    ws = workspace if workspace is not None and workspace.numel() >= need else _workspace(need, q.device)
+    st = torch.cuda.current_stream(q.device).cuda_stream
+    fws = saved.workspace
+    rc = lib.gdn_bwd_saved(ctypes.byref(pr), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(A), _ptr(do),
+                           _ptr(dht), _ptr(h0), _ptr(saved.h), _ptr(fws), fws.numel(), _ptr(dq), _ptr(dk),
+                           _ptr(dv), _ptr(db), _ptr(dg), _ptr(dh0), _ptr(ws), ws.numel(), ctypes.c_void_p(st))
+    if rc != 0:
+        raise GdnError(rc, "gdn_bwd_saved")
+    return dq, dk, dv, db, dg, dh0
+
+
 class _GdnFunction(torch.autograd.Function):
     @staticmethod
     def forward(ctx, q, k, v, g, beta, scale, initial_state, output_final_state, cu_seqlens):
-        g_cum, A, o, _, ht = chunk_gated_delta_rule_fwd(
+        # keeps the forward's operand images and chunk-entry states for the backward
+        g_cum, A, o, ht, saved = chunk_gated_delta_rule_fwd_saved(
             q, k, v, g, beta, scale=scale, initial_state=initial_state, cu_seqlens=cu_seqlens,
-            output_final_state=output_final_state, output_A=False)
+            output_final_state=output_final_state)
         ctx.save_for_backward(q, k, v, g_cum, beta, initial_state, cu_seqlens)
+        ctx.saved_fwd = saved
         ctx.scale = scale
         ctx.g_dtype, ctx.beta_dtype = g.dtype, beta.dtype
         return o, ht
@@ -254,9 +322,10 @@ class _GdnFunction(torch.autograd.Function):
     @staticmethod
     def backward(ctx, do, dht):
         q, k, v, g_cum, beta, h0, cu = ctx.saved_tensors
-        dq, dk, dv, db, dg, dh0 = chunk_gated_delta_rule_bwd(
-            q, k, v, g_cum, beta, None, do.contiguous(), dht=dht, scale=ctx.scale, initial_state=h0,
+        dq, dk, dv, db, dg, dh0 = chunk_gated_delta_rule_bwd_saved(
+            q, k, v, g_cum, beta, None, do.contiguous(), ctx.saved_fwd, dht=dht, scale=ctx.scale, initial_state=h0,
             cu_seqlens=cu)
+        ctx.saved_fwd = None
         return (dq, dk, dv, dg.to(ctx.g_dtype), db.to(ctx.beta_dtype), None, dh0, None, None)
 
 

@@ -178,6 +178,31 @@ template <typename T> T *at(void *ws, size_t off) {
         GDN_TRY(expr);                                 \
     } while (0)
 
+// Workspace of gdn_bwd_saved: the backward without its recompute passes.
+struct BwdSavedWs {
+    size_t err, chunk_off, dSe, seg_states, seg_h, seg_M, total;
+    int seg_len, n_seg;
+};
+BwdSavedWs bwd_saved_layout(const Plan &p) {
+    Carve c;
+    BwdSavedWs w;
+    w.err = c.take<uint32_t>(64);
+    w.chunk_off = c.take<int32_t>((size_t)p.n_seqs + 1);
+    w.dSe = c.take<float>((size_t)p.total_chunks * p.Hv * p.K * p.V);
+    w.seg_len = 0;
+    w.n_seg = 1;
+    w.seg_states = w.seg_h = w.seg_M = 0;
+    if (exact_split(p)) {
+        cp_geometry(p, &w.seg_len, &w.n_seg);
+        const size_t st = (size_t)p.n_seqs * p.Hv * w.n_seg * p.K * p.V;
+        w.seg_states = c.take<float>(st);
+        w.seg_h = c.take<float>(st);
+        w.seg_M = c.take<float>(st);
+    }
+    w.total = c.off;
+    return w;
+}
+
 }  // namespace
 
 extern "C" {
@@ -332,6 +357,66 @@ gdn_status gdn_bwd(const gdn_problem *p, const void *q, const void *k, const voi
     else if (pl.total_chunks > 0)
         GDN_LAUNCH("bwd_intra", launch_simt_bwd_intra(pl, q, k, v, d_o, beta, gam64, A32, P32, hbuf, dSe, dq, dk,
                                                      dv, dbeta, dg, st));
+    return GDN_OK;
+}
+
+size_t gdn_bwd_saved_workspace_bytes(const gdn_problem *p) {
+    Plan pl;
+    if (make_plan(p, &pl) != GDN_OK) return 0;
+    return tc_fwd_supported(pl) ? bwd_saved_layout(pl).total : bwd_layout(pl).total;
+}
+
+gdn_status gdn_bwd_saved(const gdn_problem *p, const void *q, const void *k, const void *v, const float *g_cum,
+                         const float *beta, const void *A, const void *d_o, const float *dht, const float *h0,
+                         const float *h, const void *fwd_workspace, size_t fwd_workspace_bytes, void *dq, void *dk,
+                         void *dv, float *dbeta, float *dg, float *dh0, void *workspace, size_t workspace_bytes,
+                         gdn_stream_t stream) {
+    Plan pl;
+    gdn_status s = make_plan(p, &pl);
+    if (s != GDN_OK) return s;
+    if (!tc_fwd_supported(pl) || pl.total_chunks == 0)  // nothing saved to reuse: the recomputing backward
+        return gdn_bwd(p, q, k, v, g_cum, beta, A, d_o, dht, h0, dq, dk, dv, dbeta, dg, dh0, workspace,
+                       workspace_bytes, stream);
+    if (!(ok_ptr(q) && ok_ptr(k) && ok_ptr(v) && ok_ptr(g_cum) && ok_ptr(beta) && ok_ptr(d_o) && ok_ptr(dq) &&
+          ok_ptr(dk) && ok_ptr(dv) && ok_ptr(dbeta) && ok_ptr(dg) && ok_ptr(h)))
+        return GDN_ERR_INVALID_ARG;
+    if (!(ok_opt(A) && ok_opt(dht) && ok_opt(h0) && ok_opt(dh0))) return GDN_ERR_INVALID_ARG;
+    if ((h0 == nullptr) != (dh0 == nullptr)) return GDN_ERR_INVALID_ARG;
+    const FwdWs fw = fwd_layout(pl);
+    if (!fwd_workspace || (reinterpret_cast<uintptr_t>(fwd_workspace) & 255u) || fwd_workspace_bytes < fw.total)
+        return GDN_ERR_WORKSPACE;
+    const BwdSavedWs w = bwd_saved_layout(pl);
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < w.total)
+        return GDN_ERR_WORKSPACE;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    pl.err = at<uint32_t>(workspace, w.err);
+    pl.chunk_off = pl.cu ? at<int32_t>(workspace, w.chunk_off) : nullptr;
+    GDN_TRY(cudaMemsetAsync(pl.err, 0, 256, st));
+    GDN_LAUNCH("chunk_table", launch_chunk_table(pl, st));
+    void *fws = const_cast<void *>(fwd_workspace);
+    const unsigned char *tiles = at<unsigned char>(fws, fw.tiles);
+    const float *vecs = at<float>(fws, fw.vecs);
+    float *dSe = at<float>(workspace, w.dSe);
+    if (w.n_seg > 1) {  // exact split of the dS scan (segments counted from the sequence end)
+        CpSplit cs;
+        cs.seg_len = w.seg_len;
+        cs.n_seg = w.n_seg;
+        cs.warm = 0;
+        cs.serial = nullptr;
+        cs.seg_states = at<float>(workspace, w.seg_states);
+        cs.seg_h = at<float>(workspace, w.seg_h);
+        cs.seg_M = at<float>(workspace, w.seg_M);
+        cs.mode = CP_SEG;
+        GDN_LAUNCH("bwd_dscan_seg", launch_tc_dscan(pl, q, k, d_o, g_cum, beta, tiles, nullptr, nullptr, nullptr, st,
+                                                    &cs));
+        GDN_LAUNCH("cp_combine",
+                   launch_cp_combine(pl, dht, cs.seg_h, cs.seg_M, cs.seg_len, cs.n_seg, cs.seg_states, st));
+        cs.mode = CP_MAIN;
+        GDN_LAUNCH("bwd_dscan_tc", launch_tc_dscan(pl, q, k, d_o, g_cum, beta, tiles, dht, dSe, dh0, st, &cs));
+    } else {
+        GDN_LAUNCH("bwd_dscan_tc", launch_tc_dscan(pl, q, k, d_o, g_cum, beta, tiles, dht, dSe, dh0, st));
+    }
+    GDN_LAUNCH("bwd_intra_tc", launch_tc_bwd_intra(pl, q, k, v, d_o, tiles, vecs, h, dSe, dq, dk, dv, dbeta, dg, st));
     return GDN_OK;
 }
 

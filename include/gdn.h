@@ -171,6 +171,34 @@ gdn_status gdn_fwd_noalloc(const gdn_problem *p,
                            gdn_stream_t stream);
 
 /*
+ * Backward that reuses what the forward saved instead of recomputing it (the
+ * save-for-backward form of gdn_bwd; no counterpart in the pages, whose
+ * backward recomputes).  The forward must have run on the same problem and
+ * inputs with its h output requested; `h` is that output and `fwd_workspace`
+ * that call's workspace, both unchanged since.  The backward then skips its
+ * A / P preparation and its state recompute (it reads the forward's operand
+ * images, gate vectors and chunk-entry states) and runs only the state-
+ * gradient scan and the per-chunk gradients.  Results equal gdn_bwd's up to
+ * rounding, provided the forward's states were exact (cp_mode AUTO or OFF; a
+ * warm-up split forward saves its approximate states, and the gradients then
+ * follow those).  Arguments otherwise as gdn_bwd; the workspace must hold
+ * gdn_bwd_saved_workspace_bytes(p) bytes.  Problems outside the tensor-core
+ * path (fp32 io, other head sizes) run gdn_bwd (h and fwd_workspace unused;
+ * the workspace must then hold gdn_bwd_workspace_bytes(p), which this query
+ * returns for them).
+ */
+size_t gdn_bwd_saved_workspace_bytes(const gdn_problem *p);
+gdn_status gdn_bwd_saved(const gdn_problem *p,
+                         const void *q, const void *k, const void *v,
+                         const float *g_cum, const float *beta, const void *A,
+                         const void *d_o, const float *dht, const float *h0,
+                         const float *h, const void *fwd_workspace,
+                         size_t fwd_workspace_bytes,
+                         void *dq, void *dk, void *dv, float *dbeta, float *dg,
+                         float *dh0, void *workspace, size_t workspace_bytes,
+                         gdn_stream_t stream);
+
+/*
  * Sequence splitting with warmup (the "AutoCP" of the FlashQLA pages: news
  * page, "FlashQLA's core advantages"; blog post, section 1).
  * gdn_cp_trigger: 1 iff the pages' rule turns splitting on for n_seqs
