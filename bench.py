@@ -516,9 +516,7 @@ def run_reference(args, rank, world):
 # capture (profiles/ncu_kernels_train_b1_t4096_h64.md): measured on the half-size training shape and
 # scaled by the 4x units of the full one (per-unit reads and writes do not depend on the unit count).
 # An entry is removed whenever its kernel changes.
-TRAFFIC = {
-    "bwd_intra_tc": 4 * (849.097216e6 + 105.029632e6),
-}
+TRAFFIC = {}
 
 
 def time_cuda(fn, dev, steps, warmup):

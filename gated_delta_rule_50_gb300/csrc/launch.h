@@ -58,6 +58,9 @@ cudaError_t launch_tc_fwd(const Plan &p, const void *q, const void *k, const voi
 
 // TMA map of a [tokens][heads][128] bf16 tensor (64 x 1 x 64 boxes, 128-byte swizzle)
 bool make_head_map(CUtensorMap *m, const void *ptr, int heads, const Plan &p);
+// TMA map of per-chunk fp32 states [units][128 keys][128 values] as a 2-D tensor of units x 128 rows:
+// boxes of 32 values x 128 keys (16 KB), 128-byte swizzle
+bool make_state_map(CUtensorMap *m, const float *ptr, size_t units);
 
 // tensor-core reverse scan of the state gradient: bf16 io, K = V = 128
 cudaError_t launch_tc_dscan(const Plan &p, const void *q, const void *k, const void *d_o, const float *g_cum,

@@ -52,12 +52,13 @@ constexpr uint32_t S_F = 180224;     // fp32 [64][65]: dA, then dL
 constexpr uint32_t S_F2 = S_F + 64 * 65 * 4;   // fp32 [64][65]: dQK staging
 constexpr uint32_t S_VEC = S_F2 + 64 * 65 * 4; // gam, Gam, E, beta, beta Gam (64 each); per-warp partial sums
 constexpr uint32_t S_BAR = S_VEC + (5 * 64 + 2 * NW * 64 + 2 * NW) * 4;
-constexpr uint32_t S_MISC = S_BAR + 16;
+constexpr uint32_t S_MISC = S_BAR + 32;
 constexpr uint32_t S_TOTAL = S_MISC + 16;
 constexpr uint32_t SMEM_BYTES = S_TOTAL + 1024;
 static_assert(SMEM_BYTES <= 232448, "shared memory");
 static_assert(S_F + 2048 * NW <= S_VEC, "transpose buffers fit in the fp32 scratch");
 static_assert(S_P == S_A + 16384 && S_VEC % 16 == 0, "operand image and vector copies");
+static_assert(S_DR % 1024 == 0 && S_F % 1024 == 0 && S_F + 32768 <= S_VEC, "state boxes (128-byte swizzle)");
 
 // TMEM columns
 constexpr uint32_t C_DQ = 0, C_DK = 64, C_HT = 128, C_KS = 256, C_QS = 320, C_DL = 384, C_DR = 448;
@@ -104,17 +105,6 @@ __device__ __forceinline__ float tile_at(const unsigned char *sm, uint32_t off, 
     const uint32_t o = (uint32_t)row * 128u + ((uint32_t)((col >> 3) ^ (row & 7)) << 4) + (uint32_t)(col & 7) * 2u;
     return __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(sm + off + o));
 }
-// element (row, col) of a 64-wide bf16 hi / lo swizzled tile pair, summed
-__device__ __forceinline__ float tile_hl(const unsigned char *sm, uint32_t hi_off, uint32_t lo_off, int row, int col) {
-    return tile_at(sm, hi_off, row, col) + tile_at(sm, lo_off, row, col);
-}
-__device__ __forceinline__ void tile_st_hl(unsigned char *sm, uint32_t hi_off, uint32_t lo_off, int row, int col,
-                                           float x) {
-    const uint32_t o = (uint32_t)row * 128u + ((uint32_t)((col >> 3) ^ (row & 7)) << 4) + (uint32_t)(col & 7) * 2u;
-    const __nv_bfloat16 h = __float2bfloat16_rn(x);
-    *reinterpret_cast<__nv_bfloat16 *>(sm + hi_off + o) = h;
-    *reinterpret_cast<__nv_bfloat16 *>(sm + lo_off + o) = __float2bfloat16_rn(x - __bfloat162float(h));
-}
 // element (row, v) of a [64 rows][128] bf16 tile loaded by two 64-column TMA boxes (8 KB each)
 __device__ __forceinline__ float tile128_at(const unsigned char *sm, uint32_t off, int row, int v) {
     return tile_at(sm, off + (uint32_t)(v >> 6) * 8192u, row, v & 63);
@@ -147,6 +137,17 @@ __device__ __noinline__ void issue_dq_dk(uint32_t sb, uint32_t tmem, uint32_t ac
                                    ID_MM, 1);
         }
         }
+
+// Column v = 32 q + lane of an fp32 state box (32 values x 128 keys, 128-byte rows, 16-byte chunk j of
+// row k at j ^ (k & 7)) for keys 32 hh + i: x[i] = state[32 hh + i][v].  Conflict-free: for each key
+// the warp reads one whole 128-byte row.
+__device__ __forceinline__ void state_col(const unsigned char *box, float (&x)[32]) {
+    const int lane = threadIdx.x & 31, hh = (threadIdx.x >> 5) >> 2;
+    const unsigned char *b = box + (uint32_t)(32 * hh) * 128u + ((lane & 3) << 2);
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+        x[i] = *reinterpret_cast<const float *>(b + i * 128 + ((((lane >> 2) ^ (i & 7))) << 4));
+}
 
 // Row k = lane of a 32 x 32 fp32 block (row stride 128 floats) into x[32]: coalesced loads of 4 rows
 // of 128 bytes per instruction, transposed through the warp's 2 KB swizzled buffer at tb, 16 rows
@@ -181,7 +182,8 @@ __device__ __forceinline__ void key_rows(const float *__restrict__ src, uint32_t
 
 __global__ void __launch_bounds__(NT, 1)
 k_tc_bwd_intra(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
-               const __grid_constant__ CUtensorMap tm_do, const __grid_constant__ CUtensorMap tm_v, Plan p,
+               const __grid_constant__ CUtensorMap tm_do, const __grid_constant__ CUtensorMap tm_v,
+               const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ CUtensorMap tm_dse, Plan p,
                IntraArgs a) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char *sm = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -201,6 +203,8 @@ k_tc_bwd_intra(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     float *rdb = rdb_all + 64 * warp, *rdg = rdg_all + 64 * warp;
     float *Fa = reinterpret_cast<float *>(sm + S_F), *Fb = reinterpret_cast<float *>(sm + S_F2);
     const uint32_t bar_tma = sb + S_BAR, bar_mma = sb + S_BAR + 8;
+    // h (4 boxes) and dSe (2 + 2 boxes, two arrivals) of the current head, fp32 with the 128-byte swizzle
+    const uint32_t bar_h = sb + S_BAR + 16, bar_d = sb + S_BAR + 24;
 
     const int gc = blockIdx.x, hq = blockIdx.y;
     const ChunkPos cp = chunk_pos(p, gc);
@@ -209,6 +213,8 @@ k_tc_bwd_intra(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     if (t == 0) {
         mbar_init(bar_tma, 1);
         mbar_init(bar_mma, 1);
+        mbar_init(bar_h, 1);
+        mbar_init(bar_d, 2);
         misc[1] = 0;
         fence_mbar_init();
     }
@@ -218,6 +224,8 @@ k_tc_bwd_intra(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     tc_fence_after();
     const uint32_t tmem = misc[0];
     uint32_t tma_ph = 0, mma_ph = 0, tma_issued = 0;
+    // state loads: h phases issued / waited for, dSe arrivals (two per phase) / phases waited for
+    uint32_t h_issued = 0, h_waited = 0, d_arrived = 0, d_waited = 0;
     bool ok = true;
 
     // Waits for the MMAs issued so far by thread 0 (which commits first).  Only warp 0 polls the
@@ -273,14 +281,24 @@ k_tc_bwd_intra(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
             tma_load_3d(sb + S_DD + 8192, &tm_v, bar_tma, 64, hv, tok0);
             bulk_load(sb + S_A, a.tiles + unit * 32768, 32768, bar_tma);
             bulk_load(sb + S_VEC, a.vecs + unit * 256, 1024, bar_tma);
+            // h -> S_DR (4 boxes); dSe boxes 0, 1 -> the fp32 scratch (free until the dP stage)
+            mbar_arrive_expect_tx(bar_h, 65536);
+            for (int b = 0; b < 4; ++b) tma_load_2d(sb + S_DR + 16384 * b, &tm_h, bar_h, 32 * b, (int)(unit * DK));
+            mbar_arrive_expect_tx(bar_d, 32768);
+            for (int b = 0; b < 2; ++b) tma_load_2d(sb + S_F + 16384 * b, &tm_dse, bar_d, 32 * b, (int)(unit * DK));
         }
+        ++h_issued;
+        ++d_arrived;
         for (int o = t; o < 2 * NW * 64 + 2 * NW; o += NT) rdb_all[o] = 0.f;  // rdb, rdg, sH, sF
         // ---------------------------------------------------------------- P1: h^T (lane v) -> TMEM; KS, QS
-        {
-            const float *hc = a.hbuf + st_off + (size_t)(32 * hh) * DV + lrow;
+        {  // h^T from its boxes: value v = lrow in box lq, keys 32 hh + i
+            bool w = true;
+            if (warp == 0) w = mbar_wait_warp(bar_h, h_waited & 1, abort_flag);
+            ok = __syncthreads_and(w && ok) != 0;
+            if (!ok) break;
+            ++h_waited;
             float xh[32];
-#pragma unroll
-            for (int i = 0; i < 32; ++i) xh[i] = hc[(size_t)i * DV];
+            state_col(sm + S_DR + 16384u * (uint32_t)lq, xh);
             uint32_t hi[16], lo[16];
             split_pack16(xh, hi, lo);
             tmem_st16(tmem + trow + C_HT + 16 * hh, hi);
@@ -289,20 +307,19 @@ k_tc_bwd_intra(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         }
         __syncthreads();  // vectors visible
         pre_mma();
+        ++d_arrived;
         if (t == 0) {
+            // dSe boxes 2, 3 -> S_DR + 0, S_DR + 32 K (h read; the R^T tiles go to S_DR + 16 K, + 48 K)
+            const int unit = gc * p.Hv + hv;
+            mbar_arrive_expect_tx(bar_d, 32768);
+            tma_load_2d(sb + S_DR, &tm_dse, bar_d, 64, unit * DK);
+            tma_load_2d(sb + S_DR + 32768, &tm_dse, bar_d, 96, unit * DK);
             // [KS^T | QS^T] = h^T [K; Q]^T: one N = 128 product (K and Q rows are adjacent, as are the
             // two accumulators)
             for (int sp = 0; sp < 2; ++sp)
                 for (int blk = 0; blk < 2; ++blk)
                     mma_chain_ta<4, 2>(tmem + C_KS, tmem + C_HT + 64 * sp + 32 * blk, kdesc(sb + S_KQ + 16384 * blk),
                                        ID_N128, (sp | blk) != 0);
-        }
-        // dSe^T (lane v) loads overlap the MMAs; stored to TMEM once h^T has been consumed
-        float xd[32];
-        {
-            const float *dc = a.dSe + st_off + (size_t)(32 * hh) * DV + lrow;
-#pragma unroll
-            for (int i = 0; i < 32; ++i) xd[i] = dc[(size_t)i * DV];
         }
         mma_sync();
         if (!ok) break;
@@ -339,7 +356,15 @@ k_tc_bwd_intra(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
             const float s = warp_transpose_sum16(part);
             if (lane < 16) rdg[16 * hh + lane] += s;
         }
-        {  // dSe^T (lane v) -> TMEM (h^T no longer needed)
+        {  // dSe^T (lane v) from its boxes -> TMEM (h^T no longer needed)
+            bool w = true;
+            if (warp == 0) w = mbar_wait_warp(bar_d, d_waited & 1, abort_flag);
+            ok = __syncthreads_and(w && ok) != 0;
+            if (!ok) break;
+            ++d_waited;
+            const uint32_t box = lq < 2 ? S_F + 16384u * (uint32_t)lq : S_DR + 32768u * (uint32_t)(lq - 2);
+            float xd[32];
+            state_col(sm + box, xd);
             uint32_t hi[16], lo[16];
             split_pack16(xd, hi, lo);
             tmem_st16(tmem + trow + C_HT + 16 * hh, hi);
@@ -438,36 +463,14 @@ k_tc_bwd_intra(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
                 rdg[16 * hh + lane] += sgt;
             }
         }
-        {  // dP (lanes 0..63) and dA (lanes 64..127): thread holds column i, rows r = 16 hh + j
+        {  // dP (lanes 0..63) and dA (lanes 64..127) -> fp32 staging Fb[r][i] = dP[r][i], Fa[r][i] = dA[r][i]
             uint32_t dd[16];
             tmem_ld16(tmem + trow + (lq < 2 ? C_KS : C_QS) + 16 * hh, dd);
             tmem_wait_ld();
-            if (lq < 2) {
-                const int i = lrow;
-                float colsum = 0.f, rowpart[16];
+            float *dst = lq < 2 ? Fb : Fa;
+            const int i = lrow & 63;
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const int r = 16 * hh + j;
-                    float m = 0.f, qk = 0.f;
-                    if (i <= r && r < n) {
-                        const float dpv = p.scale * __uint_as_float(dd[j]);
-                        m = dpv * tile_hl(sm, S_P, S_P + 8192, r, i);
-                        qk = __expf(gam[r] - gam[i]) * dpv;
-                    }
-                    Fb[r * 65 + i] = qk;  // dQK, staged
-                    rowpart[j] = m;
-                    colsum += m;
-                }
-                __syncwarp();
-                rdg[i] -= colsum;
-                __syncwarp();
-                const float s = warp_transpose_sum16(rowpart);
-                if (lane < 16) rdg[16 * hh + lane] += s;
-            } else {
-                const int i = lrow - 64;
-#pragma unroll
-                for (int j = 0; j < 16; ++j) Fa[(16 * hh + j) * 65 + i] = __uint_as_float(dd[j]);  // dA[r][i]
-            }
+            for (int j = 0; j < 16; ++j) dst[(16 * hh + j) * 65 + i] = __uint_as_float(dd[j]);
         }
         __syncthreads();
         {  // dv out: 64 rows x 256 bytes from the staging tile, 16-byte stores
@@ -500,27 +503,60 @@ k_tc_bwd_intra(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
             }
         }
         __syncthreads();
-        // dQK -> hi / lo tile [r][i] in the dO region
-        for (int o = t; o < 64 * 8; o += NT) {
-            const int r = o >> 3, ch = o & 7;
-            float x8[8];
+        // Thread (row r, 8 columns i = 8 c ..): dQK = D o scale dP -> hi / lo tile [r][i] in the dO region;
+        // dgam terms of dP o P (row and column sums); dA~ = lower part of dA -> hi / lo tile [k][l] in the P
+        // region (each thread overwrites exactly the P chunk it has read).
+        {
+            const int r = t >> 3, c = t & 7;
+            float pv[8], qk[8], da[8], m[8];
+            {
+                uint32_t ph[4], pl[4];
+                asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                             : "=r"(ph[0]), "=r"(ph[1]), "=r"(ph[2]), "=r"(ph[3]) : "r"(sw128_addr(sb + S_P, r, c)));
+                asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                             : "=r"(pl[0]), "=r"(pl[1]), "=r"(pl[2]), "=r"(pl[3])
+                             : "r"(sw128_addr(sb + S_P + 8192, r, c)));
 #pragma unroll
-            for (int e = 0; e < 8; ++e) x8[e] = Fb[r * 65 + 8 * ch + e];
-            st_split_chunk(sb + S_DO, sb + S_DO + 8192, r, ch, x8);
+                for (int e = 0; e < 4; ++e) {
+                    pv[2 * e] = bf16_lo_f(ph[e]) + bf16_lo_f(pl[e]);
+                    pv[2 * e + 1] = bf16_hi_f(ph[e]) + bf16_hi_f(pl[e]);
+                }
+            }
+            const float gr = gam[r];
+            float rs = 0.f;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const int i = 8 * c + e;
+                float mm = 0.f, q = 0.f;
+                if (i <= r && r < n) {
+                    const float dpv = p.scale * Fb[r * 65 + i];
+                    mm = dpv * pv[e];
+                    q = __expf(gr - gam[i]) * dpv;
+                }
+                qk[e] = q;
+                m[e] = mm;
+                rs += mm;
+                da[e] = i <= r ? Fa[r * 65 + i] : 0.f;
+            }
+            st_split_chunk(sb + S_DO, sb + S_DO + 8192, r, c, qk);
+            st_split_chunk(sb + S_P, sb + S_P + 8192, r, c, da);
+            rs += __shfl_xor_sync(0xffffffffu, rs, 1);  // row r: the 8 lanes of its columns
+            rs += __shfl_xor_sync(0xffffffffu, rs, 2);
+            rs += __shfl_xor_sync(0xffffffffu, rs, 4);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {  // columns: the warp's 4 rows
+                m[e] += __shfl_xor_sync(0xffffffffu, m[e], 8);
+                m[e] += __shfl_xor_sync(0xffffffffu, m[e], 16);
+            }
+            if ((lane & 7) == 0) rdg[r] += rs;
+            __syncwarp();
+            if (lane < 8)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) rdg[8 * c + e] -= m[e];
         }
         // ---------------------------------------------------------------- P5: dL = -(A^T dA A^T), strictly lower
         // on the tensor cores: Z^T = A dA~^T (dA~ = lower part of dA), then dL^T = -Z^T A.  Both are
         // M = 128 products whose rows 64..127 read neighbouring tiles and are ignored.
-        for (int o = t; o < 64 * 8; o += NT) {  // dA~ hi / lo tile [k][l] in the P region (P is consumed)
-            const int r = o >> 3, ch = o & 7;
-            float x8[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const int i = 8 * ch + e;
-                x8[e] = i <= r ? Fa[r * 65 + i] : 0.f;
-            }
-            st_split_chunk(sb + S_P, sb + S_P + 8192, r, ch, x8);
-        }
         pre_mma();
         if (t == 0) {  // Z^T[i][k] = sum_l A[i][l] dA~[k][l]
             mma_chain<4, 2, 2>(tmem + C_KS, kdesc(sb + S_A), kdesc(sb + S_P), ID_KK, 0);
@@ -570,41 +606,60 @@ k_tc_bwd_intra(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
                                    blk);
         mma_sync();
         if (!ok) break;
-        if (lq < 2) {  // thread: row r = lrow, columns i = 16 hh + j
+        if (lq < 2) {  // K K^T (lanes 0..63: row r = lrow, column i = 16 hh + j) -> fp32 staging Fb[r][i]
             uint32_t kk[16];
             tmem_ld16(tmem + trow + C_KS + 16 * hh, kk);
             tmem_wait_ld();
-            const int r = lrow;
-            float sb_ = 0.f, sg = 0.f, colpart[16];
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                const int i = 16 * hh + j;
-                float m = 0.f;
-                if (i < r && r < n) {
-                    const float w = Fa[r * 65 + i] * __expf(gam[r] - gam[i]) * __uint_as_float(kk[j]);
-                    sb_ += w;
-                    m = w * bet[r];
-                    sg += m;
-                }
-                colpart[j] = m;
-            }
-            rdb[r] += sb_;
-            rdg[r] += sg;
-            __syncwarp();
-            const float s = warp_transpose_sum16(colpart);
-            if (lane < 16) rdg[16 * hh + lane] -= s;
-        }
-        // dKK + dKK^T -> hi / lo tile [r][i] in the P region (dKK_ri = beta_r D_ri dL_ri, i < r)
-        for (int o = t; o < 64 * 64; o += NT) {
-            const int r = o >> 6, i = o & 63;
-            float s = 0.f;
-            if (i < r && r < n) s += bet[r] * __expf(gam[r] - gam[i]) * Fa[r * 65 + i];
-            if (r < i && i < n) s += bet[i] * __expf(gam[i] - gam[r]) * Fa[i * 65 + r];
-            tile_st_hl(sm, S_P, S_P + 8192, r, i, s);
+            for (int j = 0; j < 16; ++j) Fb[lrow * 65 + 16 * hh + j] = __uint_as_float(kk[j]);
         }
         tc_fence_before();  // every K K^T load is done before the columns are overwritten
         __syncthreads();
         tc_fence_after();
+        // Thread (row r, 8 columns i = 8 c ..): dbeta / dgam terms of dL o D o K K^T, and the symmetric tile
+        // dKK + dKK^T (dKK_ri = beta_r D_ri dL_ri for i < r) -> hi / lo [r][i] in the P region
+        {
+            const int r = t >> 3, c = t & 7;
+            const float gr = gam[r], br = bet[r];
+            float x[8], m[8], sb_ = 0.f, sg = 0.f;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const int i = 8 * c + e;
+                float xv = 0.f, mm = 0.f;
+                if (i < r && r < n) {
+                    const float d = __expf(gr - gam[i]);
+                    const float w = Fa[r * 65 + i] * d * Fb[r * 65 + i];
+                    sb_ += w;
+                    mm = w * br;
+                    sg += mm;
+                    xv = br * d * Fa[r * 65 + i];
+                } else if (r < i && i < n) {
+                    xv = bet[i] * __expf(gam[i] - gr) * Fa[i * 65 + r];
+                }
+                x[e] = xv;
+                m[e] = mm;
+            }
+            st_split_chunk(sb + S_P, sb + S_P + 8192, r, c, x);
+#pragma unroll
+            for (int o = 1; o <= 4; o <<= 1) {
+                sb_ += __shfl_xor_sync(0xffffffffu, sb_, o);
+                sg += __shfl_xor_sync(0xffffffffu, sg, o);
+            }
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                m[e] += __shfl_xor_sync(0xffffffffu, m[e], 8);
+                m[e] += __shfl_xor_sync(0xffffffffu, m[e], 16);
+            }
+            if ((lane & 7) == 0) {
+                rdb[r] += sb_;
+                rdg[r] += sg;
+            }
+            __syncwarp();
+            if (lane < 8)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) rdg[8 * c + e] -= m[e];
+        }
+        __syncthreads();  // the fp32 scratch is read before the transposes below reuse it
         // h and dSe (lane = key) -> TMEM as A operands of the dq / dk products.
         // The warp's 32 x 32 blocks are read with coalesced row loads (4 rows of 128 bytes per
         // instruction) and transposed through a private 2 KB swizzled buffer in the fp32 scratch
@@ -721,8 +776,11 @@ k_tc_bwd_intra(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
             p.err[4] = blockIdx.x + blockIdx.y * gridDim.x;
         }
         atomicOr(p.err, ERR_TIMEOUT);
-        // leave nothing in flight: a pending TMA load and every issued MMA
+        // leave nothing in flight: pending TMA loads and every issued MMA
         if (tma_issued > tma_ph) mbar_drain(bar_tma, (tma_issued - 1) & 1);
+        if (h_issued > h_waited) mbar_drain(bar_h, (h_issued - 1) & 1);
+        if (d_arrived & 1) mbar_arrive(bar_d);  // the second half was never issued
+        if ((d_arrived + 1) / 2 > d_waited) mbar_drain(bar_d, ((d_arrived + 1) / 2 - 1) & 1);
         mma_commit(bar_mma);
         mbar_drain(bar_mma, mma_ph & 1);
     }
@@ -741,6 +799,9 @@ cudaError_t launch_tc_bwd_intra(const Plan &p, const void *q, const void *k, con
     if (!make_head_map(&tk, k, p.Hq, p) || !make_head_map(&tq, q, p.Hq, p) || !make_head_map(&tdo, d_o, p.Hv, p) ||
         !make_head_map(&tv, v, p.Hv, p))
         return cudaErrorInvalidValue;
+    CUtensorMap th, tdse;
+    const size_t units = (size_t)p.total_chunks * p.Hv;
+    if (!make_state_map(&th, hbuf, units) || !make_state_map(&tdse, dSe, units)) return cudaErrorInvalidValue;
     cudaError_t e =
         cudaFuncSetAttribute(k_tc_bwd_intra, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
     if (e != cudaSuccess) return e;
@@ -755,7 +816,7 @@ cudaError_t launch_tc_bwd_intra(const Plan &p, const void *q, const void *k, con
     a.dbeta = dbeta;
     a.dg = dg;
     dim3 grid(p.total_chunks, p.Hq);
-    k_tc_bwd_intra<<<grid, NT, SMEM_BYTES, st>>>(tk, tq, tdo, tv, p, a);
+    k_tc_bwd_intra<<<grid, NT, SMEM_BYTES, st>>>(tk, tq, tdo, tv, th, tdse, p, a);
     return cudaGetLastError();
 }
 

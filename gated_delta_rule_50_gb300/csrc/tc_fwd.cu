@@ -468,6 +468,19 @@ bool make_head_map(CUtensorMap *m, const void *ptr, int heads, const Plan &p) {
     return r == CUDA_SUCCESS;
 }
 
+bool make_state_map(CUtensorMap *m, const float *ptr, size_t units) {
+    auto fn = encode_fn();
+    if (!fn || units == 0) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)DV, (cuuint64_t)units * DK};
+    cuuint64_t strides[1] = {(cuuint64_t)DV * 4};
+    cuuint32_t box[2] = {32, (cuuint32_t)DK};
+    cuuint32_t es[2] = {1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(ptr), dims, strides, box, es,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 bool tc_fwd_supported(const Plan &p) { return p.io == GDN_BF16 && p.K == DK && p.V == DV && p.B * p.T > 0; }
 
 cudaError_t launch_tc_fwd(const Plan &p, const void *q, const void *k, const void *v, const unsigned char *tiles,
