@@ -274,18 +274,18 @@ k_tc_bwd_intra(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         ++tma_issued;
         if (t == 0) {  // dO, V tiles; A / P operand images (S_A, S_P are adjacent); gate vectors
             const size_t unit = (size_t)gc * p.Hv + hv;
+            // h -> S_DR (4 boxes) first: it is needed first; dSe boxes 0, 1 -> the fp32 scratch
+            mbar_arrive_expect_tx(bar_h, 65536);
+            for (int b = 0; b < 4; ++b) tma_load_2d(sb + S_DR + 16384 * b, &tm_h, bar_h, 32 * b, (int)(unit * DK));
+            mbar_arrive_expect_tx(bar_d, 32768);
+            for (int b = 0; b < 2; ++b) tma_load_2d(sb + S_F + 16384 * b, &tm_dse, bar_d, 32 * b, (int)(unit * DK));
             mbar_arrive_expect_tx(bar_tma, 32768 + 32768 + 1024);
+            bulk_load(sb + S_VEC, a.vecs + unit * 256, 1024, bar_tma);
             tma_load_3d(sb + S_DO, &tm_do, bar_tma, 0, hv, tok0);
             tma_load_3d(sb + S_DO + 8192, &tm_do, bar_tma, 64, hv, tok0);
             tma_load_3d(sb + S_DD, &tm_v, bar_tma, 0, hv, tok0);
             tma_load_3d(sb + S_DD + 8192, &tm_v, bar_tma, 64, hv, tok0);
             bulk_load(sb + S_A, a.tiles + unit * 32768, 32768, bar_tma);
-            bulk_load(sb + S_VEC, a.vecs + unit * 256, 1024, bar_tma);
-            // h -> S_DR (4 boxes); dSe boxes 0, 1 -> the fp32 scratch (free until the dP stage)
-            mbar_arrive_expect_tx(bar_h, 65536);
-            for (int b = 0; b < 4; ++b) tma_load_2d(sb + S_DR + 16384 * b, &tm_h, bar_h, 32 * b, (int)(unit * DK));
-            mbar_arrive_expect_tx(bar_d, 32768);
-            for (int b = 0; b < 2; ++b) tma_load_2d(sb + S_F + 16384 * b, &tm_dse, bar_d, 32 * b, (int)(unit * DK));
         }
         ++h_issued;
         ++d_arrived;
