@@ -516,7 +516,9 @@ def run_reference(args, rank, world):
 # capture (profiles/ncu_kernels_train_b1_t4096_h64.md): measured on the half-size training shape and
 # scaled by the 4x units of the full one (per-unit reads and writes do not depend on the unit count).
 # An entry is removed whenever its kernel changes.
-TRAFFIC = {}
+TRAFFIC = {
+    "bwd_intra_tc": 4 * (844.657920e6 + 98.588416e6),
+}
 
 
 def time_cuda(fn, dev, steps, warmup):
