@@ -70,22 +70,36 @@ def run_fwd_case(x, cp_mode="auto", warmup_chunks=8, groups=None, check_aux=True
     return dict(g_cum=g_cum, A=A, o=o, ht=ht, h=h, infos=infos)
 
 
-def run_bwd_case(x, fwd=None, groups=None):
+def run_bwd_case(x, fwd=None, groups=None, saved=False):
     """Backward parity: the GPU backward gets the forward's g_cum; the oracle
-    gets the raw gate that g_cum implies (exact fp64 differences)."""
+    gets the raw gate that g_cum implies (exact fp64 differences).  With
+    ``saved`` the save-for-backward pair runs (the training step's launch
+    configuration) and must equal the recomputing backward bit for bit."""
     io = x["q"].dtype
     d = to_dev(x)
     G = x["v"].shape[2] // x["q"].shape[2]
-    if fwd is None:
+    if saved:
+        g_cum, A, _, _, sv = gdn.chunk_gated_delta_rule_fwd_saved(
+            d["q"], d["k"], d["v"], d["g"], d["beta"], scale=x["scale"], initial_state=d["h0"],
+            cu_seqlens=d["cu_seqlens"])
+        grads = gdn.chunk_gated_delta_rule_bwd_saved(
+            d["q"], d["k"], d["v"], g_cum, d["beta"], A, d["do"], sv, dht=d["dht"], scale=x["scale"],
+            initial_state=d["h0"], cu_seqlens=d["cu_seqlens"])
+        del sv
+    elif fwd is None:
         g_cum, A, _, _, _ = gdn.chunk_gated_delta_rule_fwd(
             d["q"], d["k"], d["v"], d["g"], d["beta"], scale=x["scale"], initial_state=d["h0"],
             cu_seqlens=d["cu_seqlens"], output_final_state=False)
     else:
         g_cum, A = fwd["g_cum"], fwd["A"]
-    dq, dk, dv, db, dg, dh0 = gdn.chunk_gated_delta_rule_bwd(
+    ref = gdn.chunk_gated_delta_rule_bwd(
         d["q"], d["k"], d["v"], g_cum, d["beta"], A, d["do"], dht=d["dht"], scale=x["scale"],
         initial_state=d["h0"], cu_seqlens=d["cu_seqlens"])
     torch.cuda.synchronize()
+    if saved:
+        for a, b in zip(grads, ref):
+            assert (a is None) == (b is None) and (a is None or torch.equal(a, b))
+    dq, dk, dv, db, dg, dh0 = ref
     g_rec = recovered_gate(g_cum, x["cu_seqlens"])
     xs = dict(x, g=torch.from_numpy(g_rec))
     hv = None

@@ -120,3 +120,10 @@ def test_fwd_full_size_sampled(name, groups):
 def test_bwd_full_size_sampled(name, groups):
     x = make_inputs(workload(name))
     run_bwd_case(x, groups=groups)
+
+
+def test_training_step_full_size_sampled():
+    """The benchmark's training step (save-for-backward pair) at full size: sampled head group vs the
+    oracle, all gradients bit-equal to the recomputing backward."""
+    x = make_inputs(workload("train_b2_t8192_h64"))
+    run_bwd_case(x, groups=[12], saved=True)
