@@ -84,28 +84,54 @@ __device__ void blocked_inverse(float *Lm, float *Tb, int pt) {
         for (int r = 0; r < 16; ++r) Lm[(base + r) * LS + base + jc] = x[r];
     }
     named_bar(1, 128);
+    // Off-diagonal blocks, right to left.  Warp w computes block row I = J + 1 + w as register tiles: lane
+    // (rq, cq) owns rows 2 rq, 2 rq + 1 and columns 4 cq .. 4 cq + 3 of the block (6 shared loads per 8
+    // FMAs).  Each element is summed in the order K, then k, as the textbook block recursion writes it.
+    const int w = pt >> 5, ln = pt & 31, rq = ln >> 2, cq = ln & 3;
+    float *Tw = Tb + w * 16 * TS;  // this warp's 16 x 16 T block
     for (int J = 2; J >= 0; --J) {
-        const int nblk = 3 - J;  // blocks I = J+1 .. 3
-        for (int o = pt; o < nblk * 256; o += 128) {
-            const int I = J + 1 + (o >> 8), r = (o >> 4) & 15, c = o & 15;
-            float s = 0.f;
-            for (int K = J + 1; K <= I; ++K) {
-                const float *arow = Lm + (16 * I + r) * LS + 16 * K;
-                const float *lcol = Lm + (16 * K) * LS + 16 * J + c;
+        const int I = J + 1 + w;
+        if (I <= 3) {
+            float t0[4] = {0.f, 0.f, 0.f, 0.f}, t1[4] = {0.f, 0.f, 0.f, 0.f};
+            for (int K = J + 1; K <= I; ++K) {  // T_IJ = sum_K A_IK L_KJ
+                const float *arow = Lm + (16 * I + 2 * rq) * LS + 16 * K;
+                const float *lcol = Lm + (16 * K) * LS + 16 * J + 4 * cq;
 #pragma unroll
-                for (int k = 0; k < 16; ++k) s = fmaf(arow[k], lcol[k * LS], s);
+                for (int k = 0; k < 16; ++k) {
+                    const float x0 = arow[k], x1 = arow[LS + k];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float y = lcol[k * LS + e];
+                        t0[e] = fmaf(x0, y, t0[e]);
+                        t1[e] = fmaf(x1, y, t1[e]);
+                    }
+                }
             }
-            Tb[(o >> 8) * 16 * TS + r * TS + c] = s;
-        }
-        named_bar(1, 128);
-        for (int o = pt; o < nblk * 256; o += 128) {
-            const int I = J + 1 + (o >> 8), r = (o >> 4) & 15, c = o & 15;
-            const float *trow = Tb + (o >> 8) * 16 * TS + r * TS;
-            const float *acol = Lm + (16 * J) * LS + 16 * J + c;
-            float s = 0.f;
 #pragma unroll
-            for (int k = 0; k < 16; ++k) s = fmaf(trow[k], acol[k * LS], s);
-            Lm[(16 * I + r) * LS + 16 * J + c] = -s;
+            for (int e = 0; e < 4; ++e) {
+                Tw[(2 * rq) * TS + 4 * cq + e] = t0[e];
+                Tw[(2 * rq + 1) * TS + 4 * cq + e] = t1[e];
+            }
+        }
+        named_bar(1, 128);  // every L_KJ has been read before the A_IJ below overwrite them
+        if (I <= 3) {
+            float o0[4] = {0.f, 0.f, 0.f, 0.f}, o1[4] = {0.f, 0.f, 0.f, 0.f};  // A_IJ = -T_IJ A_JJ
+            const float *acol = Lm + (16 * J) * LS + 16 * J + 4 * cq;
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+                const float x0 = Tw[(2 * rq) * TS + k], x1 = Tw[(2 * rq + 1) * TS + k];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float y = acol[k * LS + e];
+                    o0[e] = fmaf(x0, y, o0[e]);
+                    o1[e] = fmaf(x1, y, o1[e]);
+                }
+            }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                Lm[(16 * I + 2 * rq) * LS + 16 * J + 4 * cq + e] = -o0[e];
+                Lm[(16 * I + 2 * rq + 1) * LS + 16 * J + 4 * cq + e] = -o1[e];
+            }
         }
         named_bar(1, 128);
     }
@@ -124,7 +150,7 @@ __device__ __forceinline__ void put_split_chunk(unsigned char *hi_tile, unsigned
         make_uint4(pack_bf16(l[0], l[1]), pack_bf16(l[2], l[3]), pack_bf16(l[4], l[5]), pack_bf16(l[6], l[7]));
 }
 
-__global__ void __launch_bounds__(NT, 6)
+__global__ void __launch_bounds__(NT, 5)
 k_tc_prep(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q, Plan p, PrepArgs a) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char *sm = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
