@@ -335,38 +335,32 @@ k_tc_dscan(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
         for (int t = 0; t < nck && ok; ++t) {
             const int j = nck - 1 - t, gc = sr.c0 + j, tok0 = chunk_tok0(t), n = min(C, sr.tok1 - tok0);
             // (a) dS^T -> TMEM (hi / lo bf16 pairs) for KdS; dS at this chunk's end -> workspace
-            {
-                uint32_t hi[32], lo[32];
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    float h0, l0, h1, l1;
-                    split2(S[2 * i], h0, l0);
-                    split2(S[2 * i + 1], h1, l1);
-                    hi[i] = pack_bf16(h0, h1);
-                    lo[i] = pack_bf16(l0, l1);
-                }
-                tmem_st32(trow + TM_SH + 32 * hh, hi);
-                tmem_st32(trow + TM_SL + 32 * hh, lo);
-                tmem_wait_st();
+            for (int hf = 0; hf < 2; ++hf) {  // in halves: dS (64 registers) stays live throughout
+                uint32_t hi[16], lo[16];
+                split_pack16(S + 32 * hf, hi, lo);
+                tmem_st16(trow + TM_SH + 32 * hh + 16 * hf, hi);
+                tmem_st16(trow + TM_SL + 32 * hh + 16 * hf, lo);
             }
+            tmem_wait_st();
             tc_fence_before();
             mbar_arrive(bar(B_DSREADY));
-            if (dSe_out) {
-                float *dst = dSe_out + ((size_t)gc * p.Hv + hv) * DK * DV + (size_t)(64 * hh) * DV + v;
-#pragma unroll
-                for (int i = 0; i < 64; ++i) dst[(size_t)i * DV] = S[i];
+            // gate values of this warp's chunk row c = 32 hh + lane (loaded before the dSe stores below)
+            const int cg = 32 * hh + lane;
+            const float glast = a.g_cum[(size_t)(tok0 + n - 1) * p.Hv + hv];
+            float gcv = 0.f, btv = 0.f;
+            if (cg < n) {
+                const size_t gi = (size_t)(tok0 + cg) * p.Hv + hv;
+                gcv = a.g_cum[gi];
+                btv = a.beta[gi];
             }
             // gate vectors of this warp's 32 chunk rows c = 32 hh + lane
             float gl_all;
             {
-                const int c = 32 * hh + lane;
-                const float glast = a.g_cum[(size_t)(tok0 + n - 1) * p.Hv + hv];
                 float e = 0.f, bg = 0.f;
-                if (c < n) {
-                    const size_t gi = (size_t)(tok0 + c) * p.Hv + hv;
-                    const float gcv = a.g_cum[gi];
+                if (cg < n) {
                     e = __expf(glast - gcv);
-                    bg = -a.beta[gi] * __expf(gcv);
+                    bg = -btv * __expf(gcv);
                 }
                 wv[lane] = e;
                 wv[32 + lane] = bg;
@@ -376,23 +370,32 @@ k_tc_dscan(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
             // (c) dDl^T = scale PdO^T + KdS^T diag(E)
             if (!(ok = wwait(B_KDDONE, t & 1, t))) break;
             tc_fence_after();
-            uint32_t kd[32], pd[32];
-            tmem_ld32(trow + TM_KD + 32 * hh, kd);
-            tmem_ld32(trow + TM_PD + 32 * hh, pd);
-            tmem_wait_ld();
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-                float x[8];
+            for (int hf = 0; hf < 2; ++hf) {
+                uint32_t kd16[16], pd16[16];
+                tmem_ld16(trow + TM_KD + 32 * hh + 16 * hf, kd16);
+                tmem_ld16(trow + TM_PD + 32 * hh + 16 * hf, pd16);
+                tmem_wait_ld();
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const int i = 8 * q4 + e;
-                    x[e] = fmaf(p.scale, __uint_as_float(pd[i]), wv[i] * __uint_as_float(kd[i]));
+                for (int q2 = 0; q2 < 2; ++q2) {
+                    float x[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const int i = 8 * q2 + e;
+                        x[e] = fmaf(p.scale, __uint_as_float(pd16[i]), wv[16 * hf + i] * __uint_as_float(kd16[i]));
+                    }
+                    st_split_chunk(sb + SM_DD, sb + SM_DD + 16384, v, 4 * hh + 2 * hf + q2, x);
                 }
-                st_split_chunk(sb + SM_DD, sb + SM_DD + 16384, v, 4 * hh + q4, x);
             }
+            uint32_t kd[32];
             tc_fence_before();
             fence_proxy_async_smem();
             mbar_arrive(bar(B_DDREADY));
+            if (dSe_out) {  // while dR is computed: dS at this chunk's end -> workspace
+                float *dst = dSe_out + ((size_t)gc * p.Hv + hv) * DK * DV + (size_t)(64 * hh) * DV + v;
+#pragma unroll
+                for (int i = 0; i < 64; ++i) dst[(size_t)i * DV] = S[i];
+            }
             // (e) Y = -beta Gam o dR
             if (!(ok = wwait(B_DRDONE, t & 1, t))) break;
             tc_fence_after();
