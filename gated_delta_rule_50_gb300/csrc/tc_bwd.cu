@@ -273,6 +273,20 @@ k_tc_dscan(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
             if (!w && failed < 0) { failed = id; fj = t; }
             return named_bar_and(1, 128, w);
         };
+        // q row half and gate of tile row r, loaded one chunk ahead (the loads' latency overlaps a step)
+        uint4 qn[8];
+        float gn = 0.f;
+        auto load_q = [&](int t) {
+            const int tok0 = chunk_tok0(t), n = min(C, sr.tok1 - tok0);
+            if (r < n) {
+                gn = a.g_cum[(size_t)(tok0 + r) * p.Hv + hv];
+                const uint4 *qrow =
+                    reinterpret_cast<const uint4 *>(a.q + ((size_t)(tok0 + r) * p.Hq + hq) * DK + 64 * hh);
+#pragma unroll
+                for (int ch = 0; ch < 8; ++ch) qn[ch] = qrow[ch];
+            }
+        };
+        if (nck > 0) load_q(0);
         for (int t = 0; t < nck; ++t) {
             const int j = nck - 1 - t, gc = sr.c0 + j, tok0 = chunk_tok0(t), n = min(C, sr.tok1 - tok0);
             const int sl = t & 1;
@@ -289,14 +303,12 @@ k_tc_dscan(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
             if (t >= 1 && !gwait(B_DRDONE, (t - 1) & 1, t)) break;
             {
                 float gsc = 0.f;
-                if (r < n) gsc = p.scale * __expf(a.g_cum[(size_t)(tok0 + r) * p.Hv + hv]);
-                const uint4 *qrow = reinterpret_cast<const uint4 *>(a.q + ((size_t)(tok0 + r) * p.Hq + hq) * DK +
-                                                                   64 * hh);
+                if (r < n) gsc = p.scale * __expf(gn);
 #pragma unroll
                 for (int ch = 0; ch < 8; ++ch) {
                     float x[8];
                     if (r < n) {
-                        uint4 w = qrow[ch];
+                        uint4 w = qn[ch];
                         const uint32_t u[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
@@ -312,6 +324,7 @@ k_tc_dscan(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
             }
             fence_proxy_async_smem();
             mbar_arrive(bar(B_GQREADY));
+            if (t + 1 < nck) load_q(t + 1);
         }
         if (pt == 0 && ap_issued > 0) mbar_drain(bar(B_APREADY), (ap_issued - 1) & 1);  // no copy left in flight
         if (failed >= 0) record_timeout(p, failed, fj);
