@@ -13,6 +13,7 @@
 //   dL = -(A^T dA A^T) strictly lower                     (CUDA cores)
 //   dq^T += h (scale Gam o dO)^T + K^T dQK^T               dQK = D o scale dP
 //   dk^T += dSe (E o Dl)^T - h (beta Gam o dR)^T + Q^T dQK + K^T (dKK + dKK^T),  dKK = beta D o dL
+//   (the two h products run as one N = 128 product over the adjacent dq^T, dk^T accumulators)
 //
 // and the gate / beta gradients as row sums (dg is the reverse cumsum of dgam
 // inside the chunk).  dq and dk accumulate over the group's value heads in
@@ -46,8 +47,8 @@ constexpr uint32_t S_KQ = 0;         // [kb0: K 8K, Q 8K][kb1: K 8K, Q 8K]
 constexpr uint32_t S_DO = 32768;     // dO [r][v] 2 x 8K; later dQK hi / lo [r][i]
 constexpr uint32_t S_A = 49152;      // A hi / lo [r][i]
 constexpr uint32_t S_P = 65536;      // P hi / lo [r'][r]; later (dKK + dKK^T) hi / lo
-constexpr uint32_t S_DR = 81920;     // Dl^T hi | R^T hi | Dl^T lo | R^T lo ([v][i], 16K each); later E Dl, Y
-constexpr uint32_t S_DD = 147456;    // V [r][v] (TMA); dDl^T hi / lo [v][r]; dv staging; scale Gam dO hi / lo [r][v]
+constexpr uint32_t S_DR = 81920;     // Dl^T hi | R^T hi | Dl^T lo | R^T lo ([v][i], 16K each); later scale Gam dO, Y
+constexpr uint32_t S_DD = 147456;    // V [r][v] (TMA); dDl^T hi / lo [v][r]; dv staging; (E Dl)^T hi / lo [v][i]
 constexpr uint32_t S_F = 180224;     // fp32 [64][65]: dA, then dL
 constexpr uint32_t S_F2 = S_F + 64 * 65 * 4;   // fp32 [64][65]: dQK staging
 constexpr uint32_t S_VEC = S_F2 + 64 * 65 * 4; // gam, Gam, E, beta, beta Gam (64 each); per-warp partial sums
@@ -68,6 +69,7 @@ constexpr uint32_t ID_MK = idesc_bf16(128, 64, 1, 0);
 constexpr uint32_t ID_MM = idesc_bf16(128, 64, 1, 1);
 constexpr uint32_t ID_KM = idesc_bf16(128, 64, 0, 1);
 constexpr uint32_t ID_N128 = idesc_bf16(128, 128, 0, 0);
+constexpr uint32_t ID_KM128 = idesc_bf16(128, 128, 0, 1);
 static_assert(C_QS == C_KS + 64, "KS and QS accumulators must be adjacent");
 
 struct IntraArgs {
@@ -113,21 +115,17 @@ __device__ __forceinline__ float tile128_at(const unsigned char *sm, uint32_t of
 // dq^T, dk^T accumulation of one value head (issued by one thread).  A separate, non-inlined
 // function keeps the issue sequence compact and out of the kernel's register pressure.
 __device__ __noinline__ void issue_dq_dk(uint32_t sb, uint32_t tmem, uint32_t acc0) {
-        for (int tt = 0; tt < 3; ++tt)  // dq^T += h (scale Gam dO)^T
-            for (int blk = 0; blk < 2; ++blk)
-                mma_chain_ta<4, 2>(tmem + C_DQ, tmem + C_HT + (tt == 2 ? 64 : 0) + 32 * blk,
-                                   kdesc(sb + S_DD + (tt == 1 ? 16384 : 0) + 8192 * blk), ID_KK,
-                                   acc0 | (uint32_t)((tt | blk) != 0));
+        // [dq^T | dk^T] += h [scale Gam dO | Y]^T: one N = 128 product, the two value-major B tiles are
+        // adjacent 64-wide blocks (hi at S_DR, lo at S_DR + 32 K)
+        mma_chain_ta<8, 128>(tmem + C_DQ, tmem + C_HT, mdesc(sb + S_DR, 16384), ID_KM128, acc0);
+        mma_chain_ta<8, 128>(tmem + C_DQ, tmem + C_HT + 64, mdesc(sb + S_DR, 16384), ID_KM128, 1);
+        mma_chain_ta<8, 128>(tmem + C_DQ, tmem + C_HT, mdesc(sb + S_DR + 32768, 16384), ID_KM128, 1);
         for (int sp = 0; sp < 2; ++sp)  // dq^T += K^T dQK^T
             mma_chain<4, 128, 2>(tmem + C_DQ, mdesc(sb + S_KQ, 16384), kdesc(sb + S_DO + 8192 * sp), ID_MK, 1);
         // dk^T += dSe (E Dl)^T
-        mma_chain_ta<8, 128>(tmem + C_DK, tmem + C_KS, mdesc(sb + S_DR, 8192), ID_KM, acc0);
-        mma_chain_ta<8, 128>(tmem + C_DK, tmem + C_KS, mdesc(sb + S_DR + 32768, 8192), ID_KM, 1);
-        mma_chain_ta<8, 128>(tmem + C_DK, tmem + C_KS + 64, mdesc(sb + S_DR, 8192), ID_KM, 1);
-        // dk^T += h Y^T, Y = -beta Gam dR
-        mma_chain_ta<8, 128>(tmem + C_DK, tmem + C_HT, mdesc(sb + S_DR + 16384, 8192), ID_KM, 1);
-        mma_chain_ta<8, 128>(tmem + C_DK, tmem + C_HT, mdesc(sb + S_DR + 49152, 8192), ID_KM, 1);
-        mma_chain_ta<8, 128>(tmem + C_DK, tmem + C_HT + 64, mdesc(sb + S_DR + 16384, 8192), ID_KM, 1);
+        mma_chain_ta<8, 128>(tmem + C_DK, tmem + C_KS, mdesc(sb + S_DD, 8192), ID_KM, 1);
+        mma_chain_ta<8, 128>(tmem + C_DK, tmem + C_KS, mdesc(sb + S_DD + 16384, 8192), ID_KM, 1);
+        mma_chain_ta<8, 128>(tmem + C_DK, tmem + C_KS + 64, mdesc(sb + S_DD, 8192), ID_KM, 1);
         for (int sp = 0; sp < 2; ++sp) {
             // dk^T += Q^T dQK
             mma_chain<4, 128, 128>(tmem + C_DK, mdesc(sb + S_KQ + 8192, 16384), mdesc(sb + S_DO + 8192 * sp, 8192),
@@ -434,26 +432,26 @@ k_tc_bwd_intra(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         if (!ok) break;
         // ---------------------------------------------------------------- P4: dV, dbeta, dgam terms, E Dl / Y tiles
         {
-            uint32_t dr[16], dl[16];
+            uint32_t dr[16];
             tmem_ld16(tmem + trow + C_DR + 16 * hh, dr);
-            tmem_ld16(tmem + trow + C_DL + 16 * hh, dl);
             tmem_wait_ld();
             float pb[16], pg[16];
             __nv_bfloat16 *dvs = reinterpret_cast<__nv_bfloat16 *>(sm + S_DD);  // dv staging [r][128]
 #pragma unroll
             for (int q2 = 0; q2 < 2; ++q2) {
-                float y8[8], e8[8];
+                float y8[8], s8[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
                     const int i = 8 * q2 + e, c = 16 * hh + i;
                     const float drv = __uint_as_float(dr[i]);
+                    s8[e] = p.scale * Gm[c] * tile128_at(sm, S_DO, c, lrow);  // scale Gam dO (Gm = 0 past n)
                     dvs[c * DV + lrow] = __float2bfloat16_rn(bet[c] * drv);
                     pb[i] = drv * Xr[i];
                     pg[i] = -bg[c] * drv * KSr[i];
                     y8[e] = -bg[c] * drv;
-                    e8[e] = Ev[c] * __uint_as_float(dl[i]);
                 }
-                st_split_chunk(sb + S_DR, sb + S_DR + 32768, lrow, 2 * hh + q2, e8);
+                // value-major tiles [v][i]: scale Gam dO and Y = -beta Gam dR side by side (N = 128 B operand)
+                st_split_chunk(sb + S_DR, sb + S_DR + 32768, lrow, 2 * hh + q2, s8);
                 st_split_chunk(sb + S_DR + 16384, sb + S_DR + 49152, lrow, 2 * hh + q2, y8);
             }
             const float sbt = warp_transpose_sum16(pb);
@@ -483,23 +481,16 @@ k_tc_bwd_intra(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
             }
         }
         __syncthreads();
-        // scale Gam o dO tile [r][v] into the dDl region (its last reader, dA^T, is done)
-        {
-            const int r = t >> 3, q = t & 7;  // 16 values: block q >> 2, chunks 2 (q & 3), + 1
-            const float gs = p.scale * Gm[r];
-            const int vb = q >> 2;
+        {  // (E Dl)^T -> value-major hi / lo tile [v][i] in the dDl region (the dv staging has been written out)
+            uint32_t dl[16];
+            tmem_ld16(tmem + trow + C_DL + 16 * hh, dl);
+            tmem_wait_ld();
 #pragma unroll
-            for (int c2 = 0; c2 < 2; ++c2) {
-                const int ch = 2 * (q & 3) + c2;
-                const uint4 w = *reinterpret_cast<const uint4 *>(sm + S_DO + vb * 8192 + r * 128 + ((ch ^ (r & 7)) << 4));
-                const uint32_t u[4] = {w.x, w.y, w.z, w.w};
-                float x8[8];
+            for (int q2 = 0; q2 < 2; ++q2) {
+                float e8[8];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    x8[2 * e] = gs * bf16_lo_f(u[e]);
-                    x8[2 * e + 1] = gs * bf16_hi_f(u[e]);
-                }
-                st_split_chunk(sb + S_DD + vb * 8192, sb + S_DD + 16384 + vb * 8192, r, ch, x8);
+                for (int e = 0; e < 8; ++e) e8[e] = Ev[16 * hh + 8 * q2 + e] * __uint_as_float(dl[8 * q2 + e]);
+                st_split_chunk(sb + S_DD, sb + S_DD + 16384, lrow, 2 * hh + q2, e8);
             }
         }
         __syncthreads();
