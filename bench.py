@@ -609,8 +609,15 @@ def run_sweep(args):
             ms = time_cuda(lambda: gdn.chunk_gated_delta_rule_bwd(d["q"], d["k"], d["v"], g_cum, d["beta"], A,
                                                                    d["do"], dht=d["dht"], initial_state=d["h0"]),
                            dev, max(3, args.steps // 2), args.warmup)
+            g_cum, A, _, _, saved = gdn.chunk_gated_delta_rule_fwd_saved(d["q"], d["k"], d["v"], d["g"], d["beta"],
+                                                                         initial_state=d["h0"])
+            ms_saved = time_cuda(lambda: gdn.chunk_gated_delta_rule_bwd_saved(
+                d["q"], d["k"], d["v"], g_cum, d["beta"], A, d["do"], saved, dht=d["dht"], initial_state=d["h0"]),
+                dev, max(3, args.steps // 2), args.warmup)
             rows.append({"sweep": "bwd", "Hv": hv, "Hq": hv // 4, "B": B, "T": T, "tokens": tokens,
-                         "ms": round(ms, 4), "tokens_per_s": round(tokens / (ms / 1e3), 1)})
+                         "ms": round(ms, 4), "tokens_per_s": round(tokens / (ms / 1e3), 1),
+                         "saved_ms": round(ms_saved, 4), "saved_tokens_per_s": round(tokens / (ms_saved / 1e3), 1)})
+            del saved
             del d, x
     for r in rows:
         print(json.dumps(r), flush=True)
