@@ -344,6 +344,8 @@ def run_ours(args, rank, world, local_rank):
         res["e2e"] = run_e2e(args, w, x, dev, gdn, world)
     if not args.no_autocp and rank == 0:
         res["autocp"] = run_autocp(dev, gdn)
+    if not args.no_head64 and rank == 0:
+        res["head_dim_64"] = run_head64(dev, gdn)
     if rank == 0 and not args.no_cpu_baseline and world == 1:
         res["cpu_baseline"] = cpu_baseline(w, x, budget_s=args.cpu_budget)
     return res
@@ -399,6 +401,74 @@ def run_autocp(dev, gdn, steps=10, warmup=3):
     return out
 
 
+def run_head64(dev, gdn, steps=10, warmup=3):
+    """The training-shaped workload with 64-wide heads (K = V = 64): the 128-wide tensor-core kernels
+    on zero-padded copies (the library pads and slices), forward and the save-for-backward training
+    step's backward.  Inputs resident in HBM, CUDA events on the current stream."""
+    hw = workload("train_b2_t8192_h64").scaled(name="train_b2_t8192_h64_d64", K=64, V=64)
+    hx = make_inputs(hw)
+    d = {k: (t.to(dev) if isinstance(t, torch.Tensor) else t) for k, t in hx.items()}
+    out = {"workload": f"{hw.name}: B={hw.B} T={hw.T} Hq={hw.Hq} Hv={hw.Hv} K={hw.K} V={hw.V}",
+           "path": "128-wide tensor-core kernels on zero-padded operands"}
+    fwd = lambda: gdn.chunk_gated_delta_rule_fwd_saved(d["q"], d["k"], d["v"], d["g"], d["beta"], scale=hx["scale"],
+                                                       initial_state=d["h0"], output_final_state=True)
+    f = fwd()
+    bwd = lambda: gdn.chunk_gated_delta_rule_bwd_saved(d["q"], d["k"], d["v"], f[0], d["beta"], f[1], d["do"], f[4],
+                                                       dht=d["dht"], scale=hx["scale"], initial_state=d["h0"])
+    for key, fn in (("fwd", fwd), ("bwd", bwd)):
+        ms = time_cuda(fn, dev, steps, warmup)
+        out[key] = {"ms": round(ms, 4), "tokens_per_s": round(hw.tokens / (ms / 1e3), 1)}
+    return out
+
+
+def _cpulist(text):
+    cpus = set()
+    for part in text.strip().split(","):
+        if part:
+            a, _, b = part.partition("-")
+            cpus.update(range(int(a), int(b or a) + 1))
+    return cpus
+
+
+def bind_near_gpu(dev):
+    """Best effort: restricts this process to the CPUs local to the GPU (its PCI device's local_cpulist in
+    sysfs), so that pinned host buffers allocated now sit in the GPU's nearest host memory.  Returns the
+    previous affinity (to restore) or None."""
+    try:
+        bus = subprocess.run(["nvidia-smi", f"--id={dev.index}", "--query-gpu=pci.bus_id", "--format=csv,noheader"],
+                             capture_output=True, text=True, timeout=20).stdout.strip()
+        dom, rest = bus.split(":", 1)
+        with open(f"/sys/bus/pci/devices/{int(dom, 16):04x}:{rest.lower()}/local_cpulist") as fh:
+            near = _cpulist(fh.read())
+        old = os.sched_getaffinity(0)
+        if near & old and near & old != old:
+            os.sched_setaffinity(0, near & old)
+            return old
+    except Exception:
+        pass
+    return None
+
+
+def copy_rates(host, dev):
+    """Isolated host->device and device->host copy rates (GB/s) of the given pinned tensors."""
+    devs = [torch.empty_like(t, device=dev) for t in host]
+    nbytes = sum(t.numel() * t.element_size() for t in host)
+    rates = []
+    for direction in ("h2d", "d2h"):
+        for _ in range(2):
+            for a, b in zip(host, devs):
+                (b.copy_(a, non_blocking=True) if direction == "h2d" else a.copy_(b, non_blocking=True))
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for a, b in zip(host, devs):
+            (b.copy_(a, non_blocking=True) if direction == "h2d" else a.copy_(b, non_blocking=True))
+        e1.record()
+        torch.cuda.synchronize(dev)
+        rates.append(round(nbytes / (e0.elapsed_time(e1) / 1e3) / 1e9, 1))
+    return rates
+
+
 def run_e2e(args, w, x, dev, gdn, world):
     """Same step through the public API with host (pinned) buffers: every step copies its inputs
     host->device and all its outputs device->host inside the timed region.  The steps are pipelined
@@ -406,6 +476,7 @@ def run_e2e(args, w, x, dev, gdn, world):
     stream) and step k-1's outputs read back (another stream) while step k computes, with two device
     input buffers."""
     names_in = ["q", "k", "v", "g", "beta", "h0", "do", "dht"]
+    old_affinity = bind_near_gpu(dev)  # restored once every pinned buffer exists (after the warm-up)
     host = {k: x[k].pin_memory() for k in names_in if x[k] is not None}
     cu_cpu = x["cu_seqlens"]
     h2d = sum(t.numel() * t.element_size() for t in host.values())
@@ -461,6 +532,9 @@ def run_e2e(args, w, x, dev, gdn, world):
 
     run(max(3, args.warmup))
     torch.cuda.synchronize()
+    if old_affinity is not None:
+        os.sched_setaffinity(0, old_affinity)
+    h2d_gbs, d2h_gbs = copy_rates(list(host.values()), dev)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(s_in)
     run(args.steps)
@@ -471,6 +545,7 @@ def run_e2e(args, w, x, dev, gdn, world):
     ms = e0.elapsed_time(e1) / args.steps
     return {"value": round(world * w.tokens / (ms / 1e3), 1), "unit": "tokens/s", "ms_per_step": round(ms, 4),
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "copy_gbs": {"h2d": h2d_gbs, "d2h": d2h_gbs, "host_buffers_near_gpu": old_affinity is not None},
             "pipelined": "each step's host-to-device inputs and device-to-host outputs are copied on their own "
                          "streams, overlapping the neighbouring steps' compute (two device input buffers)"}
 
@@ -633,6 +708,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-autocp", action="store_true", help="skip the split-mode forward timings")
+    ap.add_argument("--no-head64", action="store_true", help="skip the 64-wide-head timings")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--sweep", action="store_true",
                     help="the pages' head-count / batch-length / token-count sweep (one JSON line per shape)")

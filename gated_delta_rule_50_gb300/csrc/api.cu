@@ -165,6 +165,58 @@ template <typename T> T *at(void *ws, size_t off) {
     return reinterpret_cast<T *>(static_cast<unsigned char *>(ws) + off);
 }
 
+// bf16 problems with a 64-wide head run the 128-wide tensor-core kernels on zero-padded copies (pad.cu)
+bool pad_to_tc(const Plan &p) { return p.io == GDN_BF16 && (p.K != 128 || p.V != 128); }
+Plan padded_plan(const Plan &p) {
+    Plan q = p;
+    q.K = 128;
+    q.V = 128;
+    return q;
+}
+// Workspace of the padded forward: the 128-wide path's own workspace first (its error record stays at
+// offset 0), then the padded inputs and the 128-wide outputs that are sliced back.
+struct PadFwdWs {
+    size_t inner, q, k, v, o, h0, ht, h, total;
+};
+PadFwdWs pad_fwd_layout(const Plan &p) {
+    const Plan pp = padded_plan(p);
+    const size_t tokens = (size_t)p.B * p.T, state = 128 * 128, nst = (size_t)p.n_seqs * p.Hv;
+    Carve c;
+    PadFwdWs w;
+    w.inner = c.take<unsigned char>(fwd_layout(pp).total);
+    w.q = c.take<uint16_t>(p.K < 128 ? tokens * p.Hq * 128 : 0);
+    w.k = c.take<uint16_t>(p.K < 128 ? tokens * p.Hq * 128 : 0);
+    w.v = c.take<uint16_t>(p.V < 128 ? tokens * p.Hv * 128 : 0);
+    w.o = c.take<uint16_t>(p.V < 128 ? tokens * p.Hv * 128 : 0);
+    w.h0 = c.take<float>(nst * state);
+    w.ht = c.take<float>(nst * state);
+    w.h = c.take<float>((size_t)p.total_chunks * p.Hv * state);
+    w.total = c.off;
+    return w;
+}
+struct PadBwdWs {
+    size_t inner, q, k, v, d_o, h0, dht, dq, dk, dv, dh0, total;
+};
+PadBwdWs pad_bwd_layout(const Plan &p) {
+    const Plan pp = padded_plan(p);
+    const size_t tokens = (size_t)p.B * p.T, state = 128 * 128, nst = (size_t)p.n_seqs * p.Hv;
+    Carve c;
+    PadBwdWs w;
+    w.inner = c.take<unsigned char>(bwd_layout(pp).total);
+    w.q = c.take<uint16_t>(p.K < 128 ? tokens * p.Hq * 128 : 0);
+    w.k = c.take<uint16_t>(p.K < 128 ? tokens * p.Hq * 128 : 0);
+    w.dq = c.take<uint16_t>(p.K < 128 ? tokens * p.Hq * 128 : 0);
+    w.dk = c.take<uint16_t>(p.K < 128 ? tokens * p.Hq * 128 : 0);
+    w.v = c.take<uint16_t>(p.V < 128 ? tokens * p.Hv * 128 : 0);
+    w.d_o = c.take<uint16_t>(p.V < 128 ? tokens * p.Hv * 128 : 0);
+    w.dv = c.take<uint16_t>(p.V < 128 ? tokens * p.Hv * 128 : 0);
+    w.h0 = c.take<float>(nst * state);
+    w.dht = c.take<float>(nst * state);
+    w.dh0 = c.take<float>(nst * state);
+    w.total = c.off;
+    return w;
+}
+
 #define GDN_TRY(expr)                                  \
     do {                                               \
         cudaError_t e_ = (expr);                       \
@@ -210,30 +262,24 @@ extern "C" {
 size_t gdn_fwd_workspace_bytes(const gdn_problem *p) {
     Plan pl;
     if (make_plan(p, &pl) != GDN_OK) return 0;
-    return fwd_layout(pl).total;
+    return pad_to_tc(pl) ? pad_fwd_layout(pl).total : fwd_layout(pl).total;
 }
 
 size_t gdn_bwd_workspace_bytes(const gdn_problem *p) {
     Plan pl;
     if (make_plan(p, &pl) != GDN_OK) return 0;
-    return bwd_layout(pl).total;
+    return pad_to_tc(pl) ? pad_bwd_layout(pl).total : bwd_layout(pl).total;
 }
 
-gdn_status gdn_fwd(const gdn_problem *p, const void *q, const void *k, const void *v, const float *g,
-                   const float *beta, const float *h0, void *o, float *g_cum, void *A, float *h,
-                   float *final_state, void *workspace, size_t workspace_bytes, gdn_stream_t stream) {
-    Plan pl;
-    gdn_status s = make_plan(p, &pl);
-    if (s != GDN_OK) return s;
-    const bool any_tok = (size_t)pl.B * pl.T > 0;
-    if (any_tok && !(ok_ptr(q) && ok_ptr(k) && ok_ptr(v) && ok_ptr(g) && ok_ptr(beta) && ok_ptr(o)))
-        return GDN_ERR_INVALID_ARG;
-    if (!(ok_opt(h0) && ok_opt(g_cum) && ok_opt(A) && ok_opt(h) && ok_opt(final_state)))
-        return GDN_ERR_INVALID_ARG;
+}  // extern "C"
+
+namespace {
+
+// The forward's launch sequence for a validated plan (arguments checked by gdn_fwd).
+gdn_status fwd_impl(Plan pl, const void *q, const void *k, const void *v, const float *g, const float *beta,
+                    const float *h0, void *o, float *g_cum, void *A, float *h, float *final_state, void *workspace,
+                    cudaStream_t st) {
     FwdWs w = fwd_layout(pl);
-    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < w.total)
-        return GDN_ERR_WORKSPACE;
-    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     pl.err = at<uint32_t>(workspace, w.err);
     pl.chunk_off = pl.cu ? at<int32_t>(workspace, w.chunk_off) : nullptr;
     GDN_TRY(cudaMemsetAsync(pl.err, 0, 256, st));
@@ -281,6 +327,62 @@ gdn_status gdn_fwd(const gdn_problem *p, const void *q, const void *k, const voi
     return GDN_OK;
 }
 
+// The backward's launch sequence for a validated plan (arguments checked by gdn_bwd).
+gdn_status bwd_impl(Plan pl, const void *q, const void *k, const void *v, const float *g_cum, const float *beta,
+                    const void *d_o, const float *dht, const float *h0, void *dq, void *dk, void *dv, float *dbeta,
+                    float *dg, float *dh0, void *workspace, cudaStream_t st);
+
+}  // namespace
+
+extern "C" {
+
+gdn_status gdn_fwd(const gdn_problem *p, const void *q, const void *k, const void *v, const float *g,
+                   const float *beta, const float *h0, void *o, float *g_cum, void *A, float *h,
+                   float *final_state, void *workspace, size_t workspace_bytes, gdn_stream_t stream) {
+    Plan pl;
+    gdn_status s = make_plan(p, &pl);
+    if (s != GDN_OK) return s;
+    const bool any_tok = (size_t)pl.B * pl.T > 0;
+    if (any_tok && !(ok_ptr(q) && ok_ptr(k) && ok_ptr(v) && ok_ptr(g) && ok_ptr(beta) && ok_ptr(o)))
+        return GDN_ERR_INVALID_ARG;
+    if (!(ok_opt(h0) && ok_opt(g_cum) && ok_opt(A) && ok_opt(h) && ok_opt(final_state)))
+        return GDN_ERR_INVALID_ARG;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (!pad_to_tc(pl)) {
+        if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < fwd_layout(pl).total)
+            return GDN_ERR_WORKSPACE;
+        return fwd_impl(pl, q, k, v, g, beta, h0, o, g_cum, A, h, final_state, workspace, st);
+    }
+    // a 64-wide head: pad to the 128-wide tiles, run, slice the outputs back
+    const PadFwdWs w = pad_fwd_layout(pl);
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < w.total)
+        return GDN_ERR_WORKSPACE;
+    const size_t tokens = (size_t)pl.B * pl.T, nst = (size_t)pl.n_seqs * pl.Hv;
+    const void *qp = q, *kp = k, *vp = v;
+    void *op = o;
+    if (pl.K < 128) {
+        qp = at<void>(workspace, w.q);
+        kp = at<void>(workspace, w.k);
+        GDN_LAUNCH("pad", launch_pad_rows(q, const_cast<void *>(qp), tokens * pl.Hq, pl.K, st));
+        GDN_LAUNCH("pad", launch_pad_rows(k, const_cast<void *>(kp), tokens * pl.Hq, pl.K, st));
+    }
+    if (pl.V < 128) {
+        vp = at<void>(workspace, w.v);
+        op = at<void>(workspace, w.o);
+        GDN_LAUNCH("pad", launch_pad_rows(v, const_cast<void *>(vp), tokens * pl.Hv, pl.V, st));
+    }
+    float *h0p = h0 ? at<float>(workspace, w.h0) : nullptr;
+    if (h0) GDN_LAUNCH("pad", launch_pad_states(h0, h0p, nst, pl.K, pl.V, st));
+    float *htp = final_state ? at<float>(workspace, w.ht) : nullptr;
+    float *hp = h ? at<float>(workspace, w.h) : nullptr;
+    s = fwd_impl(padded_plan(pl), qp, kp, vp, g, beta, h0p, op, g_cum, A, hp, htp, at<void>(workspace, w.inner), st);
+    if (s != GDN_OK) return s;
+    if (pl.V < 128) GDN_LAUNCH("slice", launch_slice_rows(op, o, tokens * pl.Hv, pl.V, st));
+    if (final_state) GDN_LAUNCH("slice", launch_slice_states(htp, final_state, nst, pl.K, pl.V, st));
+    if (h) GDN_LAUNCH("slice", launch_slice_states(hp, h, (size_t)pl.total_chunks * pl.Hv, pl.K, pl.V, st));
+    return GDN_OK;
+}
+
 gdn_status gdn_bwd(const gdn_problem *p, const void *q, const void *k, const void *v, const float *g_cum,
                    const float *beta, const void *A, const void *d_o, const float *dht, const float *h0,
                    void *dq, void *dk, void *dv, float *dbeta, float *dg, float *dh0, void *workspace,
@@ -295,10 +397,59 @@ gdn_status gdn_bwd(const gdn_problem *p, const void *q, const void *k, const voi
         return GDN_ERR_INVALID_ARG;
     if (!(ok_opt(A) && ok_opt(dht) && ok_opt(h0) && ok_opt(dh0))) return GDN_ERR_INVALID_ARG;
     if ((h0 == nullptr) != (dh0 == nullptr)) return GDN_ERR_INVALID_ARG;
-    BwdWs w = bwd_layout(pl);
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (!pad_to_tc(pl)) {
+        if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < bwd_layout(pl).total)
+            return GDN_ERR_WORKSPACE;
+        return bwd_impl(pl, q, k, v, g_cum, beta, d_o, dht, h0, dq, dk, dv, dbeta, dg, dh0, workspace, st);
+    }
+    // a 64-wide head: pad to the 128-wide tiles, run, slice the gradients back
+    const PadBwdWs w = pad_bwd_layout(pl);
     if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < w.total)
         return GDN_ERR_WORKSPACE;
-    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const size_t tokens = (size_t)pl.B * pl.T, nst = (size_t)pl.n_seqs * pl.Hv;
+    const void *qp = q, *kp = k, *vp = v, *dop = d_o;
+    void *dqp = dq, *dkp = dk, *dvp = dv;
+    if (pl.K < 128) {
+        qp = at<void>(workspace, w.q);
+        kp = at<void>(workspace, w.k);
+        dqp = at<void>(workspace, w.dq);
+        dkp = at<void>(workspace, w.dk);
+        GDN_LAUNCH("pad", launch_pad_rows(q, const_cast<void *>(qp), tokens * pl.Hq, pl.K, st));
+        GDN_LAUNCH("pad", launch_pad_rows(k, const_cast<void *>(kp), tokens * pl.Hq, pl.K, st));
+    }
+    if (pl.V < 128) {
+        vp = at<void>(workspace, w.v);
+        dop = at<void>(workspace, w.d_o);
+        dvp = at<void>(workspace, w.dv);
+        GDN_LAUNCH("pad", launch_pad_rows(v, const_cast<void *>(vp), tokens * pl.Hv, pl.V, st));
+        GDN_LAUNCH("pad", launch_pad_rows(d_o, const_cast<void *>(dop), tokens * pl.Hv, pl.V, st));
+    }
+    float *h0p = h0 ? at<float>(workspace, w.h0) : nullptr;
+    float *dhtp = dht ? at<float>(workspace, w.dht) : nullptr;
+    float *dh0p = dh0 ? at<float>(workspace, w.dh0) : nullptr;
+    if (h0) GDN_LAUNCH("pad", launch_pad_states(h0, h0p, nst, pl.K, pl.V, st));
+    if (dht) GDN_LAUNCH("pad", launch_pad_states(dht, dhtp, nst, pl.K, pl.V, st));
+    s = bwd_impl(padded_plan(pl), qp, kp, vp, g_cum, beta, dop, dhtp, h0p, dqp, dkp, dvp, dbeta, dg, dh0p,
+                 at<void>(workspace, w.inner), st);
+    if (s != GDN_OK) return s;
+    if (pl.K < 128) {
+        GDN_LAUNCH("slice", launch_slice_rows(dqp, dq, tokens * pl.Hq, pl.K, st));
+        GDN_LAUNCH("slice", launch_slice_rows(dkp, dk, tokens * pl.Hq, pl.K, st));
+    }
+    if (pl.V < 128) GDN_LAUNCH("slice", launch_slice_rows(dvp, dv, tokens * pl.Hv, pl.V, st));
+    if (dh0) GDN_LAUNCH("slice", launch_slice_states(dh0p, dh0, nst, pl.K, pl.V, st));
+    return GDN_OK;
+}
+
+}  // extern "C"
+
+namespace {
+
+gdn_status bwd_impl(Plan pl, const void *q, const void *k, const void *v, const float *g_cum, const float *beta,
+                    const void *d_o, const float *dht, const float *h0, void *dq, void *dk, void *dv, float *dbeta,
+                    float *dg, float *dh0, void *workspace, cudaStream_t st) {
+    BwdWs w = bwd_layout(pl);
     pl.err = at<uint32_t>(workspace, w.err);
     pl.chunk_off = pl.cu ? at<int32_t>(workspace, w.chunk_off) : nullptr;
     GDN_TRY(cudaMemsetAsync(pl.err, 0, 256, st));
@@ -360,10 +511,14 @@ gdn_status gdn_bwd(const gdn_problem *p, const void *q, const void *k, const voi
     return GDN_OK;
 }
 
+}  // namespace
+
+extern "C" {
+
 size_t gdn_bwd_saved_workspace_bytes(const gdn_problem *p) {
     Plan pl;
     if (make_plan(p, &pl) != GDN_OK) return 0;
-    return tc_fwd_supported(pl) ? bwd_saved_layout(pl).total : bwd_layout(pl).total;
+    return tc_fwd_supported(pl) ? bwd_saved_layout(pl).total : gdn_bwd_workspace_bytes(p);
 }
 
 gdn_status gdn_bwd_saved(const gdn_problem *p, const void *q, const void *k, const void *v, const float *g_cum,
@@ -423,6 +578,7 @@ gdn_status gdn_bwd_saved(const gdn_problem *p, const void *q, const void *k, con
 int gdn_cp_plan(const gdn_problem *p, int *seg_len, int *n_seg) {
     Plan pl;
     if (make_plan(p, &pl) != GDN_OK) return -1;
+    if (pad_to_tc(pl)) pl = padded_plan(pl);
     int L = 0, n = 1;
     const int on = (warmup_split(pl) || exact_split(pl)) ? 1 : 0;
     if (on) cp_geometry(pl, &L, &n);

@@ -56,6 +56,13 @@ cudaError_t launch_tc_fwd(const Plan &p, const void *q, const void *k, const voi
                           const float *vecs, const float *h0, void *o, float *h, float *ht, cudaStream_t st,
                           const CpSplit *cp = nullptr);
 
+// Zero padding of 64-wide heads to the 128-wide tensor-core tiles (pad.cu): rows [rows][d] bf16 <->
+// [rows][128]; states [n][K][V] fp32 <-> [n][128][128].  Pointers 16-byte aligned.
+cudaError_t launch_pad_rows(const void *src, void *dst, size_t rows, int d, cudaStream_t st);
+cudaError_t launch_slice_rows(const void *src, void *dst, size_t rows, int d, cudaStream_t st);
+cudaError_t launch_pad_states(const float *src, float *dst, size_t n, int K, int V, cudaStream_t st);
+cudaError_t launch_slice_states(const float *src, float *dst, size_t n, int K, int V, cudaStream_t st);
+
 // TMA map of a [tokens][heads][128] bf16 tensor (64 x 1 x 64 boxes, 128-byte swizzle)
 bool make_head_map(CUtensorMap *m, const void *ptr, int heads, const Plan &p);
 // TMA map of per-chunk fp32 states [units][128 keys][128 values] as a 2-D tensor of units x 128 rows:

@@ -51,6 +51,26 @@ def beta0_case():
 
 
 CASES["bf16_beta0_g0"] = beta0_case
+CASES["bf16_dk128_v64"] = lambda: small("train_b2_t8192_h64", B=2, T=150, Hq=1, Hv=2, K=128, V=64, seed=22)
+
+
+def varlen_d64_case():
+    x = small("varlen_8seq_32k", T=341, Hq=2, Hv=2, K=64, V=64, seed=23, n_varlen=6, varlen_min=1, varlen_max=200)
+    lens = [1, 64, 65, 0, 130, 81]
+    x["cu_seqlens"] = torch.tensor([0] + list(torch.tensor(lens).cumsum(0).tolist()), dtype=torch.int32)
+    return x
+
+
+CASES["bf16_d64_varlen_edge"] = varlen_d64_case
+
+
+def split_d64_case():  # 64-wide heads through the exact sequence split; one value head does not decay
+    x = small("longseq_b1_t32k_h8", T=4096 + 100, Hq=2, Hv=4, K=64, V=64, seed=24)
+    x["g"][..., 1] = 0.0
+    return x
+
+
+CASES["bf16_d64_split"] = split_d64_case
 
 
 @pytest.mark.parametrize("name", list(CASES))

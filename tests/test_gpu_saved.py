@@ -32,6 +32,7 @@ def split_case():  # the trigger splits both chains; one value head does not dec
 
 CASES = {
     "bf16_ragged": lambda: small("train_b2_t8192_h64", B=2, T=300, Hq=2, Hv=4, seed=11),
+    "bf16_d64": lambda: small("train_b2_t8192_h64", B=2, T=200, Hq=2, Hv=4, K=64, V=64, seed=25),
     "bf16_varlen_edge": varlen_edge,
     "bf16_split": split_case,
 }
