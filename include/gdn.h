@@ -43,6 +43,11 @@
  *  - Varlen: cu_seqlens != NULL requires B == 1; sequence s covers tokens
  *    [cu_seqlens[s], cu_seqlens[s+1]) and has its own h0 / ht; chunks never
  *    cross a sequence boundary.
+ *  - Execution paths: bf16 io with K = V = 128 runs the tensor-core kernels.
+ *    bf16 io with K or V = 64 runs the same kernels on zero-padded 128-wide
+ *    copies that the library makes in its workspace (exact: the padded state
+ *    rows and columns stay zero) and slices the outputs back.  fp32 io runs
+ *    the CUDA-core kernels.
  */
 #ifndef GDN_H_
 #define GDN_H_
@@ -182,8 +187,8 @@ gdn_status gdn_fwd_noalloc(const gdn_problem *p,
  * rounding, provided the forward's states were exact (cp_mode AUTO or OFF; a
  * warm-up split forward saves its approximate states, and the gradients then
  * follow those).  Arguments otherwise as gdn_bwd; the workspace must hold
- * gdn_bwd_saved_workspace_bytes(p) bytes.  Problems outside the tensor-core
- * path (fp32 io, other head sizes) run gdn_bwd (h and fwd_workspace unused;
+ * gdn_bwd_saved_workspace_bytes(p) bytes.  Problems other than bf16 with
+ * K = V = 128 (fp32 io, 64-wide heads) run gdn_bwd (h and fwd_workspace unused;
  * the workspace must then hold gdn_bwd_workspace_bytes(p), which this query
  * returns for them).
  */
