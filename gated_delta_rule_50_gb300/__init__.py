@@ -79,6 +79,8 @@ def load_library():
             lib.gdn_bwd.restype = ctypes.c_int
             lib.gdn_bwd_saved_workspace_bytes.argtypes = [pp]
             lib.gdn_bwd_saved_workspace_bytes.restype = SZ
+            lib.gdn_bwd_saved_uses_saved.argtypes = [pp]
+            lib.gdn_bwd_saved_uses_saved.restype = ctypes.c_int
             lib.gdn_bwd_saved.argtypes = [pp] + [P] * 10 + [P, SZ] + [P] * 6 + [P, SZ, P]
             lib.gdn_bwd_saved.restype = ctypes.c_int
             lib.gdn_workspace_error.argtypes = [P, P]
@@ -248,9 +250,10 @@ def chunk_gated_delta_rule_bwd(q, k, v, g, beta, A, do, dht=None, scale=None, in
 
 class SavedForward:
     """What a forward leaves for its backward: the workspace (operand images and gate vectors of every
-    chunk) and the chunk-entry states h.  Valid while the forward's inputs are unchanged."""
+    chunk) and the chunk-entry states h (None where the saved backward recomputes, see
+    gdn_bwd_saved_uses_saved).  Valid while the forward's inputs are unchanged."""
 
-    def __init__(self, workspace: torch.Tensor, h: torch.Tensor):
+    def __init__(self, workspace: torch.Tensor, h: Optional[torch.Tensor]):
         self.workspace = workspace
         self.h = h
 
@@ -266,9 +269,11 @@ def chunk_gated_delta_rule_fwd_saved(q, k, v, g, beta, scale=None, initial_state
     pr = _problem(_cuda(q, "q", q.dtype), v, scale, cu, host, cp_mode, 8)
     need = int(lib.gdn_fwd_workspace_bytes(ctypes.byref(pr)))
     ws = workspace if workspace is not None and workspace.numel() >= need else _workspace(need, q.device)
+    # the chunk-entry states are kept only where the saved backward reads them
+    keep = int(lib.gdn_bwd_saved_uses_saved(ctypes.byref(pr))) == 1
     g_cum, A, o, h, ht = chunk_gated_delta_rule_fwd(
         q, k, v, g, beta, scale=scale, initial_state=initial_state, cu_seqlens=cu_seqlens,
-        output_final_state=output_final_state, output_h=True, cp_mode=cp_mode, cu_seqlens_cpu=host,
+        output_final_state=output_final_state, output_h=keep, cp_mode=cp_mode, cu_seqlens_cpu=host,
         workspace=ws)
     return g_cum, A, o, ht, SavedForward(ws, h)
 

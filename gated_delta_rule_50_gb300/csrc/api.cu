@@ -521,6 +521,12 @@ size_t gdn_bwd_saved_workspace_bytes(const gdn_problem *p) {
     return tc_fwd_supported(pl) ? bwd_saved_layout(pl).total : gdn_bwd_workspace_bytes(p);
 }
 
+int gdn_bwd_saved_uses_saved(const gdn_problem *p) {
+    Plan pl;
+    if (make_plan(p, &pl) != GDN_OK) return -1;
+    return tc_fwd_supported(pl) && pl.total_chunks > 0 ? 1 : 0;
+}
+
 gdn_status gdn_bwd_saved(const gdn_problem *p, const void *q, const void *k, const void *v, const float *g_cum,
                          const float *beta, const void *A, const void *d_o, const float *dht, const float *h0,
                          const float *h, const void *fwd_workspace, size_t fwd_workspace_bytes, void *dq, void *dk,

@@ -193,6 +193,10 @@ gdn_status gdn_fwd_noalloc(const gdn_problem *p,
  * returns for them).
  */
 size_t gdn_bwd_saved_workspace_bytes(const gdn_problem *p);
+/* 1 if gdn_bwd_saved reads the forward's h and workspace for this problem
+ * (bf16, K = V = 128), 0 if it runs gdn_bwd instead (the forward then need not
+ * produce h), -1 for an invalid problem. */
+int gdn_bwd_saved_uses_saved(const gdn_problem *p);
 gdn_status gdn_bwd_saved(const gdn_problem *p,
                          const void *q, const void *k, const void *v,
                          const float *g_cum, const float *beta, const void *A,
