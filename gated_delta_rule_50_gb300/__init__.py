@@ -14,6 +14,12 @@ API (flash_qla 0.1.2 README, "Usage / High-level API" and "Low-level API"):
         scale=None, initial_state=None, cu_seqlens=None)
     dq, dk, dv, db, dg, dh0 = chunk_gated_delta_rule_bwd(q, k, v, g_cum, beta,
         A, do, dht=None, scale=None, initial_state=None, cu_seqlens=None)
+
+plus the save-for-backward pair that training through ``chunk_gated_delta_rule`` uses (the forward
+keeps its operand images and chunk-entry states; the backward skips its recompute passes):
+
+    g_cum, A, o, final_state, saved = chunk_gated_delta_rule_fwd_saved(q, k, v, g, beta, ...)
+    dq, dk, dv, db, dg, dh0 = chunk_gated_delta_rule_bwd_saved(q, k, v, g_cum, beta, A, do, saved, ...)
 """
 from __future__ import annotations
 
@@ -34,7 +40,8 @@ CHUNK = 64
 GDN_F32, GDN_BF16 = 0, 1
 CP_MODES = {"auto": 0, "off": 1, "warmup": 2}
 _STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported problem",
-           3: "workspace too small or misaligned", 4: "CUDA error", 5: "device-side wait timed out"}
+           3: "workspace too small or misaligned", 4: "CUDA error", 5: "device-side wait timed out",
+           6: "problem exceeds the fixed no-alloc scratch"}
 
 
 class GdnError(RuntimeError):
