@@ -187,6 +187,21 @@ def kernel_profile(lib):
     return out
 
 
+def max_over_ranks(values, world, device):
+    """Each timing's maximum over the ranks (the slowest replica sets the job's time); the values
+    themselves at world size 1."""
+    if world == 1:
+        return list(values)
+    t = torch.tensor(list(values), dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return t.tolist()
+
+
+def job_rate(units_per_rank, world, ms):
+    """Whole-job throughput: the units all ranks processed per second of the max-over-ranks time."""
+    return world * units_per_rank / (ms / 1e3)
+
+
 def run_ours(args, rank, world, local_rank):
     import ctypes
     import gated_delta_rule_50_gb300 as gdn
@@ -271,10 +286,7 @@ def run_ours(args, rank, world, local_rank):
         torch.cuda.synchronize()
         rec_ms += e0.elapsed_time(e1) / args.steps
     step_ms = fwd_ms + bwd_ms
-    if world > 1:
-        t = torch.tensor([step_ms, fwd_ms, bwd_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        step_ms, fwd_ms, bwd_ms = t.tolist()
+    step_ms, fwd_ms, bwd_ms = max_over_ranks([step_ms, fwd_ms, bwd_ms], world, dev)
 
     peaks, peak_src = load_peaks()
     alg = algorithmic(w)
@@ -313,7 +325,7 @@ def run_ours(args, rank, world, local_rank):
     t_roof_b = max(alg["bwd_flops"] / tc, alg["bwd_bytes"] / bw)
     res = {
         "metric": METRIC,
-        "value": round(world * tokens / (step_ms / 1e3), 1),
+        "value": round(job_rate(tokens, world, step_ms), 1),
         "unit": "tokens/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(step_ms, 4),
@@ -535,6 +547,8 @@ def run_e2e(args, w, x, dev, gdn, world):
     if old_affinity is not None:
         os.sched_setaffinity(0, old_affinity)
     h2d_gbs, d2h_gbs = copy_rates(list(host.values()), dev)
+    if world > 1:
+        torch.distributed.barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(s_in)
     run(args.steps)
@@ -542,8 +556,8 @@ def run_e2e(args, w, x, dev, gdn, world):
     comp.wait_stream(s_in)
     e1.record(comp)
     torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1) / args.steps
-    return {"value": round(world * w.tokens / (ms / 1e3), 1), "unit": "tokens/s", "ms_per_step": round(ms, 4),
+    ms = max_over_ranks([e0.elapsed_time(e1) / args.steps], world, dev)[0]
+    return {"value": round(job_rate(w.tokens, world, ms), 1), "unit": "tokens/s", "ms_per_step": round(ms, 4),
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
             "copy_gbs": {"h2d": h2d_gbs, "d2h": d2h_gbs, "host_buffers_near_gpu": old_affinity is not None},
             "pipelined": "each step's host-to-device inputs and device-to-host outputs are copied on their own "
