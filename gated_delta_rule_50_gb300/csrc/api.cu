@@ -255,6 +255,35 @@ BwdSavedWs bwd_saved_layout(const Plan &p) {
     return w;
 }
 
+struct PadBwdSavedWs {
+    size_t inner, q, k, v, d_o, dht, dq, dk, dv, dh0, total;
+};
+PadBwdSavedWs pad_bwd_saved_layout(const Plan &p) {
+    const Plan pp = padded_plan(p);
+    const size_t tokens = (size_t)p.B * p.T, state = 128 * 128, nst = (size_t)p.n_seqs * p.Hv;
+    Carve c;
+    PadBwdSavedWs w;
+    w.inner = c.take<unsigned char>(bwd_saved_layout(pp).total);
+    w.q = c.take<uint16_t>(p.K < 128 ? tokens * p.Hq * 128 : 0);
+    w.k = c.take<uint16_t>(p.K < 128 ? tokens * p.Hq * 128 : 0);
+    w.dq = c.take<uint16_t>(p.K < 128 ? tokens * p.Hq * 128 : 0);
+    w.dk = c.take<uint16_t>(p.K < 128 ? tokens * p.Hq * 128 : 0);
+    w.v = c.take<uint16_t>(p.V < 128 ? tokens * p.Hv * 128 : 0);
+    w.d_o = c.take<uint16_t>(p.V < 128 ? tokens * p.Hv * 128 : 0);
+    w.dv = c.take<uint16_t>(p.V < 128 ? tokens * p.Hv * 128 : 0);
+    w.dht = c.take<float>(nst * state);
+    w.dh0 = c.take<float>(nst * state);
+    w.total = c.off;
+    return w;
+}
+
+// The saved backward's launch sequence (dS scan, per-chunk gradients) for a validated tensor-core plan,
+// reading the forward's operand images, gate vectors and chunk-entry states.
+gdn_status bwd_saved_impl(Plan pl, const void *q, const void *k, const void *v, const float *g_cum,
+                          const float *beta, const void *d_o, const float *dht, const unsigned char *tiles,
+                          const float *vecs, const float *h, void *dq, void *dk, void *dv, float *dbeta, float *dg,
+                          float *dh0, void *workspace, cudaStream_t st);
+
 }  // namespace
 
 extern "C" {
@@ -518,13 +547,15 @@ extern "C" {
 size_t gdn_bwd_saved_workspace_bytes(const gdn_problem *p) {
     Plan pl;
     if (make_plan(p, &pl) != GDN_OK) return 0;
-    return tc_fwd_supported(pl) ? bwd_saved_layout(pl).total : gdn_bwd_workspace_bytes(p);
+    if (tc_fwd_supported(pl)) return bwd_saved_layout(pl).total;
+    if (pad_to_tc(pl) && pl.total_chunks > 0) return pad_bwd_saved_layout(pl).total;
+    return gdn_bwd_workspace_bytes(p);
 }
 
 int gdn_bwd_saved_uses_saved(const gdn_problem *p) {
     Plan pl;
     if (make_plan(p, &pl) != GDN_OK) return -1;
-    return tc_fwd_supported(pl) && pl.total_chunks > 0 ? 1 : 0;
+    return (tc_fwd_supported(pl) || pad_to_tc(pl)) && pl.total_chunks > 0 ? 1 : 0;
 }
 
 gdn_status gdn_bwd_saved(const gdn_problem *p, const void *q, const void *k, const void *v, const float *g_cum,
@@ -535,7 +566,8 @@ gdn_status gdn_bwd_saved(const gdn_problem *p, const void *q, const void *k, con
     Plan pl;
     gdn_status s = make_plan(p, &pl);
     if (s != GDN_OK) return s;
-    if (!tc_fwd_supported(pl) || pl.total_chunks == 0)  // nothing saved to reuse: the recomputing backward
+    const bool pad = pad_to_tc(pl);
+    if ((!tc_fwd_supported(pl) && !pad) || pl.total_chunks == 0)  // nothing saved to reuse: recompute
         return gdn_bwd(p, q, k, v, g_cum, beta, A, d_o, dht, h0, dq, dk, dv, dbeta, dg, dh0, workspace,
                        workspace_bytes, stream);
     if (!(ok_ptr(q) && ok_ptr(k) && ok_ptr(v) && ok_ptr(g_cum) && ok_ptr(beta) && ok_ptr(d_o) && ok_ptr(dq) &&
@@ -543,20 +575,75 @@ gdn_status gdn_bwd_saved(const gdn_problem *p, const void *q, const void *k, con
         return GDN_ERR_INVALID_ARG;
     if (!(ok_opt(A) && ok_opt(dht) && ok_opt(h0) && ok_opt(dh0))) return GDN_ERR_INVALID_ARG;
     if ((h0 == nullptr) != (dh0 == nullptr)) return GDN_ERR_INVALID_ARG;
-    const FwdWs fw = fwd_layout(pl);
-    if (!fwd_workspace || (reinterpret_cast<uintptr_t>(fwd_workspace) & 255u) || fwd_workspace_bytes < fw.total)
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    void *fws = const_cast<void *>(fwd_workspace);
+    const size_t fwd_need = pad ? pad_fwd_layout(pl).total : fwd_layout(pl).total;
+    if (!fws || (reinterpret_cast<uintptr_t>(fws) & 255u) || fwd_workspace_bytes < fwd_need)
         return GDN_ERR_WORKSPACE;
-    const BwdSavedWs w = bwd_saved_layout(pl);
+    if (!pad) {
+        if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) ||
+            workspace_bytes < bwd_saved_layout(pl).total)
+            return GDN_ERR_WORKSPACE;
+        const FwdWs fw = fwd_layout(pl);
+        return bwd_saved_impl(pl, q, k, v, g_cum, beta, d_o, dht, at<unsigned char>(fws, fw.tiles),
+                              at<float>(fws, fw.vecs), h, dq, dk, dv, dbeta, dg, dh0, workspace, st);
+    }
+    // a 64-wide head: the padded forward left its images, vectors and 128-wide chunk-entry states in its
+    // workspace; pad the inputs, run, slice the gradients back
+    const Plan pp = padded_plan(pl);
+    const PadFwdWs pf = pad_fwd_layout(pl);
+    const FwdWs fw = fwd_layout(pp);
+    void *finner = at<void>(fws, pf.inner);
+    const PadBwdSavedWs w = pad_bwd_saved_layout(pl);
     if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < w.total)
         return GDN_ERR_WORKSPACE;
-    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const size_t tokens = (size_t)pl.B * pl.T, nst = (size_t)pl.n_seqs * pl.Hv;
+    const void *qp = q, *kp = k, *vp = v, *dop = d_o;
+    void *dqp = dq, *dkp = dk, *dvp = dv;
+    if (pl.K < 128) {
+        qp = at<void>(workspace, w.q);
+        kp = at<void>(workspace, w.k);
+        dqp = at<void>(workspace, w.dq);
+        dkp = at<void>(workspace, w.dk);
+        GDN_LAUNCH("pad", launch_pad_rows(q, const_cast<void *>(qp), tokens * pl.Hq, pl.K, st));
+        GDN_LAUNCH("pad", launch_pad_rows(k, const_cast<void *>(kp), tokens * pl.Hq, pl.K, st));
+    }
+    if (pl.V < 128) {
+        vp = at<void>(workspace, w.v);
+        dop = at<void>(workspace, w.d_o);
+        dvp = at<void>(workspace, w.dv);
+        GDN_LAUNCH("pad", launch_pad_rows(v, const_cast<void *>(vp), tokens * pl.Hv, pl.V, st));
+        GDN_LAUNCH("pad", launch_pad_rows(d_o, const_cast<void *>(dop), tokens * pl.Hv, pl.V, st));
+    }
+    float *dhtp = dht ? at<float>(workspace, w.dht) : nullptr;
+    float *dh0p = dh0 ? at<float>(workspace, w.dh0) : nullptr;
+    if (dht) GDN_LAUNCH("pad", launch_pad_states(dht, dhtp, nst, pl.K, pl.V, st));
+    s = bwd_saved_impl(pp, qp, kp, vp, g_cum, beta, dop, dhtp, at<unsigned char>(finner, fw.tiles),
+                       at<float>(finner, fw.vecs), at<float>(fws, pf.h), dqp, dkp, dvp, dbeta, dg, dh0p,
+                       at<void>(workspace, w.inner), st);
+    if (s != GDN_OK) return s;
+    if (pl.K < 128) {
+        GDN_LAUNCH("slice", launch_slice_rows(dqp, dq, tokens * pl.Hq, pl.K, st));
+        GDN_LAUNCH("slice", launch_slice_rows(dkp, dk, tokens * pl.Hq, pl.K, st));
+    }
+    if (pl.V < 128) GDN_LAUNCH("slice", launch_slice_rows(dvp, dv, tokens * pl.Hv, pl.V, st));
+    if (dh0) GDN_LAUNCH("slice", launch_slice_states(dh0p, dh0, nst, pl.K, pl.V, st));
+    return GDN_OK;
+}
+
+}  // extern "C"
+
+namespace {
+
+gdn_status bwd_saved_impl(Plan pl, const void *q, const void *k, const void *v, const float *g_cum,
+                          const float *beta, const void *d_o, const float *dht, const unsigned char *tiles,
+                          const float *vecs, const float *h, void *dq, void *dk, void *dv, float *dbeta, float *dg,
+                          float *dh0, void *workspace, cudaStream_t st) {
+    const BwdSavedWs w = bwd_saved_layout(pl);
     pl.err = at<uint32_t>(workspace, w.err);
     pl.chunk_off = pl.cu ? at<int32_t>(workspace, w.chunk_off) : nullptr;
     GDN_TRY(cudaMemsetAsync(pl.err, 0, 256, st));
     GDN_LAUNCH("chunk_table", launch_chunk_table(pl, st));
-    void *fws = const_cast<void *>(fwd_workspace);
-    const unsigned char *tiles = at<unsigned char>(fws, fw.tiles);
-    const float *vecs = at<float>(fws, fw.vecs);
     float *dSe = at<float>(workspace, w.dSe);
     if (w.n_seg > 1) {  // exact split of the dS scan (segments counted from the sequence end)
         CpSplit cs;
@@ -580,6 +667,10 @@ gdn_status gdn_bwd_saved(const gdn_problem *p, const void *q, const void *k, con
     GDN_LAUNCH("bwd_intra_tc", launch_tc_bwd_intra(pl, q, k, v, d_o, tiles, vecs, h, dSe, dq, dk, dv, dbeta, dg, st));
     return GDN_OK;
 }
+
+}  // namespace
+
+extern "C" {
 
 int gdn_cp_plan(const gdn_problem *p, int *seg_len, int *n_seg) {
     Plan pl;

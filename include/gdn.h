@@ -187,15 +187,17 @@ gdn_status gdn_fwd_noalloc(const gdn_problem *p,
  * rounding, provided the forward's states were exact (cp_mode AUTO or OFF; a
  * warm-up split forward saves its approximate states, and the gradients then
  * follow those).  Arguments otherwise as gdn_bwd; the workspace must hold
- * gdn_bwd_saved_workspace_bytes(p) bytes.  Problems other than bf16 with
- * K = V = 128 (fp32 io, 64-wide heads) run gdn_bwd (h and fwd_workspace unused;
+ * gdn_bwd_saved_workspace_bytes(p) bytes.  For 64-wide heads the padded
+ * forward's workspace holds the 128-wide states this reads (h must still be
+ * passed: it marks that the forward ran with h requested).  fp32 problems
+ * run gdn_bwd (h and fwd_workspace unused;
  * the workspace must then hold gdn_bwd_workspace_bytes(p), which this query
  * returns for them).
  */
 size_t gdn_bwd_saved_workspace_bytes(const gdn_problem *p);
 /* 1 if gdn_bwd_saved reads the forward's h and workspace for this problem
- * (bf16, K = V = 128), 0 if it runs gdn_bwd instead (the forward then need not
- * produce h), -1 for an invalid problem. */
+ * (bf16 io with at least one chunk), 0 if it runs gdn_bwd instead (the forward
+ * then need not produce h), -1 for an invalid problem. */
 int gdn_bwd_saved_uses_saved(const gdn_problem *p);
 gdn_status gdn_bwd_saved(const gdn_problem *p,
                          const void *q, const void *k, const void *v,

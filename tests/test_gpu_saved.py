@@ -30,11 +30,19 @@ def split_case():  # the trigger splits both chains; one value head does not dec
     return x
 
 
+def split_d64_case():  # 64-wide heads, both chains split exactly; one value head does not decay
+    x = small("longseq_b1_t32k_h8", T=4096 + 100, Hq=2, Hv=4, K=64, V=64, seed=27)
+    x["g"][..., 1] = 0.0
+    return x
+
+
 CASES = {
     "bf16_ragged": lambda: small("train_b2_t8192_h64", B=2, T=300, Hq=2, Hv=4, seed=11),
     "bf16_d64": lambda: small("train_b2_t8192_h64", B=2, T=200, Hq=2, Hv=4, K=64, V=64, seed=25),
+    "bf16_k128_v64": lambda: small("train_b2_t8192_h64", B=1, T=190, Hq=1, Hv=2, K=128, V=64, seed=26),
     "bf16_varlen_edge": varlen_edge,
     "bf16_split": split_case,
+    "bf16_d64_split": split_d64_case,
 }
 
 
