@@ -60,6 +60,15 @@ def test_warmup_longseq_shape_small():
     check("final_state", ht, ht_ref, torch.bfloat16, torch.float32)
 
 
+def test_warmup_head64_padded():
+    """64-wide heads (zero-padded to the 128-wide kernels) through the warmup split."""
+    x = make_inputs(workload("longseq_b1_t32k_h8").scaled(T=4096 + 100, Hq=2, Hv=4, K=64, V=64, seed=43))
+    plan, o, ht, o_ref, ht_ref, _ = run(x, warm=6)
+    assert plan == (8, 9)
+    check("o", o, o_ref, torch.bfloat16, torch.bfloat16)
+    check("final_state", ht, ht_ref, torch.bfloat16, torch.float32)
+
+
 def test_warmup_varlen():
     x = make_inputs(workload("varlen_8seq_32k").scaled(T=2500, Hq=1, Hv=2, seed=42, n_varlen=3))
     x["cu_seqlens"] = torch.tensor([0, 700, 2200, 2500], dtype=torch.int32)
