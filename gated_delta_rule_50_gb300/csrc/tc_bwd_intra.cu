@@ -688,9 +688,13 @@ k_tc_bwd_intra(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
             tmem_wait_st();
         }
         __syncthreads();
-        // per-row results of this head (warp 0; lane holds rows lane and lane + 32): dbeta, and dg as
+        // ---------------------------------------------------------------- P6: dq^T, dk^T accumulation
+        pre_mma();
+        if (t == 0) issue_dq_dk(sb, tmem, g != 0);
+        // per-row results of this head (warp 1, while thread 0 issues the
+        // dq / dk products below; lane holds rows lane and lane + 32): dbeta, and dg as
         // the reverse cumsum of dgam inside the chunk
-        if (warp == 0) {
+        if (warp == 1) {
             float hd = 0.f, sf = 0.f;
 #pragma unroll
             for (int w = 0; w < NW; ++w) {
@@ -730,9 +734,6 @@ k_tc_bwd_intra(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
                 }
             }
         }
-        // ---------------------------------------------------------------- P6: dq^T, dk^T accumulation
-        pre_mma();
-        if (t == 0) issue_dq_dk(sb, tmem, g != 0);
         mma_sync();
     }
     // ---------------------------------------------------------------- dq, dk out (thread: key lrow, rows 16 hh + j)
