@@ -471,29 +471,6 @@ k_tc_bwd_intra(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
             for (int j = 0; j < 16; ++j) dst[(16 * hh + j) * 65 + i] = __uint_as_float(dd[j]);
         }
         __syncthreads();
-        {  // dv out: 64 rows x 256 bytes from the staging tile, 16-byte stores
-            const uint4 *src = reinterpret_cast<const uint4 *>(sm + S_DD);
-            for (int o = t; o < 64 * 16; o += NT) {
-                const int r = o >> 4, c16 = o & 15;
-                if (r < n)
-                    *reinterpret_cast<uint4 *>(a.dv + (size_t)(tok0 + r) * p.Hv * DV + (size_t)hv * DV + 8 * c16) =
-                        src[o];
-            }
-        }
-        __syncthreads();
-        {  // (E Dl)^T -> value-major hi / lo tile [v][i] in the dDl region (the dv staging has been written out)
-            uint32_t dl[16];
-            tmem_ld16(tmem + trow + C_DL + 16 * hh, dl);
-            tmem_wait_ld();
-#pragma unroll
-            for (int q2 = 0; q2 < 2; ++q2) {
-                float e8[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) e8[e] = Ev[16 * hh + 8 * q2 + e] * __uint_as_float(dl[8 * q2 + e]);
-                st_split_chunk(sb + S_DD, sb + S_DD + 16384, lrow, 2 * hh + q2, e8);
-            }
-        }
-        __syncthreads();
         // Thread (row r, 8 columns i = 8 c ..): dQK = D o scale dP -> hi / lo tile [r][i] in the dO region;
         // dgam terms of dP o P (row and column sums); dA~ = lower part of dA -> hi / lo tile [k][l] in the P
         // region (each thread overwrites exactly the P chunk it has read).
@@ -553,6 +530,29 @@ k_tc_bwd_intra(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
             mma_chain<4, 2, 2>(tmem + C_KS, kdesc(sb + S_A), kdesc(sb + S_P), ID_KK, 0);
             mma_chain<4, 2, 2>(tmem + C_KS, kdesc(sb + S_A), kdesc(sb + S_P + 8192), ID_KK, 1);
             mma_chain<4, 2, 2>(tmem + C_KS, kdesc(sb + S_A + 8192), kdesc(sb + S_P), ID_KK, 1);
+        }
+        // while Z runs: dv out, then (E Dl)^T into the staging region
+        {  // dv out: 64 rows x 256 bytes from the staging tile, 16-byte stores
+            const uint4 *src = reinterpret_cast<const uint4 *>(sm + S_DD);
+            for (int o = t; o < 64 * 16; o += NT) {
+                const int r = o >> 4, c16 = o & 15;
+                if (r < n)
+                    *reinterpret_cast<uint4 *>(a.dv + (size_t)(tok0 + r) * p.Hv * DV + (size_t)hv * DV + 8 * c16) =
+                        src[o];
+            }
+        }
+        __syncthreads();
+        {  // (E Dl)^T -> value-major hi / lo tile [v][i] in the dDl region (the dv staging has been written out)
+            uint32_t dl[16];
+            tmem_ld16(tmem + trow + C_DL + 16 * hh, dl);
+            tmem_wait_ld();
+#pragma unroll
+            for (int q2 = 0; q2 < 2; ++q2) {
+                float e8[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) e8[e] = Ev[16 * hh + 8 * q2 + e] * __uint_as_float(dl[8 * q2 + e]);
+                st_split_chunk(sb + S_DD, sb + S_DD + 16384, lrow, 2 * hh + q2, e8);
+            }
         }
         mma_sync();
         if (!ok) break;
