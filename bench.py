@@ -500,6 +500,11 @@ def run_e2e(args, w, x, dev, gdn, world):
     outs_host = [None, None]
     ev_read = [None, None]                             # read-back into host set b done
     d2h = 0
+    # workspaces allocated once, as a training loop keeps them (steps run in order on one stream)
+    ws_f = torch.empty(gdn.workspace_bytes("fwd", bufs[0]["q"], bufs[0]["v"], None, cu_cpu), dtype=torch.uint8,
+                       device=dev)
+    ws_b = torch.empty(gdn.workspace_bytes("bwd_saved", bufs[0]["q"], bufs[0]["v"], None, cu_cpu),
+                       dtype=torch.uint8, device=dev)
 
     def copy_in(k):
         b = k & 1
@@ -516,10 +521,11 @@ def run_e2e(args, w, x, dev, gdn, world):
         comp.wait_event(ev_in[b])
         g_cum, A, o, ht, saved = gdn.chunk_gated_delta_rule_fwd_saved(
             d["q"], d["k"], d["v"], d["g"], d["beta"], scale=x["scale"], initial_state=d.get("h0"),
-            output_final_state=True, cu_seqlens_cpu=cu_cpu)
+            output_final_state=True, cu_seqlens_cpu=cu_cpu, workspace=ws_f)
         grads = gdn.chunk_gated_delta_rule_bwd_saved(d["q"], d["k"], d["v"], g_cum, d["beta"], A, d["do"], saved,
                                                      dht=d.get("dht"), scale=x["scale"],
-                                                     initial_state=d.get("h0"), cu_seqlens_cpu=cu_cpu)
+                                                     initial_state=d.get("h0"), cu_seqlens_cpu=cu_cpu,
+                                                     workspace=ws_b)
         ev_free[b].record(comp)
         outs = [o, ht] + [t for t in grads if t is not None]
         d2h = sum(t.numel() * t.element_size() for t in outs)
@@ -542,7 +548,7 @@ def run_e2e(args, w, x, dev, gdn, world):
                 ev_read[k & 1].synchronize()  # host set k & 1 is free again
             compute(k)
 
-    run(max(3, args.warmup))
+    run(max(6, args.warmup))  # long enough for the allocator to settle on two steps in flight
     torch.cuda.synchronize()
     if old_affinity is not None:
         os.sched_setaffinity(0, old_affinity)
