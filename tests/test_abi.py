@@ -133,3 +133,34 @@ def test_cp_plan_geometry(lib):
     assert lib.gdn_cp_plan(ctypes.byref(p), ctypes.byref(L), ctypes.byref(n)) == 0
     p = _prob(B=2, T=8192, Hq=16, Hv=64, n_seqs=2, cp_mode=2)
     assert lib.gdn_cp_plan(ctypes.byref(p), ctypes.byref(L), ctypes.byref(n)) == 0
+
+
+def test_head64_padded_planning(lib):
+    """64-wide bf16 heads plan onto the 128-wide tensor-core path: the same sequence split as a 128-wide
+    problem, a workspace that holds the padded copies on top of the 128-wide one, and a saved backward
+    that reads the forward's states; fp32 problems recompute instead."""
+    lib.gdn_cp_plan.argtypes = [ctypes.POINTER(gdn._Problem), ctypes.POINTER(ctypes.c_int),
+                                ctypes.POINTER(ctypes.c_int)]
+    lib.gdn_cp_plan.restype = ctypes.c_int
+    lib.gdn_bwd_saved_uses_saved.argtypes = [ctypes.POINTER(gdn._Problem)]
+    lib.gdn_bwd_saved_uses_saved.restype = ctypes.c_int
+    L, n = ctypes.c_int(), ctypes.c_int()
+    p64 = _prob(B=1, T=32768, Hq=4, Hv=8, n_seqs=1, K=64, V=64)
+    p128 = _prob(B=1, T=32768, Hq=4, Hv=8, n_seqs=1)
+    assert lib.gdn_cp_plan(ctypes.byref(p64), ctypes.byref(L), ctypes.byref(n)) == 1
+    assert (L.value, n.value) == (23, 23)
+    tokens, state = 32768, 128 * 128 * 4
+    for fn in (lib.gdn_fwd_workspace_bytes, lib.gdn_bwd_workspace_bytes, lib.gdn_bwd_saved_workspace_bytes):
+        w64, w128 = fn(ctypes.byref(p64)), fn(ctypes.byref(p128))
+        assert w64 > w128 + tokens * 4 * 128 * 2  # at least the padded q (or the padded dq)
+    # forward: padded q, k, v, o, h0, ht and per-chunk states beside the 128-wide workspace
+    extra = lib.gdn_fwd_workspace_bytes(ctypes.byref(p64)) - lib.gdn_fwd_workspace_bytes(ctypes.byref(p128))
+    assert extra >= tokens * (2 * 4 + 2 * 8) * 128 * 2 + (2 * 8 + 512 * 8) * state
+    assert lib.gdn_bwd_saved_uses_saved(ctypes.byref(p64)) == 1
+    assert lib.gdn_bwd_saved_uses_saved(ctypes.byref(p128)) == 1
+    assert lib.gdn_bwd_saved_uses_saved(ctypes.byref(_prob(io_dtype=0, K=64, V=64))) == 0
+    assert lib.gdn_bwd_saved_uses_saved(ctypes.byref(_prob(T=0))) == 0
+    assert lib.gdn_bwd_saved_uses_saved(ctypes.byref(_prob(Hv=3))) == -1
+    # fp32 with 64-wide heads stays on the CUDA-core path: no padded copies in its workspace
+    f64 = _prob(B=1, T=32768, Hq=4, Hv=8, n_seqs=1, K=64, V=64, io_dtype=0)
+    assert lib.gdn_fwd_workspace_bytes(ctypes.byref(f64)) < lib.gdn_fwd_workspace_bytes(ctypes.byref(p64))
