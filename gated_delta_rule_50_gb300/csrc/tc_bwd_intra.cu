@@ -261,15 +261,7 @@ k_tc_bwd_intra(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         tma_load_3d(sb + S_KQ + 8192, &tm_q, bar_tma, 0, hq, tok0);
         tma_load_3d(sb + S_KQ + 16384, &tm_k, bar_tma, 64, hq, tok0);
         tma_load_3d(sb + S_KQ + 24576, &tm_q, bar_tma, 64, hq, tok0);
-        // the first head's h and dSe boxes 0, 1 (own barriers) load alongside the k / q tiles
-        const size_t unit0 = (size_t)gc * p.Hv + hq * p.G;
-        mbar_arrive_expect_tx(bar_h, 65536);
-        for (int b = 0; b < 4; ++b) tma_load_2d(sb + S_DR + 16384 * b, &tm_h, bar_h, 32 * b, (int)(unit0 * DK));
-        mbar_arrive_expect_tx(bar_d, 32768);
-        for (int b = 0; b < 2; ++b) tma_load_2d(sb + S_F + 16384 * b, &tm_dse, bar_d, 32 * b, (int)(unit0 * DK));
     }
-    ++h_issued;
-    ++d_arrived;
     tma_wait();
 
 
@@ -280,14 +272,11 @@ k_tc_bwd_intra(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         ++tma_issued;
         if (t == 0) {  // dO, V tiles; A / P operand images (S_A, S_P are adjacent); gate vectors
             const size_t unit = (size_t)gc * p.Hv + hv;
-            if (g > 0) {  // h -> S_DR (4 boxes) first: it is needed first; dSe boxes 0, 1 -> the fp32 scratch
-                mbar_arrive_expect_tx(bar_h, 65536);
-                for (int b = 0; b < 4; ++b)
-                    tma_load_2d(sb + S_DR + 16384 * b, &tm_h, bar_h, 32 * b, (int)(unit * DK));
-                mbar_arrive_expect_tx(bar_d, 32768);
-                for (int b = 0; b < 2; ++b)
-                    tma_load_2d(sb + S_F + 16384 * b, &tm_dse, bar_d, 32 * b, (int)(unit * DK));
-            }
+            // h -> S_DR (4 boxes) first: it is needed first; dSe boxes 0, 1 -> the fp32 scratch
+            mbar_arrive_expect_tx(bar_h, 65536);
+            for (int b = 0; b < 4; ++b) tma_load_2d(sb + S_DR + 16384 * b, &tm_h, bar_h, 32 * b, (int)(unit * DK));
+            mbar_arrive_expect_tx(bar_d, 32768);
+            for (int b = 0; b < 2; ++b) tma_load_2d(sb + S_F + 16384 * b, &tm_dse, bar_d, 32 * b, (int)(unit * DK));
             mbar_arrive_expect_tx(bar_tma, 32768 + 32768 + 1024);
             bulk_load(sb + S_VEC, a.vecs + unit * 256, 1024, bar_tma);
             tma_load_3d(sb + S_DO, &tm_do, bar_tma, 0, hv, tok0);
@@ -296,10 +285,8 @@ k_tc_bwd_intra(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
             tma_load_3d(sb + S_DD + 8192, &tm_v, bar_tma, 64, hv, tok0);
             bulk_load(sb + S_A, a.tiles + unit * 32768, 32768, bar_tma);
         }
-        if (g > 0) {
-            ++h_issued;
-            ++d_arrived;
-        }
+        ++h_issued;
+        ++d_arrived;
         for (int o = t; o < 2 * NW * 64 + 2 * NW; o += NT) rdb_all[o] = 0.f;  // rdb, rdg, sH, sF
         // ---------------------------------------------------------------- P1: h^T (lane v) -> TMEM; KS, QS
         {  // h^T from its boxes: value v = lrow in box lq, keys 32 hh + i
