@@ -10,7 +10,7 @@
 //   Dl^T = R^T A^T,  KdS^T = dSe^T K^T,  PdO^T = dO^T P   dDl = scale P^T dO + diag(E) K dSe
 //   dR^T = dDl^T A                                        dV = diag(beta) dR
 //   [Dl; R] dO^T -> dP^T (rows 0..63),  [Dl; R] dDl^T -> dA^T (rows 64..127)
-//   dL = -(A^T dA A^T) strictly lower                     (CUDA cores)
+//   dL = -(A^T dA A^T) strictly lower                     (Z^T = A dA~^T, then dL^T = -Z^T A)
 //   dq^T += h (scale Gam o dO)^T + K^T dQK^T               dQK = D o scale dP
 //   dk^T += dSe (E o Dl)^T - h (beta Gam o dR)^T + Q^T dQK + K^T (dKK + dKK^T),  dKK = beta D o dL
 //   (the two h products run as one N = 128 product over the adjacent dq^T, dk^T accumulators)
@@ -23,9 +23,14 @@
 //
 // The kernel is phase-sequential: 512 threads (each TMEM lane quarter is
 // served by four warps, one per 16 chunk rows), one of them issues the MMAs of
-// a phase and all wait on one mbarrier before the next phase.  The k, q, dO and
-// v chunk tiles arrive by TMA; dv leaves through a shared-memory staging tile
-// in 16-byte stores.  Many CTAs (one per chunk and q/k head) keep the GPU busy.
+// a phase and all wait on one mbarrier before the next phase; work that needs
+// no result of the running MMAs (dv store-out, the (E Dl)^T tile, the dbeta / dg
+// reduction) runs meanwhile.  The k, q, dO and v chunk tiles arrive by TMA, the
+// A / P operand images and gate vectors by bulk copy, h and dSe by TMA as
+// 128-byte-swizzled fp32 boxes (value-major reads for the TMEM A operands) and
+// again by coalesced row loads transposed in shared memory (key-major, for the
+// dq / dk products); dv leaves through a shared-memory staging tile in 16-byte
+// stores.  Many CTAs (one per chunk and q/k head) keep the GPU busy.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
