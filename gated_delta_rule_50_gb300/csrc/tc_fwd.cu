@@ -5,8 +5,8 @@
 //
 // All contractions run on tcgen05 (kind::f16, fp32 accumulation in TMEM) in the
 // value-major form: every MMA has M = 128 = the value dimension, so TMEM lane v
-// holds value column v and the thread owning lane v keeps the state row
-// S^T[v][:] in registers.  Per chunk (n <= 64 rows, entry state S), with A, P
+// holds value column v and the four threads owning lane v (one per quarter of
+// the keys) keep the state row S^T[v][:] in registers, 32 keys each.  Per chunk (n <= 64 rows, entry state S), with A, P
 // and the gate vectors of the chunk precomputed by the prep kernel (tc_prep.cu):
 //
 //   KS^T = S^T K^T,  QS^T = S^T Q^T                               (S split hi + lo, from TMEM)
@@ -24,7 +24,7 @@
 // FlashQLA blog post, section 2) forms the corrected values U - W S; here the
 // same Dl is formed as A R, which needs neither W nor U.
 //
-// Warp roles (320 threads):
+// Warp roles (576 threads):
 //   warp 0      producer: k, q (TMA) and the A / P operand image (bulk copy), 2 stages;
 //               v (TMA) and the gate vectors (bulk copy), 2 stages
 //   warp 1      TMEM allocator and single-thread MMA issuer
