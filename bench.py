@@ -2,9 +2,14 @@
 """Benchmark of the gated delta rule chunked prefill, forward + backward, on GB300.
 
 One step = one forward pass (gdn_fwd: gate cumsum, A, state scan, o, final
-state) plus one backward pass (gdn_bwd) over the training-shaped workload
-B=2, T=8192, Hq=16, Hv=64, K=V=128, bf16 io with fp32 gates and states, all
-inputs resident in HBM.  Prints ONE JSON line (rank 0).
+state, keeping the chunk-entry states) plus one backward pass (gdn_bwd_saved:
+dS scan and per-chunk gradients from what the forward kept) over the
+training-shaped workload B=2, T=8192, Hq=16, Hv=64, K=V=128, bf16 io with fp32
+gates and states, all inputs resident in HBM.  Prints ONE JSON line (rank 0)
+with the step's tokens/s and beside it: the recomputing backward (gdn_bwd),
+the dominant kernel's roofline, the end-to-end step from pinned host memory,
+the split modes of the small-head long-sequence workload, 64-wide heads and
+the CPU oracle baseline.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
