@@ -41,6 +41,15 @@ L2_FLUSH_BYTES = 512 << 20
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
+def workload_config(w, world):
+    """The ``config`` object of both arms' JSON lines (the same workload string in each)."""
+    return {"workload": f"{w.name}: B={w.B} T={w.T} Hq={w.Hq} Hv={w.Hv} K={w.K} V={w.V} chunk=64, "
+                        "fwd+bwd per step",
+            "global_batch": w.B * world, "seq_len": w.T,
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+            "l2": "512 MB buffer written between timed steps (outside the per-step events)"}
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -322,7 +331,7 @@ def run_ours(args, rank, world, local_rank):
             roof["avg_launch_us"] = round(avg_s * 1e6, 2)
             roof["algorithmic_flops"] = fl
             roof["algorithmic_bytes"] = by
-            roof["traffic"] = TRAFFIC.get(name)
+            roof["traffic"] = traffic_bytes(name)
     # whole-pass roofline (both passes, measured peaks)
     bw = peaks["hbm_gbs"] * 1e9
     tc = peaks["bf16_tflops"] * 1e12
@@ -338,10 +347,7 @@ def run_ours(args, rank, world, local_rank):
         "dtype": "bf16" if w.io_dtype == torch.bfloat16 else "f32",
         "data": "synthetic (seeded; q,k unit-norm N(0,1), v N(0,1), g=-softplus(N(0,1)) with 10% "
                 "of heads g=0, beta=sigmoid(N(0,1)), h0/dht 0.1 N(0,1))",
-        "config": {"workload": f"{w.name}: B={w.B} T={w.T} Hq={w.Hq} Hv={w.Hv} K={w.K} V={w.V} chunk=64, "
-                               "fwd+bwd per step", "global_batch": w.B * world, "seq_len": w.T,
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "l2": "512 MB buffer written between timed steps (outside the per-step events)"},
+        "config": workload_config(w, world),
         "fwd": {"ms": round(fwd_ms, 4), "tokens_per_s": round(world * tokens / (fwd_ms / 1e3), 1),
                 "roofline_frac": round(t_roof_f / (fwd_ms / 1e3), 4)},
         "bwd": {"ms": round(bwd_ms, 4), "tokens_per_s": round(world * tokens / (bwd_ms / 1e3), 1),
@@ -357,6 +363,14 @@ def run_ours(args, rank, world, local_rank):
         "wall_s_timed_region": round(wall, 4),
         "peaks": {"source": peak_src, "hbm_gbs": peaks["hbm_gbs"], "bf16_tflops": peaks["bf16_tflops"]},
     }
+    # the pages' forward (no chunk-entry states kept) on this workload and on the prefill workload
+    res["fwd_only"] = run_fwd_only(dev, gdn, w, d, cu_cpu, flush, peaks)
+    if not args.no_prefill:
+        pw = workload("prefill_b4_t4096")
+        px = make_inputs(pw)
+        pd = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in px.items()}
+        res["prefill_b4_t4096"] = run_fwd_only(dev, gdn, pw, pd, None, flush, peaks)
+        del pd, px
     if not args.no_e2e:
         res["e2e"] = run_e2e(args, w, x, dev, gdn, world)
     if not args.no_autocp and rank == 0:
@@ -366,6 +380,38 @@ def run_ours(args, rank, world, local_rank):
     if rank == 0 and not args.no_cpu_baseline and world == 1:
         res["cpu_baseline"] = cpu_baseline(w, x, budget_s=args.cpu_budget)
     return res
+
+
+def run_fwd_only(dev, gdn, w, d, cu_cpu, flush, peaks, steps=20, warmup=5):
+    """The forward as the pages' interface runs it (o and the final state; no chunk-entry states kept),
+    inputs resident in HBM, L2 flushed before every timed call, per-call CUDA events."""
+    ws = torch.empty(gdn.workspace_bytes("fwd", d["q"], d["v"], d["cu_seqlens"], cu_cpu), dtype=torch.uint8,
+                     device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def f():
+        return gdn.chunk_gated_delta_rule_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], scale=d["scale"],
+                                              initial_state=d["h0"], cu_seqlens=d["cu_seqlens"],
+                                              cu_seqlens_cpu=cu_cpu, output_final_state=True, workspace=ws)
+    for _ in range(warmup):
+        f()
+    torch.cuda.synchronize(dev)
+    tot = 0.0
+    for i in range(steps):
+        flush.fill_(i & 0xFF)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        f()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        tot += e0.elapsed_time(e1)
+    ms = tot / steps
+    alg = algorithmic(w)
+    t_roof = max(alg["fwd_flops"] / (peaks["bf16_tflops"] * 1e12), alg["fwd_bytes"] / (peaks["hbm_gbs"] * 1e9))
+    return {"workload": f"{w.name}: B={w.B} T={w.T} Hq={w.Hq} Hv={w.Hv} K={w.K} V={w.V}, forward "
+                        f"({'with' if w.has_h0 else 'no'} initial state, final state out, no h)",
+            "ms": round(ms, 4), "tokens_per_s": round(w.tokens / (ms / 1e3), 1),
+            "roofline_frac": round(t_roof / (ms / 1e3), 4), "roofline_us": round(t_roof * 1e6, 1)}
 
 
 def run_autocp(dev, gdn, steps=10, warmup=3):
@@ -630,17 +676,15 @@ def run_reference(args, rank, world):
     lib = oracle.load()
     cores = oracle.max_threads(lib)
     s, nh = oracle_sample(w, x, 1)
-    for _ in range(args.warmup):
-        time_oracle_step(w, s) if False else None
+    for _ in range(args.warmup):   # untimed warm-up steps on the same sample
+        time_oracle_step(w, s)
     times = [time_oracle_step(w, s) for _ in range(args.steps)]
     dt = sum(times) / len(times)
     value = w.tokens * (nh / w.Hv) / dt
     return {"impl": "reference", "metric": METRIC, "value": round(value, 1), "unit": "tokens/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 2),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": {"workload": f"{w.name}: B={w.B} T={w.T} Hq={w.Hq} Hv={w.Hv} "
-                                                        f"K={w.K} V={w.V}, fwd+bwd per step",
-                                            "global_batch": w.B, "seq_len": w.T},
+            "data": "synthetic", "config": workload_config(w, world),
             "cpu_baseline": {"value": round(value, 1), "unit": "tokens/s", "cores": cores, "kind": "oracle",
                              "sample": f"fwd+bwd of 1 of {w.Hq} q/k head groups ({nh} value heads), "
                                        "all tokens, per step; scaled by the head fraction"},
@@ -648,13 +692,29 @@ def run_reference(args, rank, world):
                     "d2h_bytes_per_step": 0}}
 
 
-# kernel -> DRAM bytes (read + write) per launch at the benchmark workload, from the committed ncu
-# capture (profiles/ncu_kernels_train_b1_t4096_h64.md): measured on the half-size training shape and
-# scaled by the 4x units of the full one (per-unit reads and writes do not depend on the unit count).
-# An entry is removed whenever its kernel changes.
-TRAFFIC = {
-    "bwd_intra_tc": 4 * (844.359424e6 + 99.836928e6),
-}
+# kernel -> (DRAM bytes read + written per launch at the benchmark workload, from one ncu capture of
+# that kernel; sha256 prefix of the kernel's source file when the counters were taken).  A capture on
+# the half-size training shape is scaled by the 4x units of the full one (per-unit reads and writes do
+# not depend on the unit count).  The figure is reported only while the source is unchanged.
+TRAFFIC = {}
+KERNEL_SOURCES = {"fwd_prep_tc": "tc_prep.cu", "bwd_prep_tc": "tc_prep.cu", "fwd_tc": "tc_fwd.cu",
+                  "bwd_state_tc": "tc_fwd.cu", "bwd_dscan_tc": "tc_bwd.cu", "bwd_intra_tc": "tc_bwd_intra.cu"}
+
+
+def source_sha16(kernel):
+    import hashlib
+    f = KERNEL_SOURCES.get(kernel)
+    if f is None:
+        return None
+    with open(os.path.join(ROOT, "gated_delta_rule_50_gb300", "csrc", f), "rb") as fh:
+        return hashlib.sha256(fh.read()).hexdigest()[:16]
+
+
+def traffic_bytes(kernel):
+    entry = TRAFFIC.get(kernel)
+    if entry is None or entry[1] != source_sha16(kernel):
+        return None
+    return entry[0]
 
 
 def time_cuda(fn, dev, steps, warmup):
@@ -734,6 +794,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-autocp", action="store_true", help="skip the split-mode forward timings")
     ap.add_argument("--no-head64", action="store_true", help="skip the 64-wide-head timings")
+    ap.add_argument("--no-prefill", action="store_true", help="skip the prefill workload's forward")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--sweep", action="store_true",
                     help="the pages' head-count / batch-length / token-count sweep (one JSON line per shape)")
@@ -744,6 +805,11 @@ def main():
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", 1))
     local_rank = int(os.environ.get("LOCAL_RANK", 0))
+    if args.gpus != world:
+        # N ranks come from the launcher (torchrun sets WORLD_SIZE); a bare --gpus N would time one rank
+        print(json.dumps({"error": f"--gpus {args.gpus} but WORLD_SIZE={world}: launch N > 1 ranks with "
+                                   f"torch.distributed.run --nproc-per-node {args.gpus}"}), flush=True)
+        sys.exit(2)
     if world > 1 and args.impl == "ours":
         torch.distributed.init_process_group(backend="nccl" if torch.cuda.is_available() else "gloo",
                                              device_id=torch.device("cuda", local_rank)

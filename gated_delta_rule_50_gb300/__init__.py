@@ -56,7 +56,7 @@ class _Problem(ctypes.Structure):
                 ("n_seqs", ctypes.c_int64), ("cu_seqlens", ctypes.c_void_p),
                 ("cu_seqlens_host", ctypes.c_void_p), ("io_dtype", ctypes.c_int),
                 ("scale", ctypes.c_float), ("cp_mode", ctypes.c_int32),
-                ("warmup_chunks", ctypes.c_int32)]
+                ("warmup_chunks", ctypes.c_int32), ("out_f32", ctypes.c_int32)]
 
 
 _lib = None
@@ -90,11 +90,17 @@ def load_library():
             lib.gdn_bwd_saved_uses_saved.restype = ctypes.c_int
             lib.gdn_bwd_saved.argtypes = [pp] + [P] * 10 + [P, SZ] + [P] * 6 + [P, SZ, P]
             lib.gdn_bwd_saved.restype = ctypes.c_int
+            lib.gdn_fwd_noalloc.argtypes = [pp] + [P] * 11 + [P]
+            lib.gdn_fwd_noalloc.restype = ctypes.c_int
+            lib.gdn_fwd_noalloc_error.argtypes = [P]
+            lib.gdn_fwd_noalloc_error.restype = ctypes.c_int
             lib.gdn_workspace_error.argtypes = [P, P]
             lib.gdn_workspace_error.restype = ctypes.c_int
             lib.gdn_status_str.argtypes = [ctypes.c_int]
             lib.gdn_status_str.restype = ctypes.c_char_p
             lib.gdn_version.restype = ctypes.c_char_p
+            lib.gdn_debug_set_wait.argtypes = [ctypes.c_int64, ctypes.c_int32]
+            lib.gdn_debug_set_wait.restype = None
             lib.gdn_cp_trigger.argtypes = [ctypes.c_int64] * 3
             lib.gdn_cp_trigger.restype = ctypes.c_int
             IP = ctypes.POINTER(ctypes.c_int)
@@ -126,7 +132,7 @@ def _cuda(t: Optional[torch.Tensor], name: str, dtype=None) -> Optional[torch.Te
     return t.contiguous()
 
 
-def _problem(q, v, scale, cu_seqlens, cu_host, cp_mode, warmup_chunks):
+def _problem(q, v, scale, cu_seqlens, cu_host, cp_mode, warmup_chunks, out_f32=False):
     B, T, Hq, K = q.shape
     Hv, V = v.shape[2], v.shape[3]
     pr = _Problem()
@@ -141,6 +147,7 @@ def _problem(q, v, scale, cu_seqlens, cu_host, cp_mode, warmup_chunks):
     pr.scale = float(K ** -0.5 if scale is None else scale)
     pr.cp_mode = CP_MODES[cp_mode] if isinstance(cp_mode, str) else int(cp_mode)
     pr.warmup_chunks = int(warmup_chunks)
+    pr.out_f32 = 1 if out_f32 else 0
     return pr
 
 
@@ -187,24 +194,27 @@ def _workspace(nbytes: int, device) -> torch.Tensor:
 def chunk_gated_delta_rule_fwd(q, k, v, g, beta, scale=None, initial_state=None, cu_seqlens=None,
                                output_final_state=True, output_h=False, output_A=True,
                                cp_mode="auto", warmup_chunks=8, cu_seqlens_cpu=None,
-                               workspace: Optional[torch.Tensor] = None):
-    """Returns (g_cum, A, o, h, final_state); h / A / final_state may be None."""
+                               workspace: Optional[torch.Tensor] = None, out_f32=False):
+    """Returns (g_cum, A, o, h, final_state); h / A / final_state may be None.  ``out_f32`` (bf16
+    inputs): o and A come back as fp32, the kernels' values before their final rounding (a checking
+    mode; see gdn.h)."""
     lib = load_library()
     io = q.dtype
     q, k, v = _cuda(q, "q", io), _cuda(k, "k", io), _cuda(v, "v", io)
     g, beta = _cuda(g, "g", torch.float32), _cuda(beta, "beta", torch.float32)
     h0 = _cuda(initial_state, "initial_state", torch.float32)
     cu, host = _cu(cu_seqlens, cu_seqlens_cpu)
-    pr = _problem(q, v, scale, cu, host, cp_mode, warmup_chunks)
+    pr = _problem(q, v, scale, cu, host, cp_mode, warmup_chunks, out_f32)
     B, T, Hq, K = q.shape
     Hv, V = v.shape[2], v.shape[3]
     dev = q.device
+    odt = torch.float32 if out_f32 else io
     nseq = int(pr.n_seqs)
     nchunks = (sum((int(host[i + 1]) - int(host[i]) + CHUNK - 1) // CHUNK for i in range(nseq))
                if cu is not None else B * ((T + CHUNK - 1) // CHUNK))
-    o = torch.empty(B, T, Hv, V, dtype=io, device=dev)
+    o = torch.empty(B, T, Hv, V, dtype=odt, device=dev)
     g_cum = torch.empty(B, T, Hv, dtype=torch.float32, device=dev)
-    A = torch.empty(B, T, Hv, CHUNK, dtype=io, device=dev) if output_A else None
+    A = torch.empty(B, T, Hv, CHUNK, dtype=odt, device=dev) if output_A else None
     h = (torch.empty(nchunks, Hv, K, V, dtype=torch.float32, device=dev) if output_h else None)
     ht = torch.empty(nseq, Hv, K, V, dtype=torch.float32, device=dev) if output_final_state else None
     need = int(lib.gdn_fwd_workspace_bytes(ctypes.byref(pr)))
@@ -223,11 +233,12 @@ def chunk_gated_delta_rule_fwd(q, k, v, g, beta, scale=None, initial_state=None,
 
 def chunk_gated_delta_rule_bwd(q, k, v, g, beta, A, do, dht=None, scale=None, initial_state=None,
                                cu_seqlens=None, cu_seqlens_cpu=None,
-                               workspace: Optional[torch.Tensor] = None, cp_mode="auto"):
+                               workspace: Optional[torch.Tensor] = None, cp_mode="auto", out_f32=False):
     """``g`` is the forward's returned chunk-local cumsum.  Returns
     (dq, dk, dv, db, dg, dh0); dg is the gradient of the raw gate.  ``cp_mode``
     "auto" splits long sequences of small batch x heads exactly; any other mode
-    runs the backward unsplit."""
+    runs the backward unsplit.  ``out_f32`` (bf16 inputs): dq, dk, dv come back as fp32 (checking
+    mode)."""
     lib = load_library()
     io = q.dtype
     q, k, v = _cuda(q, "q", io), _cuda(k, "k", io), _cuda(v, "v", io)
@@ -237,8 +248,10 @@ def chunk_gated_delta_rule_bwd(q, k, v, g, beta, A, do, dht=None, scale=None, in
     h0 = _cuda(initial_state, "initial_state", torch.float32)
     dht = _cuda(dht, "dht", torch.float32)
     cu, host = _cu(cu_seqlens, cu_seqlens_cpu)
-    pr = _problem(q, v, scale, cu, host, cp_mode, 8)
-    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    pr = _problem(q, v, scale, cu, host, cp_mode, 8, out_f32)
+    odt = torch.float32 if out_f32 else io
+    dq, dk, dv = (torch.empty(q.shape, dtype=odt, device=q.device), torch.empty(k.shape, dtype=odt, device=q.device),
+                  torch.empty(v.shape, dtype=odt, device=q.device))
     db = torch.empty_like(beta)
     dg = torch.empty_like(g)
     dh0 = torch.empty_like(h0) if h0 is not None else None
@@ -267,13 +280,13 @@ class SavedForward:
 
 def chunk_gated_delta_rule_fwd_saved(q, k, v, g, beta, scale=None, initial_state=None, cu_seqlens=None,
                                      output_final_state=True, cp_mode="auto", cu_seqlens_cpu=None,
-                                     workspace: Optional[torch.Tensor] = None):
+                                     workspace: Optional[torch.Tensor] = None, out_f32=False):
     """Forward that keeps what its backward needs.  Returns (g_cum, A, o, final_state, saved); pass
     ``saved`` to chunk_gated_delta_rule_bwd_saved, which then skips the backward's recompute passes.
     A given ``workspace`` (large enough) is used and must stay untouched until that backward."""
     lib = load_library()
     cu, host = _cu(cu_seqlens, cu_seqlens_cpu)
-    pr = _problem(_cuda(q, "q", q.dtype), v, scale, cu, host, cp_mode, 8)
+    pr = _problem(_cuda(q, "q", q.dtype), v, scale, cu, host, cp_mode, 8, out_f32)
     need = int(lib.gdn_fwd_workspace_bytes(ctypes.byref(pr)))
     ws = workspace if workspace is not None and workspace.numel() >= need else _workspace(need, q.device)
     # the chunk-entry states are kept only where the saved backward reads them
@@ -281,13 +294,13 @@ def chunk_gated_delta_rule_fwd_saved(q, k, v, g, beta, scale=None, initial_state
     g_cum, A, o, h, ht = chunk_gated_delta_rule_fwd(
         q, k, v, g, beta, scale=scale, initial_state=initial_state, cu_seqlens=cu_seqlens,
         output_final_state=output_final_state, output_h=keep, cp_mode=cp_mode, cu_seqlens_cpu=host,
-        workspace=ws)
+        workspace=ws, out_f32=out_f32)
     return g_cum, A, o, ht, SavedForward(ws, h)
 
 
 def chunk_gated_delta_rule_bwd_saved(q, k, v, g, beta, A, do, saved: SavedForward, dht=None, scale=None,
                                      initial_state=None, cu_seqlens=None, cu_seqlens_cpu=None, cp_mode="auto",
-                                     workspace: Optional[torch.Tensor] = None):
+                                     workspace: Optional[torch.Tensor] = None, out_f32=False):
     """Backward from a chunk_gated_delta_rule_fwd_saved forward on the same inputs (g = its g_cum).
     Returns (dq, dk, dv, db, dg, dh0), equal to chunk_gated_delta_rule_bwd's up to rounding."""
     lib = load_library()
@@ -299,8 +312,10 @@ def chunk_gated_delta_rule_bwd_saved(q, k, v, g, beta, A, do, saved: SavedForwar
     h0 = _cuda(initial_state, "initial_state", torch.float32)
     dht = _cuda(dht, "dht", torch.float32)
     cu, host = _cu(cu_seqlens, cu_seqlens_cpu)
-    pr = _problem(q, v, scale, cu, host, cp_mode, 8)
-    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    pr = _problem(q, v, scale, cu, host, cp_mode, 8, out_f32)
+    odt = torch.float32 if out_f32 else io
+    dq, dk, dv = (torch.empty(q.shape, dtype=odt, device=q.device), torch.empty(k.shape, dtype=odt, device=q.device),
+                  torch.empty(v.shape, dtype=odt, device=q.device))
     db = torch.empty_like(beta)
     dg = torch.empty_like(g)
     dh0 = torch.empty_like(h0) if h0 is not None else None

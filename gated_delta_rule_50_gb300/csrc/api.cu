@@ -3,6 +3,7 @@
 // the stream is never synchronised (except in gdn_workspace_error, which says so).
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
 #include <cstring>
 
@@ -14,6 +15,11 @@
 using namespace gdn;
 
 namespace {
+
+// Test aid of gdn_debug_set_wait: the forward chain's wait limit (0: the default) and dropped load.
+std::atomic<long long> g_dbg_wait_ns{0};
+std::atomic<int> g_dbg_drop_chunk{-1};
+constexpr unsigned long long kDefaultWaitNs = 1000000000ull;
 
 bool aligned16(const void *ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
 bool ok_ptr(const void *ptr) { return ptr != nullptr && aligned16(ptr); }
@@ -29,6 +35,7 @@ gdn_status make_plan(const gdn_problem *pr, Plan *pl) {
     if (pr->cp_mode < GDN_CP_AUTO || pr->cp_mode > GDN_CP_WARMUP) return GDN_ERR_INVALID_ARG;
     if (pr->cp_mode == GDN_CP_WARMUP && (pr->warmup_chunks < 1 || pr->warmup_chunks > 64))
         return GDN_ERR_INVALID_ARG;
+    if (pr->out_f32 != 0 && pr->out_f32 != 1) return GDN_ERR_INVALID_ARG;
     if ((pr->K != 64 && pr->K != 128) || (pr->V != 64 && pr->V != 128)) return GDN_ERR_UNSUPPORTED;
     if (pr->B * pr->T > INT32_MAX / 2 || pr->Hv > 65535 || pr->Hq > 65535) return GDN_ERR_UNSUPPORTED;
     std::memset(pl, 0, sizeof(*pl));
@@ -36,6 +43,10 @@ gdn_status make_plan(const gdn_problem *pr, Plan *pl) {
     pl->K = (int)pr->K; pl->V = (int)pr->V; pl->G = (int)(pr->Hv / pr->Hq);
     pl->io = pr->io_dtype;
     pl->scale = pr->scale;
+    pl->out_f32 = pr->io_dtype == GDN_BF16 ? pr->out_f32 : 0;
+    const long long wns = g_dbg_wait_ns.load();
+    pl->wait_ns = wns > 0 ? (unsigned long long)wns : kDefaultWaitNs;
+    pl->drop_load_chunk = g_dbg_drop_chunk.load();
     pl->cp_mode = pr->cp_mode;
     pl->warmup_chunks = pr->warmup_chunks;
     if (pr->cu_seqlens) {
@@ -175,8 +186,10 @@ Plan padded_plan(const Plan &p) {
 }
 // Workspace of the padded forward: the 128-wide path's own workspace first (its error record stays at
 // offset 0), then the padded inputs and the 128-wide outputs that are sliced back.
+// The padded output o comes last, so that what a saved backward reads (the inner workspace and the
+// 128-wide states h, ending at saved_end) sits at the same offsets whatever the output dtype.
 struct PadFwdWs {
-    size_t inner, q, k, v, o, h0, ht, h, total;
+    size_t inner, q, k, v, h0, ht, h, saved_end, o, total;
 };
 PadFwdWs pad_fwd_layout(const Plan &p) {
     const Plan pp = padded_plan(p);
@@ -187,10 +200,11 @@ PadFwdWs pad_fwd_layout(const Plan &p) {
     w.q = c.take<uint16_t>(p.K < 128 ? tokens * p.Hq * 128 : 0);
     w.k = c.take<uint16_t>(p.K < 128 ? tokens * p.Hq * 128 : 0);
     w.v = c.take<uint16_t>(p.V < 128 ? tokens * p.Hv * 128 : 0);
-    w.o = c.take<uint16_t>(p.V < 128 ? tokens * p.Hv * 128 : 0);
     w.h0 = c.take<float>(nst * state);
     w.ht = c.take<float>(nst * state);
     w.h = c.take<float>((size_t)p.total_chunks * p.Hv * state);
+    w.saved_end = c.off;
+    w.o = c.take<uint16_t>(p.V < 128 ? tokens * p.Hv * 128 * (p.out_f32 ? 2 : 1) : 0);
     w.total = c.off;
     return w;
 }
@@ -205,11 +219,11 @@ PadBwdWs pad_bwd_layout(const Plan &p) {
     w.inner = c.take<unsigned char>(bwd_layout(pp).total);
     w.q = c.take<uint16_t>(p.K < 128 ? tokens * p.Hq * 128 : 0);
     w.k = c.take<uint16_t>(p.K < 128 ? tokens * p.Hq * 128 : 0);
-    w.dq = c.take<uint16_t>(p.K < 128 ? tokens * p.Hq * 128 : 0);
-    w.dk = c.take<uint16_t>(p.K < 128 ? tokens * p.Hq * 128 : 0);
+    w.dq = c.take<uint16_t>(p.K < 128 ? tokens * p.Hq * 128 * (p.out_f32 ? 2 : 1) : 0);
+    w.dk = c.take<uint16_t>(p.K < 128 ? tokens * p.Hq * 128 * (p.out_f32 ? 2 : 1) : 0);
     w.v = c.take<uint16_t>(p.V < 128 ? tokens * p.Hv * 128 : 0);
     w.d_o = c.take<uint16_t>(p.V < 128 ? tokens * p.Hv * 128 : 0);
-    w.dv = c.take<uint16_t>(p.V < 128 ? tokens * p.Hv * 128 : 0);
+    w.dv = c.take<uint16_t>(p.V < 128 ? tokens * p.Hv * 128 * (p.out_f32 ? 2 : 1) : 0);
     w.h0 = c.take<float>(nst * state);
     w.dht = c.take<float>(nst * state);
     w.dh0 = c.take<float>(nst * state);
@@ -266,11 +280,11 @@ PadBwdSavedWs pad_bwd_saved_layout(const Plan &p) {
     w.inner = c.take<unsigned char>(bwd_saved_layout(pp).total);
     w.q = c.take<uint16_t>(p.K < 128 ? tokens * p.Hq * 128 : 0);
     w.k = c.take<uint16_t>(p.K < 128 ? tokens * p.Hq * 128 : 0);
-    w.dq = c.take<uint16_t>(p.K < 128 ? tokens * p.Hq * 128 : 0);
-    w.dk = c.take<uint16_t>(p.K < 128 ? tokens * p.Hq * 128 : 0);
+    w.dq = c.take<uint16_t>(p.K < 128 ? tokens * p.Hq * 128 * (p.out_f32 ? 2 : 1) : 0);
+    w.dk = c.take<uint16_t>(p.K < 128 ? tokens * p.Hq * 128 * (p.out_f32 ? 2 : 1) : 0);
     w.v = c.take<uint16_t>(p.V < 128 ? tokens * p.Hv * 128 : 0);
     w.d_o = c.take<uint16_t>(p.V < 128 ? tokens * p.Hv * 128 : 0);
-    w.dv = c.take<uint16_t>(p.V < 128 ? tokens * p.Hv * 128 : 0);
+    w.dv = c.take<uint16_t>(p.V < 128 ? tokens * p.Hv * 128 * (p.out_f32 ? 2 : 1) : 0);
     w.dht = c.take<float>(nst * state);
     w.dh0 = c.take<float>(nst * state);
     w.total = c.off;
@@ -406,7 +420,7 @@ gdn_status gdn_fwd(const gdn_problem *p, const void *q, const void *k, const voi
     float *hp = h ? at<float>(workspace, w.h) : nullptr;
     s = fwd_impl(padded_plan(pl), qp, kp, vp, g, beta, h0p, op, g_cum, A, hp, htp, at<void>(workspace, w.inner), st);
     if (s != GDN_OK) return s;
-    if (pl.V < 128) GDN_LAUNCH("slice", launch_slice_rows(op, o, tokens * pl.Hv, pl.V, st));
+    if (pl.V < 128) GDN_LAUNCH("slice", launch_slice_rows(op, o, tokens * pl.Hv, pl.V, pl.out_f32 ? 4 : 2, st));
     if (final_state) GDN_LAUNCH("slice", launch_slice_states(htp, final_state, nst, pl.K, pl.V, st));
     if (h) GDN_LAUNCH("slice", launch_slice_states(hp, h, (size_t)pl.total_chunks * pl.Hv, pl.K, pl.V, st));
     return GDN_OK;
@@ -463,10 +477,10 @@ gdn_status gdn_bwd(const gdn_problem *p, const void *q, const void *k, const voi
                  at<void>(workspace, w.inner), st);
     if (s != GDN_OK) return s;
     if (pl.K < 128) {
-        GDN_LAUNCH("slice", launch_slice_rows(dqp, dq, tokens * pl.Hq, pl.K, st));
-        GDN_LAUNCH("slice", launch_slice_rows(dkp, dk, tokens * pl.Hq, pl.K, st));
+        GDN_LAUNCH("slice", launch_slice_rows(dqp, dq, tokens * pl.Hq, pl.K, pl.out_f32 ? 4 : 2, st));
+        GDN_LAUNCH("slice", launch_slice_rows(dkp, dk, tokens * pl.Hq, pl.K, pl.out_f32 ? 4 : 2, st));
     }
-    if (pl.V < 128) GDN_LAUNCH("slice", launch_slice_rows(dvp, dv, tokens * pl.Hv, pl.V, st));
+    if (pl.V < 128) GDN_LAUNCH("slice", launch_slice_rows(dvp, dv, tokens * pl.Hv, pl.V, pl.out_f32 ? 4 : 2, st));
     if (dh0) GDN_LAUNCH("slice", launch_slice_states(dh0p, dh0, nst, pl.K, pl.V, st));
     return GDN_OK;
 }
@@ -577,7 +591,7 @@ gdn_status gdn_bwd_saved(const gdn_problem *p, const void *q, const void *k, con
     if ((h0 == nullptr) != (dh0 == nullptr)) return GDN_ERR_INVALID_ARG;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     void *fws = const_cast<void *>(fwd_workspace);
-    const size_t fwd_need = pad ? pad_fwd_layout(pl).total : fwd_layout(pl).total;
+    const size_t fwd_need = pad ? pad_fwd_layout(pl).saved_end : fwd_layout(pl).total;
     if (!fws || (reinterpret_cast<uintptr_t>(fws) & 255u) || fwd_workspace_bytes < fwd_need)
         return GDN_ERR_WORKSPACE;
     if (!pad) {
@@ -623,10 +637,10 @@ gdn_status gdn_bwd_saved(const gdn_problem *p, const void *q, const void *k, con
                        at<void>(workspace, w.inner), st);
     if (s != GDN_OK) return s;
     if (pl.K < 128) {
-        GDN_LAUNCH("slice", launch_slice_rows(dqp, dq, tokens * pl.Hq, pl.K, st));
-        GDN_LAUNCH("slice", launch_slice_rows(dkp, dk, tokens * pl.Hq, pl.K, st));
+        GDN_LAUNCH("slice", launch_slice_rows(dqp, dq, tokens * pl.Hq, pl.K, pl.out_f32 ? 4 : 2, st));
+        GDN_LAUNCH("slice", launch_slice_rows(dkp, dk, tokens * pl.Hq, pl.K, pl.out_f32 ? 4 : 2, st));
     }
-    if (pl.V < 128) GDN_LAUNCH("slice", launch_slice_rows(dvp, dv, tokens * pl.Hv, pl.V, st));
+    if (pl.V < 128) GDN_LAUNCH("slice", launch_slice_rows(dvp, dv, tokens * pl.Hv, pl.V, pl.out_f32 ? 4 : 2, st));
     if (dh0) GDN_LAUNCH("slice", launch_slice_states(dh0p, dh0, nst, pl.K, pl.V, st));
     return GDN_OK;
 }
@@ -716,6 +730,11 @@ const char *gdn_status_str(gdn_status s) {
     return "unknown status";
 }
 
-const char *gdn_version(void) { return "gdn-gb300 0.1 sm_103a"; }
+const char *gdn_version(void) { return "gdn-gb300 0.2 sm_103a"; }
+
+void gdn_debug_set_wait(int64_t wait_ns, int32_t drop_load_chunk) {
+    g_dbg_wait_ns.store(wait_ns > 0 ? (long long)wait_ns : 0);
+    g_dbg_drop_chunk.store(drop_load_chunk >= 0 ? drop_load_chunk : -1);
+}
 
 }  // extern "C"

@@ -32,7 +32,12 @@ struct Plan {
     int32_t *chunk_off; // device [n_seqs + 1] chunk offsets (varlen) or nullptr
     gdn_dtype io;
     float scale;
+    int out_f32;        // bf16 io: o, A, dq, dk, dv written as fp32 (checking mode)
     uint32_t *err;      // device error word
+    // test aid (gdn_debug_set_wait): limit of the forward chain's device-side waits, and a chunk whose
+    // k / q / operand-image load the chain's producer skips (-1: none)
+    unsigned long long wait_ns;
+    int drop_load_chunk;
 };
 
 struct SeqRange { int tok0, tok1, c0, c1; };  // token span and global chunk span

@@ -56,10 +56,11 @@ cudaError_t launch_tc_fwd(const Plan &p, const void *q, const void *k, const voi
                           const float *vecs, const float *h0, void *o, float *h, float *ht, cudaStream_t st,
                           const CpSplit *cp = nullptr);
 
-// Zero padding of 64-wide heads to the 128-wide tensor-core tiles (pad.cu): rows [rows][d] bf16 <->
-// [rows][128]; states [n][K][V] fp32 <-> [n][128][128].  Pointers 16-byte aligned.
+// Zero padding of 64-wide heads to the 128-wide tensor-core tiles (pad.cu): rows [rows][d] bf16 ->
+// [rows][128]; slices back [rows][128] -> [rows][d] of bf16 or fp32 elements; states [n][K][V] fp32 <->
+// [n][128][128].  Pointers 16-byte aligned.
 cudaError_t launch_pad_rows(const void *src, void *dst, size_t rows, int d, cudaStream_t st);
-cudaError_t launch_slice_rows(const void *src, void *dst, size_t rows, int d, cudaStream_t st);
+cudaError_t launch_slice_rows(const void *src, void *dst, size_t rows, int d, int elem_bytes, cudaStream_t st);
 cudaError_t launch_pad_states(const float *src, float *dst, size_t n, int K, int V, cudaStream_t st);
 cudaError_t launch_slice_states(const float *src, float *dst, size_t n, int K, int V, cudaStream_t st);
 

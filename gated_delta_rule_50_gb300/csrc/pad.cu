@@ -23,12 +23,13 @@ __global__ void k_pad_rows(const uint4 *__restrict__ src, uint4 *__restrict__ ds
     }
 }
 
-// dst [rows][d] <- the leading d columns of src [rows][128].
-__global__ void k_slice_rows(const uint4 *__restrict__ src, uint4 *__restrict__ dst, size_t rows, int d) {
-    const size_t cpr = (size_t)d / 8, n = rows * cpr;
+// dst [rows][d] <- the leading d columns of src [rows][128]; cpr = 16-byte chunks per dst row, spr per src row.
+__global__ void k_slice_rows(const uint4 *__restrict__ src, uint4 *__restrict__ dst, size_t rows, size_t cpr,
+                             size_t spr) {
+    const size_t n = rows * cpr;
     for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
         const size_t r = i / cpr, c = i - r * cpr;
-        dst[i] = src[r * (W / 8) + c];
+        dst[i] = src[r * spr + c];
     }
 }
 
@@ -63,10 +64,11 @@ cudaError_t launch_pad_rows(const void *src, void *dst, size_t rows, int d, cuda
     return cudaGetLastError();
 }
 
-cudaError_t launch_slice_rows(const void *src, void *dst, size_t rows, int d, cudaStream_t st) {
+cudaError_t launch_slice_rows(const void *src, void *dst, size_t rows, int d, int elem_bytes, cudaStream_t st) {
     if (rows == 0) return cudaSuccess;
-    k_slice_rows<<<grid_for(rows * (size_t)d / 8), 256, 0, st>>>(static_cast<const uint4 *>(src),
-                                                                 static_cast<uint4 *>(dst), rows, d);
+    const size_t cpr = (size_t)d * elem_bytes / 16, spr = (size_t)W * elem_bytes / 16;
+    k_slice_rows<<<grid_for(rows * cpr), 256, 0, st>>>(static_cast<const uint4 *>(src), static_cast<uint4 *>(dst),
+                                                       rows, cpr, spr);
     return cudaGetLastError();
 }
 

@@ -66,15 +66,16 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
-// Bounded wait.  Returns false if the barrier did not complete within WAIT_NS
+// Bounded wait.  Returns false if the barrier did not complete within limit_ns
 // or another thread already raised *abort; on its own expiry it raises *abort.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort) {
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort,
+                                          uint64_t limit_ns = WAIT_NS) {
     if (mbar_test(bar, parity)) return true;
     const uint64_t t0 = global_ns();
     for (;;) {
         if (mbar_try(bar, parity)) return true;
         if (*abort) return false;
-        if (global_ns() - t0 > WAIT_NS) {
+        if (global_ns() - t0 > limit_ns) {
             *abort = 1;
             return false;
         }
@@ -82,14 +83,15 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
 }
 // Warp-uniform result of a bounded wait (tcgen05.ld and other .sync.aligned
 // instructions after it need every lane of the warp).
-__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, volatile int *abort) {
-    return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort));
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, volatile int *abort,
+                                               uint64_t limit_ns = WAIT_NS) {
+    return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort, limit_ns));
 }
 // Bounded wait without an abort flag (used for draining at exit).
-__device__ __forceinline__ bool mbar_drain(uint32_t bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_drain(uint32_t bar, uint32_t parity, uint64_t limit_ns = WAIT_NS) {
     const uint64_t t0 = global_ns();
     while (!mbar_test(bar, parity))
-        if (global_ns() - t0 > WAIT_NS) return false;
+        if (global_ns() - t0 > limit_ns) return false;
     return true;
 }
 

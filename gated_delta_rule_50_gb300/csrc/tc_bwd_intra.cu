@@ -81,7 +81,7 @@ struct IntraArgs {
     const unsigned char *tiles;  // [chunks][Hv] x 32 KB: A hi / lo, P hi / lo operand images
     const float *vecs;           // [chunks][Hv] x {gam, Gam, E, beta} x 64
     const float *hbuf, *dSe;
-    __nv_bfloat16 *dq, *dk, *dv;
+    void *dq, *dk, *dv;  // bf16, or fp32 when p.out_f32
     float *dbeta, *dg;
 };
 
@@ -450,7 +450,11 @@ k_tc_bwd_intra(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
                     const int i = 8 * q2 + e, c = 16 * hh + i;
                     const float drv = __uint_as_float(dr[i]);
                     s8[e] = p.scale * Gm[c] * tile128_at(sm, S_DO, c, lrow);  // scale Gam dO (Gm = 0 past n)
-                    dvs[c * DV + lrow] = __float2bfloat16_rn(bet[c] * drv);
+                    if (!p.out_f32)
+                        dvs[c * DV + lrow] = __float2bfloat16_rn(bet[c] * drv);
+                    else if (c < n)  // checking mode: fp32 dv straight out (one 128-byte row segment per warp)
+                        static_cast<float *>(a.dv)[(size_t)(tok0 + c) * p.Hv * DV + (size_t)hv * DV + lrow] =
+                            bet[c] * drv;
                     pb[i] = drv * Xr[i];
                     pg[i] = -bg[c] * drv * KSr[i];
                     y8[e] = -bg[c] * drv;
@@ -537,13 +541,13 @@ k_tc_bwd_intra(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
             mma_chain<4, 2, 2>(tmem + C_KS, kdesc(sb + S_A + 8192), kdesc(sb + S_P), ID_KK, 1);
         }
         // while Z runs: dv out, then (E Dl)^T into the staging region
-        {  // dv out: 64 rows x 256 bytes from the staging tile, 16-byte stores
+        if (!p.out_f32) {  // dv out: 64 rows x 256 bytes from the staging tile, 16-byte stores
             const uint4 *src = reinterpret_cast<const uint4 *>(sm + S_DD);
             for (int o = t; o < 64 * 16; o += NT) {
                 const int r = o >> 4, c16 = o & 15;
                 if (r < n)
-                    *reinterpret_cast<uint4 *>(a.dv + (size_t)(tok0 + r) * p.Hv * DV + (size_t)hv * DV + 8 * c16) =
-                        src[o];
+                    *reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(a.dv) + (size_t)(tok0 + r) * p.Hv * DV +
+                                               (size_t)hv * DV + 8 * c16) = src[o];
             }
         }
         __syncthreads();
@@ -742,7 +746,21 @@ k_tc_bwd_intra(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         mma_sync();
     }
     // ---------------------------------------------------------------- dq, dk out (thread: key lrow, rows 16 hh + j)
-    if (ok) {
+    if (ok && p.out_f32) {  // checking mode: fp32 dq, dk
+        uint32_t d[16];
+        const size_t rs = (size_t)p.Hq * DK, o0 = (size_t)tok0 * rs + (size_t)hq * DK + lrow;
+        float *dqp = static_cast<float *>(a.dq) + o0, *dkp = static_cast<float *>(a.dk) + o0;
+        tmem_ld16(tmem + trow + C_DQ + 16 * hh, d);
+        tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+            if (16 * hh + j < n) dqp[(size_t)(16 * hh + j) * rs] = __uint_as_float(d[j]);
+        tmem_ld16(tmem + trow + C_DK + 16 * hh, d);
+        tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+            if (16 * hh + j < n) dkp[(size_t)(16 * hh + j) * rs] = __uint_as_float(d[j]);
+    } else if (ok) {
         uint32_t d[16];
         uint16_t *dqp = reinterpret_cast<uint16_t *>(a.dq) + (size_t)hq * DK + lrow;
         uint16_t *dkp = reinterpret_cast<uint16_t *>(a.dk) + (size_t)hq * DK + lrow;
@@ -807,9 +825,9 @@ cudaError_t launch_tc_bwd_intra(const Plan &p, const void *q, const void *k, con
     a.vecs = vecs;
     a.hbuf = hbuf;
     a.dSe = dSe;
-    a.dq = static_cast<__nv_bfloat16 *>(dq);
-    a.dk = static_cast<__nv_bfloat16 *>(dk);
-    a.dv = static_cast<__nv_bfloat16 *>(dv);
+    a.dq = dq;
+    a.dk = dk;
+    a.dv = dv;
     a.dbeta = dbeta;
     a.dg = dg;
     dim3 grid(p.total_chunks, p.Hq);

@@ -79,7 +79,7 @@ struct FwdArgs {
     const unsigned char *tiles;  // [chunks][Hv] x 32 KB operand images from the prep kernel
     const float *vecs;           // [chunks][Hv] x {gam, Gam, E, beta} x 64
     const float *h0;
-    __nv_bfloat16 *o;
+    void *o;  // bf16, or fp32 when p.out_f32
     float *h, *ht;
     // sequence splitting (see cp.cu and launch.h): seg_len > 0 enables it
     int seg_len, n_seg, warm, mode;  // mode: CP_WARM, CP_MAIN or CP_SEG
@@ -163,7 +163,7 @@ k_tc_fwd(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
     sr.c0 += jb;
     sr.c1 = sr.c0 + (je - jb);
     const int nck = je - jb;
-    __nv_bfloat16 *o_out = outs ? a.o : nullptr;
+    void *o_out = outs ? a.o : nullptr;
     float *h_out = outs ? a.h : nullptr;
 
     if (threadIdx.x == 0) {
@@ -191,21 +191,23 @@ k_tc_fwd(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
             for (int j = 0; j < nck; ++j) {
                 const int st = j & 1;
                 const size_t unit = (size_t)(sr.c0 + j) * p.Hv + hv;
-                if (j >= 2 && !mbar_wait(bar(B_EMPTY0 + st), ((j >> 1) - 1) & 1, abort_flag)) {
+                if (j >= 2 && !mbar_wait(bar(B_EMPTY0 + st), ((j >> 1) - 1) & 1, abort_flag, p.wait_ns)) {
                     record_timeout(p, B_EMPTY0 + st, j);
                     break;
                 }
                 const int tok0 = sr.tok0 + j * C;
-                mbar_arrive_expect_tx(bar(B_FULL0 + st), KQ_BYTES + AP_BYTES);
-                const uint32_t dst = sb + SM_KQ + st * KQ_STAGE;
-                tma_load_3d(dst, &tm_k, bar(B_FULL0 + st), 0, hq, tok0);
-                tma_load_3d(dst + 8192, &tm_q, bar(B_FULL0 + st), 0, hq, tok0);
-                tma_load_3d(dst + 16384, &tm_k, bar(B_FULL0 + st), 64, hq, tok0);
-                tma_load_3d(dst + 24576, &tm_q, bar(B_FULL0 + st), 64, hq, tok0);
-                bulk_load(dst + AP_OFF, a.tiles + unit * AP_BYTES, AP_BYTES, bar(B_FULL0 + st));
+                if (j != p.drop_load_chunk) {  // (the test aid skips this chunk: its consumer's wait expires)
+                    mbar_arrive_expect_tx(bar(B_FULL0 + st), KQ_BYTES + AP_BYTES);
+                    const uint32_t dst = sb + SM_KQ + st * KQ_STAGE;
+                    tma_load_3d(dst, &tm_k, bar(B_FULL0 + st), 0, hq, tok0);
+                    tma_load_3d(dst + 8192, &tm_q, bar(B_FULL0 + st), 0, hq, tok0);
+                    tma_load_3d(dst + 16384, &tm_k, bar(B_FULL0 + st), 64, hq, tok0);
+                    tma_load_3d(dst + 24576, &tm_q, bar(B_FULL0 + st), 64, hq, tok0);
+                    bulk_load(dst + AP_OFF, a.tiles + unit * AP_BYTES, AP_BYTES, bar(B_FULL0 + st));
+                }
                 issued = j + 1;
                 // v tile and gate vectors; the buffer last held the staged o of chunk j - 2
-                if (j >= 2 && !mbar_wait(bar(B_VEMPTY0 + st), ((j >> 1) - 1) & 1, abort_flag)) {
+                if (j >= 2 && !mbar_wait(bar(B_VEMPTY0 + st), ((j >> 1) - 1) & 1, abort_flag, p.wait_ns)) {
                     record_timeout(p, B_VEMPTY0 + st, j);
                     break;
                 }
@@ -218,9 +220,10 @@ k_tc_fwd(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
                 vissued = j + 1;
             }
             // never leave with copies in flight
-            for (int j = (issued > 2 ? issued - 2 : 0); j < issued; ++j) mbar_drain(bar(B_FULL0 + (j & 1)), (j >> 1) & 1);
+            for (int j = (issued > 2 ? issued - 2 : 0); j < issued; ++j)
+                if (j != p.drop_load_chunk) mbar_drain(bar(B_FULL0 + (j & 1)), (j >> 1) & 1, p.wait_ns);
             for (int j = (vissued > 2 ? vissued - 2 : 0); j < vissued; ++j)
-                mbar_drain(bar(B_VFULL0 + (j & 1)), (j >> 1) & 1);
+                mbar_drain(bar(B_VFULL0 + (j & 1)), (j >> 1) & 1, p.wait_ns);
         }
         __syncwarp();
     } else if (warp == W_MMA) {
@@ -229,7 +232,7 @@ k_tc_fwd(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
             auto kq = [&](int st) { return sb + SM_KQ + (uint32_t)st * KQ_STAGE; };
             int failed = -1, fj = 0;
             auto wait = [&](int id, uint32_t par, int j) {
-                if (mbar_wait(bar(id), par, abort_flag)) return true;
+                if (mbar_wait(bar(id), par, abort_flag, p.wait_ns)) return true;
                 failed = id;
                 fj = j;
                 return false;
@@ -276,7 +279,7 @@ k_tc_fwd(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
             }
             // every issued MMA completes before TMEM is released
             mma_commit(bar(B_FINAL));
-            mbar_drain(bar(B_FINAL), 0);
+            mbar_drain(bar(B_FINAL), 0, p.wait_ns);
             if (failed >= 0) record_timeout(p, failed, fj);
         }
         __syncwarp();
@@ -289,7 +292,7 @@ k_tc_fwd(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
         const uint32_t trow = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
         int failed = -1, fj = 0;
         auto wwait = [&](int id, uint32_t par, int j) {  // warp-uniform bounded wait
-            bool w = mbar_wait_warp(bar(id), par, abort_flag);
+            bool w = mbar_wait_warp(bar(id), par, abort_flag, p.wait_ns);
             if (!w && failed < 0) { failed = id; fj = j; }
             return w;
         };
@@ -322,6 +325,18 @@ k_tc_fwd(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
             tmem_wait_ld();
             tc_fence_before();
             mbar_arrive(bar(B_EPIFREE0 + b));
+            if (p.out_f32) {  // checking mode: the fp32 value, one 128-byte row segment per warp and row
+                float *of = static_cast<float *>(o_out) + (size_t)tok0 * p.Hv * DV + (size_t)hv * DV + v;
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const int c = 16 * hh + i;
+                    if (c < n)
+                        of[(size_t)c * p.Hv * DV] =
+                            p.scale * fmaf(gm[i], __uint_as_float(qs[i]), __uint_as_float(oo[i]));
+                }
+                mbar_arrive(bar(B_VEMPTY0 + b));
+                return true;
+            }
 #pragma unroll
             for (int i = 0; i < 16; ++i)  // row i of this warp's 16, column lane
                 stg[i * 32 + lane] =
@@ -333,7 +348,8 @@ k_tc_fwd(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
                 const int ri = 8 * k2 + (lane >> 2), c = 16 * hh + ri;
                 const uint4 w = src[ri * 4 + (lane & 3)];
                 if (c < n)
-                    *reinterpret_cast<uint4 *>(o_out + ((size_t)(tok0 + c) * p.Hv + hv) * DV + 32 * (warp & 3) +
+                    *reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(o_out) +
+                                               ((size_t)(tok0 + c) * p.Hv + hv) * DV + 32 * (warp & 3) +
                                                8 * (lane & 3)) = w;
             }
             mbar_arrive(bar(B_VEMPTY0 + b));
@@ -495,7 +511,7 @@ cudaError_t launch_tc_fwd(const Plan &p, const void *q, const void *k, const voi
     a.tiles = tiles;
     a.vecs = vecs;
     a.h0 = h0;
-    a.o = static_cast<__nv_bfloat16 *>(o);
+    a.o = o;
     a.h = h;
     a.ht = ht;
     a.seg_len = 0;

@@ -50,7 +50,7 @@ struct PrepArgs {
     const float *g, *beta;
     int g_is_cum;
     float *g_cum;
-    __nv_bfloat16 *A;
+    void *A;  // [B,T,Hv,64]: bf16, or fp32 when p.out_f32
     float *A32, *P32;
     unsigned char *tiles;  // [chunks][Hv] x 32 KB
     float *vecs;           // [chunks][Hv] x 256
@@ -282,9 +282,16 @@ k_tc_prep(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                 for (int e = 0; e < 8; ++e) vals[e] = Lm[r * 65 + 8 * ch + e];
                 put_split_chunk(img, img + 8192, r, ch, vals);
                 if (a.A && r < n) {
-                    const uint4 pk = make_uint4(pack_bf16(vals[0], vals[1]), pack_bf16(vals[2], vals[3]),
-                                                pack_bf16(vals[4], vals[5]), pack_bf16(vals[6], vals[7]));
-                    *reinterpret_cast<uint4 *>(a.A + ((size_t)(tok0 + r) * p.Hv + hv) * C + 8 * ch) = pk;
+                    const size_t ao = ((size_t)(tok0 + r) * p.Hv + hv) * C + 8 * ch;
+                    if (p.out_f32) {
+                        float4 *d = reinterpret_cast<float4 *>(static_cast<float *>(a.A) + ao);
+                        d[0] = make_float4(vals[0], vals[1], vals[2], vals[3]);
+                        d[1] = make_float4(vals[4], vals[5], vals[6], vals[7]);
+                    } else {
+                        const uint4 pk = make_uint4(pack_bf16(vals[0], vals[1]), pack_bf16(vals[2], vals[3]),
+                                                    pack_bf16(vals[4], vals[5]), pack_bf16(vals[6], vals[7]));
+                        *reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(a.A) + ao) = pk;
+                    }
                 }
                 if (a.A32) {
                     float4 *d = reinterpret_cast<float4 *>(a.A32 + unit * C * C + (size_t)r * C + 8 * ch);
@@ -328,7 +335,7 @@ cudaError_t launch_tc_prep(const Plan &p, const void *q, const void *k, const fl
     a.beta = beta;
     a.g_is_cum = g_is_cum ? 1 : 0;
     a.g_cum = g_cum;
-    a.A = static_cast<__nv_bfloat16 *>(A);
+    a.A = A;
     a.A32 = A32;
     a.P32 = P32;
     a.tiles = tiles;

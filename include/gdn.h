@@ -93,7 +93,18 @@ typedef struct {
     float scale;                     /* output scale; K^-0.5 is the usual choice     */
     int32_t cp_mode;                 /* gdn_cp_mode                                  */
     int32_t warmup_chunks;           /* GDN_CP_WARMUP only: chunks of warmup (6..8)  */
+    int32_t out_f32;                 /* checking mode, 0 or 1; see below              */
 } gdn_problem;
+
+/*
+ * out_f32 = 1 with io_dtype GDN_BF16: the same kernels, in the same order,
+ * write o and A (gdn_fwd) and dq, dk, dv (gdn_bwd, gdn_bwd_saved) as fp32
+ * instead of rounding them to bf16; those buffers are then fp32 tensors of
+ * the shapes above.  It exposes the value each kernel holds before its final
+ * rounding, so that a test can hold it to an error bound tighter than one
+ * bf16 rounding.  Ignored for GDN_F32 (every output is fp32 already).  The
+ * forward's saved state for gdn_bwd_saved does not depend on it.
+ */
 
 /* Bytes of device workspace gdn_fwd / gdn_bwd need for this problem (0 on a
  * bad problem).  The workspace must be 256-byte aligned. */
@@ -165,8 +176,18 @@ gdn_status gdn_bwd(const gdn_problem *p,
  *     rewrites what it reads and clears its error word), so calls whose GPU
  *     work overlaps -- on different streams or host threads -- race on it and
  *     must be serialised by the caller.
- *   - The first call on each device looks the array's address up with that
- *     device current; make that first call before any stream capture.
+ *   - The array's address belongs to the CUDA context current at the call.
+ *     Outside stream capture each call looks it up afresh, so a device reset
+ *     or a caller-made driver context is served with its own address.  During
+ *     capture the address cached for the current context by an earlier call
+ *     is used: make one call in each context before any stream capture (a
+ *     capture in a context never seen before returns GDN_ERR_CUDA).
+ *   - What fits: the tensor-core forward needs about 33 KB per (chunk, value
+ *     head), so about 1000 chunk x value-head units fit (e.g. B = 1, T = 8192,
+ *     Hv = 8: 1024 units, just over; T = 4096, Hv = 8: 512 units plus the
+ *     sequence split's segment states, about 30 MB, fits).
+ *     gdn_fwd_workspace_bytes(p) is the exact test.
+ *   - Invalid or unsupported problems return gdn_fwd's own status.
  */
 #define GDN_NOALLOC_SCRATCH_BYTES (32u << 20)
 gdn_status gdn_fwd_noalloc(const gdn_problem *p,
@@ -174,6 +195,11 @@ gdn_status gdn_fwd_noalloc(const gdn_problem *p,
                            const float *g, const float *beta, const float *h0,
                            void *o, float *g_cum, void *A, float *h, float *final_state,
                            gdn_stream_t stream);
+/* The error word gdn_fwd_noalloc's last call left in the shared array of the
+ * current context (synchronises `stream`): GDN_OK, or GDN_ERR_TIMEOUT when a
+ * device-side bounded wait of that call expired; GDN_ERR_CUDA if the array
+ * cannot be reached. */
+gdn_status gdn_fwd_noalloc_error(gdn_stream_t stream);
 
 /*
  * Backward that reuses what the forward saved instead of recomputing it (the
@@ -243,8 +269,23 @@ const char *gdn_status_str(gdn_status s);
 void gdn_profile_enable(int on);
 int gdn_profile_read(char *names, int name_stride, int *counts, double *ms, int max_entries);
 
-/* Library version string, e.g. "gdn-gb300 0.1 sm_103a". */
+/* Library version string, e.g. "gdn-gb300 0.2 sm_103a". */
 const char *gdn_version(void);
+
+/*
+ * Test aid for the bounded device-side waits (process-wide; set it only while
+ * no other thread calls the library).  Problems planned after this call use
+ * wait_ns as the limit of every mbarrier wait of the forward's state-chain
+ * kernel (wait_ns <= 0 restores the default of one second) and, when
+ * drop_load_chunk >= 0, that kernel's producer skips the k / q / operand-image
+ * load of the chunk with this index in every chain.  The consumer's wait on
+ * that load then expires: the kernel records GDN_ERR_TIMEOUT in the workspace
+ * error word (read by gdn_workspace_error), waits for its own copies and
+ * tensor-core operations in flight, frees its tensor memory and returns, and
+ * the outputs of that call are incomplete.  Later calls on the same stream
+ * run normally.  gdn_debug_set_wait(0, -1) restores the defaults.
+ */
+void gdn_debug_set_wait(int64_t wait_ns, int32_t drop_load_chunk);
 
 #ifdef __cplusplus
 }

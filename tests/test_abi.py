@@ -54,37 +54,84 @@ def test_workspace_bytes_validation(lib, kw, ok):
     assert (n > 0) == ok
 
 
-def test_varlen_host_offsets_validated(lib):
-    cu = (ctypes.c_int32 * 3)(0, 100, 128)
-    bad = (ctypes.c_int32 * 3)(0, 100, 120)          # does not end at T
-    dummy = ctypes.c_void_p(256)                      # never dereferenced on this path
-    p = _prob(n_seqs=2, cu_seqlens=dummy, cu_seqlens_host=ctypes.cast(cu, ctypes.c_void_p))
-    assert lib.gdn_fwd_workspace_bytes(ctypes.byref(p)) > 0
-    p.cu_seqlens_host = ctypes.cast(bad, ctypes.c_void_p)
-    assert lib.gdn_fwd_workspace_bytes(ctypes.byref(p)) == 0
-    p.cu_seqlens_host = None                          # host copy is required
-    assert lib.gdn_fwd_workspace_bytes(ctypes.byref(p)) == 0
+# Argument checks that hand the library placeholder addresses run in a child process that sees no GPU
+# (CUDA_VISIBLE_DEVICES=""): the statuses asserted come from host validation, and even a regression in the
+# validation order could not launch a kernel on a fabricated address.
+_NO_GPU_CHECKS = r"""
+import ctypes, sys
+sys.path.insert(0, ROOT)
+import gated_delta_rule_50_gb300 as gdn
+lib = gdn.load_library()
+P = ctypes.c_void_p
+def prob(**kw):
+    p = gdn._Problem()
+    p.B, p.T, p.Hq, p.Hv, p.K, p.V, p.n_seqs = 1, 128, 2, 4, 128, 128, 1
+    p.io_dtype, p.scale, p.cp_mode, p.warmup_chunks = 1, 0.1, 0, 8
+    for k, v in kw.items():
+        setattr(p, k, v)
+    return p
+out = {}
+# varlen: the host copy of the offsets is validated (the device pointer is never read on this path)
+cu = (ctypes.c_int32 * 3)(0, 100, 128)
+bad = (ctypes.c_int32 * 3)(0, 100, 120)
+p = prob(n_seqs=2, cu_seqlens=P(256), cu_seqlens_host=ctypes.cast(cu, P))
+out["varlen_ok"] = lib.gdn_fwd_workspace_bytes(ctypes.byref(p)) > 0
+p.cu_seqlens_host = ctypes.cast(bad, P)
+out["varlen_bad_end"] = lib.gdn_fwd_workspace_bytes(ctypes.byref(p))
+p.cu_seqlens_host = None
+out["varlen_no_host"] = lib.gdn_fwd_workspace_bytes(ctypes.byref(p))
+p = prob()
+out["null_q"] = lib.gdn_fwd(ctypes.byref(p), None, P(256), P(256), P(256), P(256), None, P(256), None, None,
+                            None, None, P(256), 1 << 40, None)
+out["misaligned"] = lib.gdn_fwd(ctypes.byref(p), P(257), P(256), P(256), P(256), P(256), None, P(256), None,
+                                None, None, None, P(256), 1 << 40, None)
+out["small_ws"] = lib.gdn_fwd(ctypes.byref(p), P(256), P(256), P(256), P(256), P(256), None, P(256), None, None,
+                              None, None, P(256), 16, None)
+out["bwd_h0_dh0"] = lib.gdn_bwd(ctypes.byref(p), *([P(256)] * 5), None, P(256), None, P(256), *([P(256)] * 5),
+                                None, P(256), 1 << 40, None)
+out["out_f32_bad"] = lib.gdn_fwd_workspace_bytes(ctypes.byref(prob(out_f32=2)))
+# the no-alloc forward answers an invalid or unsupported problem with gdn_fwd's own status
+for name, kw in (("k96", {"K": 96}), ("hv3", {"Hv": 3})):
+    q = prob(**kw)
+    out["noalloc_" + name] = lib.gdn_fwd_noalloc(ctypes.byref(q), *([None] * 11), None)
+    out["fwd_" + name] = lib.gdn_fwd(ctypes.byref(q), *([None] * 11), None, 0, None)
+print(repr(out))
+"""
 
 
-def test_bad_pointers_rejected_without_launch(lib):
-    p = _prob()
-    P = ctypes.c_void_p
-    # null q: rejected on the host (status 1) before any CUDA call
-    rc = lib.gdn_fwd(ctypes.byref(p), None, P(256), P(256), P(256), P(256), None, P(256), None, None,
-                     None, None, P(256), 1 << 40, None)
-    assert rc == 1
-    # misaligned pointer
-    rc = lib.gdn_fwd(ctypes.byref(p), P(257), P(256), P(256), P(256), P(256), None, P(256), None, None,
-                     None, None, P(256), 1 << 40, None)
-    assert rc == 1
-    # workspace too small
-    rc = lib.gdn_fwd(ctypes.byref(p), P(256), P(256), P(256), P(256), P(256), None, P(256), None, None,
-                     None, None, P(256), 16, None)
-    assert rc == 3
-    # bwd: dh0 must be given iff h0 is
-    rc = lib.gdn_bwd(ctypes.byref(p), *([P(256)] * 5), None, P(256), None, P(256), *([P(256)] * 5), None,
-                     P(256), 1 << 40, None)
-    assert rc == 1
+def _no_gpu_results():
+    import ast
+    import subprocess
+    import sys
+    env = dict(os.environ, CUDA_VISIBLE_DEVICES="")
+    r = subprocess.run([sys.executable, "-c", f"ROOT = {ROOT!r}\n" + _NO_GPU_CHECKS], env=env,
+                       capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    return ast.literal_eval(r.stdout.strip().splitlines()[-1])
+
+
+@pytest.fixture(scope="module")
+def no_gpu():
+    return _no_gpu_results()
+
+
+def test_varlen_host_offsets_validated(no_gpu):
+    assert no_gpu["varlen_ok"]
+    assert no_gpu["varlen_bad_end"] == 0      # does not end at T
+    assert no_gpu["varlen_no_host"] == 0      # the host copy is required
+
+
+def test_bad_pointers_rejected_without_launch(no_gpu):
+    assert no_gpu["null_q"] == 1              # null q: rejected on the host
+    assert no_gpu["misaligned"] == 1          # misaligned pointer
+    assert no_gpu["small_ws"] == 3            # workspace too small
+    assert no_gpu["bwd_h0_dh0"] == 1          # dh0 must be given iff h0 is
+    assert no_gpu["out_f32_bad"] == 0         # out_f32 is 0 or 1
+
+
+def test_noalloc_status_matches_gdn_fwd(no_gpu):
+    assert no_gpu["noalloc_k96"] == no_gpu["fwd_k96"] == 2
+    assert no_gpu["noalloc_hv3"] == no_gpu["fwd_hv3"] == 1
 
 
 def test_python_api_names_match_pages():

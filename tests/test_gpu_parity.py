@@ -73,40 +73,75 @@ def split_d64_case():  # 64-wide heads through the exact sequence split; one val
 CASES["bf16_d64_split"] = split_d64_case
 
 
-@pytest.mark.parametrize("name", list(CASES))
-def test_fwd_small(name):
+def _store_modes(name):
+    """bf16 io runs twice: bf16 outputs (bound + half an ulp of bf16) and the fp32-store checking mode
+    (the plain bound); fp32 io has only fp32 outputs."""
+    return [False, True] if not name.endswith("fp32") and "fp32_" not in name else [False]
+
+
+SMALL = [(n, f) for n in CASES for f in _store_modes(n)]
+
+
+@pytest.mark.parametrize("name,out_f32", SMALL)
+def test_fwd_small(name, out_f32):
     x = CASES[name]()
-    run_fwd_case(x)
+    run_fwd_case(x, out_f32=out_f32)
 
 
-@pytest.mark.parametrize("name", list(CASES))
-def test_bwd_small(name):
+@pytest.mark.parametrize("name,out_f32", SMALL)
+def test_bwd_small(name, out_f32):
     x = CASES[name]()
     if x["do"] is None:
         pytest.skip("no upstream gradient")
-    run_bwd_case(x)
+    run_bwd_case(x, out_f32=out_f32)
 
 
-def test_fwd_h_output_and_state_continuation():
-    """The returned chunk-entry states equal the final states of prefix runs,
-    and running two halves with state passing equals one run."""
+@pytest.mark.parametrize("varlen", [False, True])
+def test_fwd_h_output_vs_oracle_and_state_continuation(varlen):
+    """The returned chunk-entry states h equal the oracle's final states of the prefix runs (fp32
+    output: 2e-3 * RMS), and running two halves with state passing equals one run."""
     import gated_delta_rule_50_gb300 as gdn
-    x = small("train_b2_t8192_h64", B=1, T=256, Hq=1, Hv=2, seed=20)
+    import oracle
+    from parity import check
+    x = small("train_b2_t8192_h64", B=1, T=300, Hq=1, Hv=2, seed=20)
+    cu = torch.tensor([0, 130, 300], dtype=torch.int32) if varlen else None
     d = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
-    _, _, o, h, ht = gdn.chunk_gated_delta_rule_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"],
-                                                    initial_state=d["h0"], output_h=True)
-    for c in (1, 2, 3):
-        t = 64 * c
-        _, _, _, _, hp = gdn.chunk_gated_delta_rule_fwd(d["q"][:, :t], d["k"][:, :t], d["v"][:, :t],
-                                                        d["g"][:, :t], d["beta"][:, :t],
-                                                        initial_state=d["h0"])
-        assert torch.allclose(h[0, c], hp[0], atol=1e-5, rtol=1e-5)
+    h0 = d["h0"] if not varlen else d["h0"].repeat(2, 1, 1, 1) * torch.tensor([1.0, -0.5], device="cuda").view(2, 1, 1, 1)
+    _, _, o, h, ht = gdn.chunk_gated_delta_rule_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], scale=x["scale"],
+                                                    initial_state=h0, output_h=True,
+                                                    cu_seqlens=cu.cuda() if varlen else None)
+    torch.cuda.synchronize()
+    h = h.reshape(-1, 2, 128, 128)  # [chunks over all sequences][Hv][K][V]
+    seqs = [(0, 130), (130, 300)] if varlen else [(0, 300)]
+    ci = 0
+    h0c = h0.cpu()
+    for si, (a, b) in enumerate(seqs):
+        for c0 in range(a, b, 64):
+            if c0 == a:
+                ref = h0c[si].double().numpy()
+            else:
+                sl = slice(a, c0)
+                _, ref = oracle.oracle_fwd(x["q"][:, sl], x["k"][:, sl], x["v"][:, sl], x["g"][:, sl],
+                                           x["beta"][:, sl], x["scale"], h0c[si:si + 1])
+                ref = ref[0]
+            check(f"h[{ci}]", h[ci], ref, x["q"].dtype, torch.float32)
+            ci += 1
+    assert ci == h.shape[0]
+    if varlen:
+        return
     _, _, o1, _, h1 = gdn.chunk_gated_delta_rule_fwd(d["q"][:, :128], d["k"][:, :128], d["v"][:, :128],
-                                                     d["g"][:, :128], d["beta"][:, :128], initial_state=d["h0"])
+                                                     d["g"][:, :128], d["beta"][:, :128], scale=x["scale"],
+                                                     initial_state=d["h0"], out_f32=True)
     _, _, o2, _, h2 = gdn.chunk_gated_delta_rule_fwd(d["q"][:, 128:], d["k"][:, 128:], d["v"][:, 128:],
-                                                     d["g"][:, 128:], d["beta"][:, 128:], initial_state=h1)
-    assert torch.allclose(torch.cat([o1, o2], 1).float(), o.float(), atol=2e-2, rtol=0)
-    assert torch.allclose(h2, ht, atol=1e-4, rtol=1e-4)
+                                                     d["g"][:, 128:], d["beta"][:, 128:], scale=x["scale"],
+                                                     initial_state=h1, out_f32=True)
+    _, _, of, _, _ = gdn.chunk_gated_delta_rule_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], scale=x["scale"],
+                                                    initial_state=d["h0"], out_f32=True)
+    torch.cuda.synchronize()
+    o_ref, ht_ref = oracle.oracle_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["scale"], x["h0"])
+    check("o (two halves)", torch.cat([o1, o2], 1), o_ref, x["q"].dtype, torch.float32)
+    check("o (one run)", of, o_ref, x["q"].dtype, torch.float32)
+    check("final_state (two halves)", h2, ht_ref, x["q"].dtype, torch.float32)
 
 
 def test_autograd_matches_low_level():
@@ -125,25 +160,35 @@ def test_autograd_matches_low_level():
 
 
 # ------------------------------------------------------------- full-size workloads
-@pytest.mark.parametrize("name,groups", [("prefill_b4_t4096", [0, 9]),
-                                         ("train_b2_t8192_h64", [3]),
-                                         ("varlen_8seq_32k", [5]),
-                                         ("longseq_b1_t32k_h8", [2])])
-def test_fwd_full_size_sampled(name, groups):
+FULL_FWD = [("prefill_b4_t4096", [0, 9]), ("train_b2_t8192_h64", [3]), ("varlen_8seq_32k", [5]),
+            ("longseq_b1_t32k_h8", [2])]
+FULL_BWD = [("train_b2_t8192_h64", [7]), ("varlen_8seq_32k", [11]), ("longseq_b1_t32k_h8", [1])]
+
+
+@pytest.mark.parametrize("out_f32", [False, True])
+@pytest.mark.parametrize("name,groups", FULL_FWD)
+def test_fwd_full_size_sampled(name, groups, out_f32):
     x = make_inputs(workload(name))
-    run_fwd_case(x, groups=groups, check_aux=(name != "train_b2_t8192_h64"))
+    run_fwd_case(x, groups=groups, check_aux=(name != "train_b2_t8192_h64"), out_f32=out_f32)
 
 
-@pytest.mark.parametrize("name,groups", [("train_b2_t8192_h64", [7]),
-                                         ("varlen_8seq_32k", [11]),
-                                         ("longseq_b1_t32k_h8", [1])])
-def test_bwd_full_size_sampled(name, groups):
+@pytest.mark.parametrize("out_f32", [False, True])
+@pytest.mark.parametrize("name,groups", FULL_BWD)
+def test_bwd_full_size_sampled(name, groups, out_f32):
     x = make_inputs(workload(name))
-    run_bwd_case(x, groups=groups)
+    run_bwd_case(x, groups=groups, out_f32=out_f32)
 
 
-def test_training_step_full_size_sampled():
-    """The benchmark's training step (save-for-backward pair) at full size: sampled head group vs the
-    oracle, all gradients bit-equal to the recomputing backward."""
+def test_tiny_fp32_full_config():
+    """The tiny fp32 configuration (B=1, T=256, H=2, K=V=64) forward and backward at 1e-5 * RMS."""
+    x = make_inputs(workload("tiny_fp32"))
+    run_fwd_case(x)
+    run_bwd_case(x)
+
+
+@pytest.mark.parametrize("out_f32", [False, True])
+def test_training_step_full_size_sampled(out_f32):
+    """The benchmark's training step (save-for-backward pair) at full size: all gradients bit-equal to
+    the recomputing backward; sampled head group vs the oracle."""
     x = make_inputs(workload("train_b2_t8192_h64"))
-    run_bwd_case(x, groups=[12], saved=True)
+    run_bwd_case(x, groups=[12], saved=True, out_f32=out_f32)

@@ -1,13 +1,9 @@
 """The save-for-backward pair (chunk_gated_delta_rule_fwd_saved / _bwd_saved, C entry gdn_bwd_saved)
 against the fp64 oracle and against the recomputing backward."""
-import numpy as np
 import pytest
 import torch
 
-import gated_delta_rule_50_gb300 as gdn
-import oracle
-from gpu_cases import recovered_gate, to_dev
-from parity import check
+from gpu_cases import run_bwd_case
 from synth import make_inputs, workload
 
 pytestmark = pytest.mark.gpu
@@ -46,30 +42,9 @@ CASES = {
 }
 
 
+@pytest.mark.parametrize("out_f32", [False, True])
 @pytest.mark.parametrize("name", list(CASES))
-def test_bwd_saved_matches_oracle_and_recompute(name):
-    x = CASES[name]()
-    d = to_dev(x)
-    g_cum, A, o, ht, saved = gdn.chunk_gated_delta_rule_fwd_saved(
-        d["q"], d["k"], d["v"], d["g"], d["beta"], scale=x["scale"], initial_state=d["h0"],
-        cu_seqlens=d["cu_seqlens"])
-    got = gdn.chunk_gated_delta_rule_bwd_saved(
-        d["q"], d["k"], d["v"], g_cum, d["beta"], A, d["do"], saved, dht=d["dht"], scale=x["scale"],
-        initial_state=d["h0"], cu_seqlens=d["cu_seqlens"])
-    ref = gdn.chunk_gated_delta_rule_bwd(
-        d["q"], d["k"], d["v"], g_cum, d["beta"], A, d["do"], dht=d["dht"], scale=x["scale"],
-        initial_state=d["h0"], cu_seqlens=d["cu_seqlens"])
-    torch.cuda.synchronize()
-    # the same chain kernel produced h in both: the saved backward equals the recomputing one
-    for a, b in zip(got, ref):
-        if a is not None:
-            assert torch.equal(a, b)
-    io = x["q"].dtype
-    xs = dict(x, g=torch.from_numpy(recovered_gate(g_cum, x["cu_seqlens"])))
-    r = oracle.oracle_bwd(xs["q"], xs["k"], xs["v"], xs["g"], xs["beta"], xs["do"], x["scale"], xs["h0"],
-                          xs["dht"], cu_seqlens=x["cu_seqlens"])
-    names = ["dq", "dk", "dv", "dbeta", "dg", "dh0"]
-    stored = [io, io, io, torch.float32, torch.float32, torch.float32]
-    for i in range(6):
-        if got[i] is not None:
-            check(names[i], got[i], r[i], io, stored[i])
+def test_bwd_saved_matches_oracle_and_recompute(name, out_f32):
+    """The saved pair equals the recomputing backward bit for bit (both from the CUDA forward's g_cum);
+    the recomputing backward, given a host-computed g_cum, matches the oracle."""
+    run_bwd_case(CASES[name](), saved=True, out_f32=out_f32)

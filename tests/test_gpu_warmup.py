@@ -14,13 +14,14 @@ from synth import make_inputs, workload
 pytestmark = pytest.mark.gpu
 
 
-def run(x, warm, groups=None):
+def run(x, warm, groups=None, out_f32=False):
     d = to_dev(x)
     plan = gdn.cp_plan(d["q"], d["v"], cu_seqlens=d["cu_seqlens"], cp_mode="warmup", warmup_chunks=warm)
     assert plan is not None
     _, _, o, _, ht = gdn.chunk_gated_delta_rule_fwd(
         d["q"], d["k"], d["v"], d["g"], d["beta"], scale=x["scale"], initial_state=d["h0"],
-        cu_seqlens=d["cu_seqlens"], output_final_state=True, cp_mode="warmup", warmup_chunks=warm)
+        cu_seqlens=d["cu_seqlens"], output_final_state=True, cp_mode="warmup", warmup_chunks=warm,
+        out_f32=out_f32)
     torch.cuda.synchronize()
     xs, hv = (x, None) if groups is None else select_groups(x, groups, x["v"].shape[2] // x["q"].shape[2], None)
     o_ref, ht_ref = oracle.oracle_fwd_warmup(xs["q"], xs["k"], xs["v"], xs["g"], xs["beta"], x["scale"], xs["h0"],
@@ -79,35 +80,37 @@ def test_warmup_varlen():
     check("final_state", ht, ht_ref, torch.bfloat16, torch.float32)
 
 
-def test_warmup_full_size_sampled():
+@pytest.mark.parametrize("out_f32", [False, True])
+def test_warmup_full_size_sampled(out_f32):
     x = make_inputs(workload("longseq_b1_t32k_h8"))
-    _, o, ht, o_ref, ht_ref, _ = run(x, warm=8, groups=[1])
-    check("o", o, o_ref, torch.bfloat16, torch.bfloat16)
+    _, o, ht, o_ref, ht_ref, _ = run(x, warm=8, groups=[1], out_f32=out_f32)
+    check("o", o, o_ref, torch.bfloat16, torch.float32 if out_f32 else torch.bfloat16)
     check("final_state", ht, ht_ref, torch.bfloat16, torch.float32)
 
 
 # ------------------------------------------------------------------ exact split (default mode)
-def run_exact(x):
+def run_exact(x, out_f32=False):
     d = to_dev(x)
     plan = gdn.cp_plan(d["q"], d["v"], cu_seqlens=d["cu_seqlens"], cp_mode="auto")
     assert plan is not None
     _, _, o, _, ht = gdn.chunk_gated_delta_rule_fwd(
         d["q"], d["k"], d["v"], d["g"], d["beta"], scale=x["scale"], initial_state=d["h0"],
-        cu_seqlens=d["cu_seqlens"], output_final_state=True, cp_mode="auto")
+        cu_seqlens=d["cu_seqlens"], output_final_state=True, cp_mode="auto", out_f32=out_f32)
     torch.cuda.synchronize()
     o_ref, ht_ref = oracle.oracle_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["scale"], x["h0"],
                                       cu_seqlens=x["cu_seqlens"])
     return plan, o, ht, o_ref, ht_ref
 
 
-def test_exact_split_matches_unsplit_with_non_decaying_heads():
+@pytest.mark.parametrize("out_f32", [False, True])
+def test_exact_split_matches_unsplit_with_non_decaying_heads(out_f32):
     """Default mode on a shape the trigger splits: exact even for g = 0 heads, where warmup is invalid."""
     x = make_inputs(workload("longseq_b1_t32k_h8").scaled(T=8192 + 100, Hq=2, Hv=4, seed=43))
     x["g"][..., 1] = 0.0
     x["g"][..., 2] *= 0.02
-    plan, o, ht, o_ref, ht_ref = run_exact(x)
+    plan, o, ht, o_ref, ht_ref = run_exact(x, out_f32=out_f32)
     assert plan == (11, 12)
-    check("o", o, o_ref, torch.bfloat16, torch.bfloat16)
+    check("o", o, o_ref, torch.bfloat16, torch.float32 if out_f32 else torch.bfloat16)
     check("final_state", ht, ht_ref, torch.bfloat16, torch.float32)
 
 
@@ -121,11 +124,12 @@ def test_exact_split_varlen_no_h0():
     check("final_state", ht, ht_ref, torch.bfloat16, torch.float32)
 
 
-def test_exact_split_backward():
+@pytest.mark.parametrize("out_f32", [False, True])
+def test_exact_split_backward(out_f32):
     """Both backward chains split through segment transitions (default mode, trigger on)."""
     from gpu_cases import run_bwd_case
     x = make_inputs(workload("longseq_b1_t32k_h8").scaled(T=4096 + 100, Hq=2, Hv=4, seed=45))
     x["g"][..., 1] = 0.0
     d = to_dev(x)
     assert gdn.cp_plan(d["q"], d["v"], cp_mode="auto") == (8, 9)
-    run_bwd_case(x)
+    run_bwd_case(x, out_f32=out_f32)
