@@ -141,7 +141,8 @@ k_tc_dscan(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
     auto chunk_tok0 = [&](int t) { return sr.tok0 + (nck - 1 - t) * C; };
 
     if (threadIdx.x == 0) {
-        const uint32_t counts[B_COUNT] = {1, 1, 1, 1, 1, 128, 256, 1, 256, 1, 256, 1, 1};
+        // GQREADY: the 4 aux warps; DSREADY, DDREADY, YREADY: the 8 state warps (one arrival per warp)
+        const uint32_t counts[B_COUNT] = {1, 1, 1, 1, 1, 4, 8, 1, 8, 1, 8, 1, 1};
         for (int i = 0; i < B_COUNT; ++i) mbar_init(bar(i), counts[i]);
         misc[1] = 0;
         fence_mbar_init();
@@ -323,7 +324,7 @@ k_tc_dscan(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
                 }
             }
             fence_proxy_async_smem();
-            mbar_arrive(bar(B_GQREADY));
+            mbar_arrive_warp(bar(B_GQREADY));
             if (t + 1 < nck) load_q(t + 1);
         }
         if (pt == 0 && ap_issued > 0) mbar_drain(bar(B_APREADY), (ap_issued - 1) & 1);  // no copy left in flight
@@ -352,12 +353,10 @@ k_tc_dscan(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
             for (int hf = 0; hf < 2; ++hf) {  // in halves: dS (64 registers) stays live throughout
                 uint32_t hi[16], lo[16];
                 split_pack16(S + 32 * hf, hi, lo);
-                tmem_st16(trow + TM_SH + 32 * hh + 16 * hf, hi);
-                tmem_st16(trow + TM_SL + 32 * hh + 16 * hf, lo);
+                tmem_st16x2(trow + TM_SH + 32 * hh + 16 * hf, hi, trow + TM_SL + 32 * hh + 16 * hf, lo);
             }
-            tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(bar(B_DSREADY));
+            mbar_arrive_warp(bar(B_DSREADY));
             // gate values of this warp's chunk row c = 32 hh + lane (loaded before the dSe stores below)
             const int cg = 32 * hh + lane;
             const float glast = a.g_cum[(size_t)(tok0 + n - 1) * p.Hv + hv];
@@ -386,9 +385,7 @@ k_tc_dscan(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
 #pragma unroll
             for (int hf = 0; hf < 2; ++hf) {
                 uint32_t kd16[16], pd16[16];
-                tmem_ld16(trow + TM_KD + 32 * hh + 16 * hf, kd16);
-                tmem_ld16(trow + TM_PD + 32 * hh + 16 * hf, pd16);
-                tmem_wait_ld();
+                tmem_ld16x2(trow + TM_KD + 32 * hh + 16 * hf, kd16, trow + TM_PD + 32 * hh + 16 * hf, pd16);
 #pragma unroll
                 for (int q2 = 0; q2 < 2; ++q2) {
                     float x[8];
@@ -403,7 +400,7 @@ k_tc_dscan(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
             uint32_t kd[32];
             tc_fence_before();
             fence_proxy_async_smem();
-            mbar_arrive(bar(B_DDREADY));
+            mbar_arrive_warp(bar(B_DDREADY));
             if (dSe_out) {  // while dR is computed: dS at this chunk's end -> workspace
                 float *dst = dSe_out + ((size_t)gc * p.Hv + hv) * DK * DV + (size_t)(64 * hh) * DV + v;
 #pragma unroll
@@ -413,7 +410,6 @@ k_tc_dscan(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
             if (!(ok = wwait(B_DRDONE, t & 1, t))) break;
             tc_fence_after();
             tmem_ld32(trow + TM_DR + 32 * hh, kd);
-            tmem_wait_ld();
 #pragma unroll
             for (int q4 = 0; q4 < 4; ++q4) {
                 float x[8];
@@ -423,16 +419,14 @@ k_tc_dscan(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
             }
             tc_fence_before();
             fence_proxy_async_smem();
-            mbar_arrive(bar(B_YREADY));
+            mbar_arrive_warp(bar(B_YREADY));
             // (g) dS^T <- Gam_last dS^T + U
             if (!(ok = wwait(B_UDONE, t & 1, t))) break;
             tc_fence_after();
             tmem_ld32(trow + TM_U + 64 * hh, kd);
-            tmem_wait_ld();
 #pragma unroll
             for (int i = 0; i < 32; ++i) S[i] = fmaf(gl_all, S[i], __uint_as_float(kd[i]));
             tmem_ld32(trow + TM_U + 64 * hh + 32, kd);
-            tmem_wait_ld();
 #pragma unroll
             for (int i = 0; i < 32; ++i) S[32 + i] = fmaf(gl_all, S[32 + i], __uint_as_float(kd[i]));
             tc_fence_before();

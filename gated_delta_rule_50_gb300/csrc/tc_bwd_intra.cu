@@ -81,7 +81,7 @@ struct IntraArgs {
     const unsigned char *tiles;  // [chunks][Hv] x 32 KB: A hi / lo, P hi / lo operand images
     const float *vecs;           // [chunks][Hv] x {gam, Gam, E, beta} x 64
     const float *hbuf, *dSe;
-    void *dq, *dk, *dv;  // bf16, or fp32 when p.out_f32
+    void *dq, *dk, *dv;  // bf16, or fp32 in the checking mode (p.out_f32)
     float *dbeta, *dg;
 };
 
@@ -183,6 +183,7 @@ __device__ __forceinline__ void key_rows(const float *__restrict__ src, uint32_t
     }
 }
 
+template <bool F32OUT>
 __global__ void __launch_bounds__(NT, 1)
 k_tc_bwd_intra(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
                const __grid_constant__ CUtensorMap tm_do, const __grid_constant__ CUtensorMap tm_v,
@@ -304,9 +305,7 @@ k_tc_bwd_intra(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
             state_col(sm + S_DR + 16384u * (uint32_t)lq, xh);
             uint32_t hi[16], lo[16];
             split_pack16(xh, hi, lo);
-            tmem_st16(tmem + trow + C_HT + 16 * hh, hi);
-            tmem_st16(tmem + trow + C_HT + 64 + 16 * hh, lo);
-            tmem_wait_st();
+            tmem_st16x2(tmem + trow + C_HT + 16 * hh, hi, tmem + trow + C_HT + 64 + 16 * hh, lo);
         }
         __syncthreads();  // vectors visible
         pre_mma();
@@ -333,9 +332,7 @@ k_tc_bwd_intra(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         float Xr[16], KSr[16];  // (V - Gam KS) and KS at chunk rows c = 16 hh + i, value lrow
         {
             uint32_t ks[16], qs[16];
-            tmem_ld16(tmem + trow + C_KS + 16 * hh, ks);
-            tmem_ld16(tmem + trow + C_QS + 16 * hh, qs);
-            tmem_wait_ld();
+            tmem_ld16x2(tmem + trow + C_KS + 16 * hh, ks, tmem + trow + C_QS + 16 * hh, qs);
             float part[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
@@ -370,9 +367,7 @@ k_tc_bwd_intra(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
             state_col(sm + box, xd);
             uint32_t hi[16], lo[16];
             split_pack16(xd, hi, lo);
-            tmem_st16(tmem + trow + C_HT + 16 * hh, hi);
-            tmem_st16(tmem + trow + C_HT + 64 + 16 * hh, lo);
-            tmem_wait_st();
+            tmem_st16x2(tmem + trow + C_HT + 16 * hh, hi, tmem + trow + C_HT + 64 + 16 * hh, lo);
         }
         pre_mma();
         if (t == 0) {
@@ -393,10 +388,8 @@ k_tc_bwd_intra(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         // ---------------------------------------------------------------- P3: dDl^T and Dl^T tiles; F
         {
             uint32_t dl[16], kd[16], pd[16];
-            tmem_ld16(tmem + trow + C_DL + 16 * hh, dl);
-            tmem_ld16(tmem + trow + C_KS + 16 * hh, kd);
+            tmem_ld16x2(tmem + trow + C_DL + 16 * hh, dl, tmem + trow + C_KS + 16 * hh, kd);
             tmem_ld16(tmem + trow + C_QS + 16 * hh, pd);
-            tmem_wait_ld();
             float part[16];
 #pragma unroll
             for (int q2 = 0; q2 < 2; ++q2) {
@@ -439,7 +432,6 @@ k_tc_bwd_intra(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         {
             uint32_t dr[16];
             tmem_ld16(tmem + trow + C_DR + 16 * hh, dr);
-            tmem_wait_ld();
             float pb[16], pg[16];
             __nv_bfloat16 *dvs = reinterpret_cast<__nv_bfloat16 *>(sm + S_DD);  // dv staging [r][128]
 #pragma unroll
@@ -450,7 +442,7 @@ k_tc_bwd_intra(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
                     const int i = 8 * q2 + e, c = 16 * hh + i;
                     const float drv = __uint_as_float(dr[i]);
                     s8[e] = p.scale * Gm[c] * tile128_at(sm, S_DO, c, lrow);  // scale Gam dO (Gm = 0 past n)
-                    if (!p.out_f32)
+                    if (!F32OUT)
                         dvs[c * DV + lrow] = __float2bfloat16_rn(bet[c] * drv);
                     else if (c < n)  // checking mode: fp32 dv straight out (one 128-byte row segment per warp)
                         static_cast<float *>(a.dv)[(size_t)(tok0 + c) * p.Hv * DV + (size_t)hv * DV + lrow] =
@@ -473,7 +465,6 @@ k_tc_bwd_intra(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         {  // dP (lanes 0..63) and dA (lanes 64..127) -> fp32 staging Fb[r][i] = dP[r][i], Fa[r][i] = dA[r][i]
             uint32_t dd[16];
             tmem_ld16(tmem + trow + (lq < 2 ? C_KS : C_QS) + 16 * hh, dd);
-            tmem_wait_ld();
             float *dst = lq < 2 ? Fb : Fa;
             const int i = lrow & 63;
 #pragma unroll
@@ -541,7 +532,7 @@ k_tc_bwd_intra(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
             mma_chain<4, 2, 2>(tmem + C_KS, kdesc(sb + S_A + 8192), kdesc(sb + S_P), ID_KK, 1);
         }
         // while Z runs: dv out, then (E Dl)^T into the staging region
-        if (!p.out_f32) {  // dv out: 64 rows x 256 bytes from the staging tile, 16-byte stores
+        if (!F32OUT) {  // dv out: 64 rows x 256 bytes from the staging tile, 16-byte stores
             const uint4 *src = reinterpret_cast<const uint4 *>(sm + S_DD);
             for (int o = t; o < 64 * 16; o += NT) {
                 const int r = o >> 4, c16 = o & 15;
@@ -554,7 +545,6 @@ k_tc_bwd_intra(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         {  // (E Dl)^T -> value-major hi / lo tile [v][i] in the dDl region (the dv staging has been written out)
             uint32_t dl[16];
             tmem_ld16(tmem + trow + C_DL + 16 * hh, dl);
-            tmem_wait_ld();
 #pragma unroll
             for (int q2 = 0; q2 < 2; ++q2) {
                 float e8[8];
@@ -568,7 +558,6 @@ k_tc_bwd_intra(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         if (lq < 2) {  // Z^T rows (lanes 0..63) -> hi / lo bf16 A operand in TMEM
             uint32_t z[16], hi[8], lo[8];
             tmem_ld16(tmem + trow + C_KS + 16 * hh, z);
-            tmem_wait_ld();
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 float h0, l0, h1, l1;
@@ -577,9 +566,7 @@ k_tc_bwd_intra(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
                 hi[i] = pack_bf16(h0, h1);
                 lo[i] = pack_bf16(l0, l1);
             }
-            tmem_st8(tmem + trow + C_QS + 8 * hh, hi);
-            tmem_st8(tmem + trow + C_QS + 32 + 8 * hh, lo);
-            tmem_wait_st();
+            tmem_st8x2(tmem + trow + C_QS + 8 * hh, hi, tmem + trow + C_QS + 32 + 8 * hh, lo);
         }
         pre_mma();
         if (t == 0) {  // (A^T Z)^T[i][r] = sum_k Z^T[i][k] A[k][r]   (A read MN-major)
@@ -592,7 +579,6 @@ k_tc_bwd_intra(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         if (lq < 2) {  // Fa[r][i] = dL[r][i] = -(A^T Z)[r][i]
             uint32_t z[16];
             tmem_ld16(tmem + trow + C_KS + 16 * hh, z);
-            tmem_wait_ld();
             const int i = lrow;
 #pragma unroll
             for (int j = 0; j < 16; ++j) Fa[(16 * hh + j) * 65 + i] = -__uint_as_float(z[j]);
@@ -609,7 +595,6 @@ k_tc_bwd_intra(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         if (lq < 2) {  // K K^T (lanes 0..63: row r = lrow, column i = 16 hh + j) -> fp32 staging Fb[r][i]
             uint32_t kk[16];
             tmem_ld16(tmem + trow + C_KS + 16 * hh, kk);
-            tmem_wait_ld();
 #pragma unroll
             for (int j = 0; j < 16; ++j) Fb[lrow * 65 + 16 * hh + j] = __uint_as_float(kk[j]);
         }
@@ -671,15 +656,11 @@ k_tc_bwd_intra(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
                 uint32_t hi[16], lo[16];
                 key_rows(a.hbuf + st_off + (size_t)(32 * lq) * DV + 32 * hh, tb, x);
                 split_pack16(x, hi, lo);
-                tmem_st16(tmem + trow + C_HT + 16 * hh, hi);
-                tmem_st16(tmem + trow + C_HT + 64 + 16 * hh, lo);
+                tmem_st16x2(tmem + trow + C_HT + 16 * hh, hi, tmem + trow + C_HT + 64 + 16 * hh, lo);
                 key_rows(a.dSe + st_off + (size_t)(32 * lq) * DV + 32 * hh, tb, x);
                 {  // <h, dSe> partial: h read back from its hi / lo TMEM pair (about 16 significant bits)
                     uint32_t h2[16], l2[16];
-                    tmem_wait_st();
-                    tmem_ld16(tmem + trow + C_HT + 16 * hh, h2);
-                    tmem_ld16(tmem + trow + C_HT + 64 + 16 * hh, l2);
-                    tmem_wait_ld();
+                    tmem_ld16x2(tmem + trow + C_HT + 16 * hh, h2, tmem + trow + C_HT + 64 + 16 * hh, l2);
                     float hd = 0.f;
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
@@ -691,10 +672,8 @@ k_tc_bwd_intra(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
                     if (lane == 0) sH[warp] = hd;
                 }
                 split_pack16(x, hi, lo);
-                tmem_st16(tmem + trow + C_KS + 16 * hh, hi);
-                tmem_st16(tmem + trow + C_KS + 64 + 16 * hh, lo);
+                tmem_st16x2(tmem + trow + C_KS + 16 * hh, hi, tmem + trow + C_KS + 64 + 16 * hh, lo);
             }
-            tmem_wait_st();
         }
         __syncthreads();
         // ---------------------------------------------------------------- P6: dq^T, dk^T accumulation
@@ -746,17 +725,15 @@ k_tc_bwd_intra(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         mma_sync();
     }
     // ---------------------------------------------------------------- dq, dk out (thread: key lrow, rows 16 hh + j)
-    if (ok && p.out_f32) {  // checking mode: fp32 dq, dk
+    if (ok && F32OUT) {  // checking mode: fp32 dq, dk
         uint32_t d[16];
         const size_t rs = (size_t)p.Hq * DK, o0 = (size_t)tok0 * rs + (size_t)hq * DK + lrow;
         float *dqp = static_cast<float *>(a.dq) + o0, *dkp = static_cast<float *>(a.dk) + o0;
         tmem_ld16(tmem + trow + C_DQ + 16 * hh, d);
-        tmem_wait_ld();
 #pragma unroll
         for (int j = 0; j < 16; ++j)
             if (16 * hh + j < n) dqp[(size_t)(16 * hh + j) * rs] = __uint_as_float(d[j]);
         tmem_ld16(tmem + trow + C_DK + 16 * hh, d);
-        tmem_wait_ld();
 #pragma unroll
         for (int j = 0; j < 16; ++j)
             if (16 * hh + j < n) dkp[(size_t)(16 * hh + j) * rs] = __uint_as_float(d[j]);
@@ -766,7 +743,6 @@ k_tc_bwd_intra(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         uint16_t *dkp = reinterpret_cast<uint16_t *>(a.dk) + (size_t)hq * DK + lrow;
         const size_t rs = (size_t)p.Hq * DK;
         tmem_ld16(tmem + trow + C_DQ + 16 * hh, d);
-        tmem_wait_ld();
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
             const int r = 16 * hh + j;
@@ -776,7 +752,6 @@ k_tc_bwd_intra(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
             }
         }
         tmem_ld16(tmem + trow + C_DK + 16 * hh, d);
-        tmem_wait_ld();
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
             const int r = 16 * hh + j;
@@ -817,8 +792,8 @@ cudaError_t launch_tc_bwd_intra(const Plan &p, const void *q, const void *k, con
     CUtensorMap th, tdse;
     const size_t units = (size_t)p.total_chunks * p.Hv;
     if (!make_state_map(&th, hbuf, units) || !make_state_map(&tdse, dSe, units)) return cudaErrorInvalidValue;
-    cudaError_t e =
-        cudaFuncSetAttribute(k_tc_bwd_intra, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+    auto kern = p.out_f32 ? k_tc_bwd_intra<true> : k_tc_bwd_intra<false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
     if (e != cudaSuccess) return e;
     IntraArgs a;
     a.tiles = tiles;
@@ -831,7 +806,7 @@ cudaError_t launch_tc_bwd_intra(const Plan &p, const void *q, const void *k, con
     a.dbeta = dbeta;
     a.dg = dg;
     dim3 grid(p.total_chunks, p.Hq);
-    k_tc_bwd_intra<<<grid, NT, SMEM_BYTES, st>>>(tk, tq, tdo, tv, th, tdse, p, a);
+    kern<<<grid, NT, SMEM_BYTES, st>>>(tk, tq, tdo, tv, th, tdse, p, a);
     return cudaGetLastError();
 }
 

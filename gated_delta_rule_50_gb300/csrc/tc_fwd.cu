@@ -47,6 +47,7 @@ constexpr int DK = 128, DV = 128;
 constexpr int NUM_THREADS = 576;
 constexpr int W_TMA = 0, W_MMA = 1, W_STATE0 = 2;
 constexpr uint32_t NSTATE = NUM_THREADS - 64;  // state threads: 16 warps, four per TMEM lane quarter
+constexpr uint32_t NSW = NSTATE / 32;            // state warps (one barrier arrival each)
 
 // shared memory map (bytes from a 1024-aligned base)
 constexpr uint32_t SM_KQ = 0;             // 2 stages x {[kb0: K 8K, Q 8K][kb1: K 8K, Q 8K], A hi / lo, P hi / lo}
@@ -79,7 +80,7 @@ struct FwdArgs {
     const unsigned char *tiles;  // [chunks][Hv] x 32 KB operand images from the prep kernel
     const float *vecs;           // [chunks][Hv] x {gam, Gam, E, beta} x 64
     const float *h0;
-    void *o;  // bf16, or fp32 when p.out_f32
+    void *o;  // bf16, or fp32 in the checking mode (p.out_f32)
     float *h, *ht;
     // sequence splitting (see cp.cu and launch.h): seg_len > 0 enables it
     int seg_len, n_seg, warm, mode;  // mode: CP_WARM, CP_MAIN or CP_SEG
@@ -99,6 +100,7 @@ __device__ void record_timeout(const Plan &p, int bar_id, int chunk) {
     atomicOr(p.err, ERR_TIMEOUT);
 }
 
+template <bool F32OUT>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 k_tc_fwd(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
          const __grid_constant__ CUtensorMap tm_v, Plan p, FwdArgs a) {
@@ -167,8 +169,7 @@ k_tc_fwd(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
     float *h_out = outs ? a.h : nullptr;
 
     if (threadIdx.x == 0) {
-        const uint32_t counts[B_COUNT] = {1,      1, 1, 1,      NSTATE, 1, NSTATE, 1,      NSTATE, 1,
-                                          1,      NSTATE, NSTATE, 1, 1,      1, NSTATE, NSTATE};
+        const uint32_t counts[B_COUNT] = {1, 1, 1, 1, NSW, 1, NSW, 1, NSW, 1, 1, NSW, NSW, 1, 1, 1, NSW, NSW};
         for (int i = 0; i < B_COUNT; ++i) mbar_init(bar(i), counts[i]);
         misc[1] = 0;
         fence_mbar_init();
@@ -309,8 +310,8 @@ k_tc_fwd(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
             const int tok0 = sr.tok0 + jj * C, n = min(C, sr.tok1 - tok0), b = jj & 1;
             const float *Gm = vecs(jj) + 64;
             if (!o_out) {  // nothing to write: release QS / O and the v buffer (this thread is past R of jj)
-                mbar_arrive(bar(B_EPIFREE0 + b));
-                mbar_arrive(bar(B_VEMPTY0 + b));
+                mbar_arrive_warp(bar(B_EPIFREE0 + b));
+                mbar_arrive_warp(bar(B_VEMPTY0 + b));
                 return true;
             }
             if (!wwait(B_ODONE, jj & 1, jj)) return false;
@@ -320,12 +321,10 @@ k_tc_fwd(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
             float gm[16];  // loaded before any store (generic pointers: no reordering across stores)
 #pragma unroll
             for (int i = 0; i < 16; ++i) gm[i] = Gm[16 * hh + i];
-            tmem_ld16(trow + TM_QS + 64 * b + 16 * hh, qs);
-            tmem_ld16(trow + TM_O + 16 * hh, oo);
-            tmem_wait_ld();
+            tmem_ld16x2(trow + TM_QS + 64 * b + 16 * hh, qs, trow + TM_O + 16 * hh, oo);
             tc_fence_before();
-            mbar_arrive(bar(B_EPIFREE0 + b));
-            if (p.out_f32) {  // checking mode: the fp32 value, one 128-byte row segment per warp and row
+            mbar_arrive_warp(bar(B_EPIFREE0 + b));
+            if (F32OUT) {  // checking mode: the fp32 value, one 128-byte row segment per warp and row
                 float *of = static_cast<float *>(o_out) + (size_t)tok0 * p.Hv * DV + (size_t)hv * DV + v;
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
@@ -334,7 +333,7 @@ k_tc_fwd(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
                         of[(size_t)c * p.Hv * DV] =
                             p.scale * fmaf(gm[i], __uint_as_float(qs[i]), __uint_as_float(oo[i]));
                 }
-                mbar_arrive(bar(B_VEMPTY0 + b));
+                mbar_arrive_warp(bar(B_VEMPTY0 + b));
                 return true;
             }
 #pragma unroll
@@ -352,7 +351,9 @@ k_tc_fwd(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
                                                ((size_t)(tok0 + c) * p.Hv + hv) * DV + 32 * (warp & 3) +
                                                8 * (lane & 3)) = w;
             }
-            mbar_arrive(bar(B_VEMPTY0 + b));
+            // the staging writes (generic proxy) are ordered before the next TMA write of this buffer
+            fence_proxy_async_smem();
+            mbar_arrive_warp(bar(B_VEMPTY0 + b));
             return true;
         };
 
@@ -363,12 +364,10 @@ k_tc_fwd(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
             {
                 uint32_t shi[16], slo[16];
                 split_pack16(S, shi, slo);
-                tmem_st16(trow + TM_SH + 16 * hh, shi);
-                tmem_st16(trow + TM_SL + 16 * hh, slo);
-                tmem_wait_st();
+                tmem_st16x2(trow + TM_SH + 16 * hh, shi, trow + TM_SL + 16 * hh, slo);
             }
             tc_fence_before();
-            mbar_arrive(bar(B_SSREADY));
+            mbar_arrive_warp(bar(B_SSREADY));
             if (h_out) {  // while KS is computed: the chunk-entry state (backward recompute)
                 const size_t hb = ((size_t)(sr.c0 + j) * p.Hv + hv) * DK * DV;
 #pragma unroll
@@ -381,7 +380,6 @@ k_tc_fwd(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
             const float *vj = vecs(j), *Gm = vj + 64, *Ev = vj + 128, *bet = vj + 192;
             uint32_t raw[32];
             tmem_ld16(trow + TM_KS + 16 * hh, *reinterpret_cast<uint32_t(*)[16]>(raw));
-            tmem_wait_ld();
             // v at (row c, column v) of the swizzled tile (two 64-column boxes); rows past the chunk end
             // are finite (next tokens or zero fill) and meet beta = 0
             const unsigned char *vt = sm + SM_V + (j & 1) * V_STAGE + (v >> 6) * 8192;
@@ -399,14 +397,13 @@ k_tc_fwd(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
             for (int q = 0; q < 2; ++q) st_split_chunk(sb + SM_RT, sb + SM_RT + 16384, v, 2 * hh + q, R + 8 * q);
             tc_fence_before();
             fence_proxy_async_smem();
-            mbar_arrive(bar(B_RTREADY));
+            mbar_arrive_warp(bar(B_RTREADY));
             // while Dl is computed: o of chunk j - 1
             if (j >= 1 && !(ok = epilogue(j - 1))) break;
             // (e) Dl^T -> Dl^T tile (R region) and (E Dl)^T hi / lo pairs in TMEM
             if (!(ok = wwait(B_DLDONE, j & 1, j))) break;
             tc_fence_after();
             tmem_ld16(trow + TM_DL + 16 * hh, *reinterpret_cast<uint32_t(*)[16]>(raw));
-            tmem_wait_ld();
             {
                 float ED[16], Dl[16];
 #pragma unroll
@@ -425,19 +422,16 @@ k_tc_fwd(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
                     ehi[i] = pack_bf16(h0, h1);
                     elo[i] = pack_bf16(l0, l1);
                 }
-                tmem_st8(trow + TM_EDH + 8 * hh, ehi);
-                tmem_st8(trow + TM_EDL + 8 * hh, elo);
-                tmem_wait_st();
+                tmem_st8x2(trow + TM_EDH + 8 * hh, ehi, trow + TM_EDL + 8 * hh, elo);
             }
             tc_fence_before();
             fence_proxy_async_smem();
-            mbar_arrive(bar(B_EDREADY));
+            mbar_arrive_warp(bar(B_EDREADY));
             // (g) S^T <- Gam_last S^T + U^T
             if (!(ok = wwait(B_UPDDONE, j & 1, j))) break;
             tc_fence_after();
             const float gl = Gm[n - 1];
             tmem_ld32(trow + TM_U + 32 * hh, raw);
-            tmem_wait_ld();
 #pragma unroll
             for (int i = 0; i < 32; ++i) S[i] = fmaf(gl, S[i], __uint_as_float(raw[i]));
             tc_fence_before();
@@ -505,7 +499,8 @@ cudaError_t launch_tc_fwd(const Plan &p, const void *q, const void *k, const voi
     CUtensorMap tk, tq, tv;
     if (!make_head_map(&tk, k, p.Hq, p) || !make_head_map(&tq, q, p.Hq, p) || !make_head_map(&tv, v, p.Hv, p))
         return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(k_tc_fwd, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+    auto kern = p.out_f32 ? k_tc_fwd<true> : k_tc_fwd<false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
     if (e != cudaSuccess) return e;
     FwdArgs a;
     a.tiles = tiles;
@@ -532,7 +527,7 @@ cudaError_t launch_tc_fwd(const Plan &p, const void *q, const void *k, const voi
         a.seg_M = cp->seg_M;
     }
     dim3 grid(p.n_seqs * a.n_seg * (a.mode == CP_SEG ? 2 : 1), p.Hv);
-    k_tc_fwd<<<grid, NUM_THREADS, SMEM_BYTES, st>>>(tk, tq, tv, p, a);
+    kern<<<grid, NUM_THREADS, SMEM_BYTES, st>>>(tk, tq, tv, p, a);
     return cudaGetLastError();
 }
 

@@ -238,7 +238,6 @@ k_tc_prep(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
             uint32_t r0[32], r1[32];
             tmem_ld32(tmem + ((uint32_t)(32 * warp) << 16), r0);
             tmem_ld32(tmem + ((uint32_t)(32 * warp) << 16) + 32, r1);
-            tmem_wait_ld();
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
                 raw[i] = r0[i];
