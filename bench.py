@@ -279,6 +279,7 @@ def run_ours(args, rank, world, local_rank):
         evs[i][1].record(stream)
         bwd(f)
         evs[i][2].record(stream)
+        f = None                        # a training step frees its saved tensors before the next forward
     torch.cuda.synchronize()
     wall = time.perf_counter() - t0
     lib.gdn_profile_enable(0)
