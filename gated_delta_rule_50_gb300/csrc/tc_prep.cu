@@ -150,7 +150,7 @@ __device__ __forceinline__ void put_split_chunk(unsigned char *hi_tile, unsigned
         make_uint4(pack_bf16(l[0], l[1]), pack_bf16(l[2], l[3]), pack_bf16(l[4], l[5]), pack_bf16(l[6], l[7]));
 }
 
-__global__ void __launch_bounds__(NT, 5)
+__global__ void __launch_bounds__(NT, 6)
 k_tc_prep(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q, Plan p, PrepArgs a) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char *sm = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -233,39 +233,38 @@ k_tc_prep(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
             Ev[t] = t < n ? __expf(glast - gam[t]) : 0.f;
         }
         unsigned char *img = a.tiles + unit * 32768;
-        uint32_t raw[64];  // this thread's row of K K^T (t < 64) or Q K^T (t >= 64), read from TMEM
-        {
-            uint32_t r0[32], r1[32];
-            tmem_ld32(tmem + ((uint32_t)(32 * warp) << 16), r0);
-            tmem_ld32(tmem + ((uint32_t)(32 * warp) << 16) + 32, r1);
+        // this thread's row of K K^T (t < 64) or Q K^T (t >= 64), read from TMEM in two 32-column halves
+        // (half a row at a time keeps the register footprint small)
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                raw[i] = r0[i];
-                raw[32 + i] = r1[i];
-            }
-        }
-        if (t < 64) {  // L = beta D o K K^T, strictly lower
-            const int r = t;
-            const float gr = gam[r], br = bet[r];
+        for (int half = 0; half < 2; ++half) {
+            uint32_t raw[32];
+            tmem_ld32(tmem + ((uint32_t)(32 * warp) << 16) + 32 * half, raw);
+            if (t < 64) {  // L = beta D o K K^T, strictly lower
+                const int r = t;
+                const float gr = gam[r], br = bet[r];
 #pragma unroll
-            for (int i = 0; i < 64; ++i)
-                Lm[r * 65 + i] = (i < r && r < n) ? br * __expf(gr - gam[i]) * __uint_as_float(raw[i]) : 0.f;
-        } else {  // P = D o Q K^T, lower incl. diagonal -> image (and fp32 copy)
-            const int r = t - 64;
-            const float gr = gam[r];
-            float *p32 = a.P32 ? a.P32 + unit * C * C + (size_t)r * C : nullptr;
-#pragma unroll
-            for (int ch = 0; ch < 8; ++ch) {
-                float pv[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const int i = 8 * ch + e;
-                    pv[e] = (i <= r && r < n) ? __expf(gr - gam[i]) * __uint_as_float(raw[i]) : 0.f;
+                for (int k = 0; k < 32; ++k) {
+                    const int i = 32 * half + k;
+                    Lm[r * 65 + i] = (i < r && r < n) ? br * __expf(gr - gam[i]) * __uint_as_float(raw[k]) : 0.f;
                 }
-                put_split_chunk(img + 16384, img + 24576, r, ch, pv);
-                if (p32) {
-                    reinterpret_cast<float4 *>(p32)[2 * ch] = make_float4(pv[0], pv[1], pv[2], pv[3]);
-                    reinterpret_cast<float4 *>(p32)[2 * ch + 1] = make_float4(pv[4], pv[5], pv[6], pv[7]);
+            } else {  // P = D o Q K^T, lower incl. diagonal -> image (and fp32 copy)
+                const int r = t - 64;
+                const float gr = gam[r];
+                float *p32 = a.P32 ? a.P32 + unit * C * C + (size_t)r * C : nullptr;
+#pragma unroll
+                for (int cq = 0; cq < 4; ++cq) {
+                    const int ch = 4 * half + cq;
+                    float pv[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const int i = 8 * ch + e;
+                        pv[e] = (i <= r && r < n) ? __expf(gr - gam[i]) * __uint_as_float(raw[8 * cq + e]) : 0.f;
+                    }
+                    put_split_chunk(img + 16384, img + 24576, r, ch, pv);
+                    if (p32) {
+                        reinterpret_cast<float4 *>(p32)[2 * ch] = make_float4(pv[0], pv[1], pv[2], pv[3]);
+                        reinterpret_cast<float4 *>(p32)[2 * ch + 1] = make_float4(pv[4], pv[5], pv[6], pv[7]);
+                    }
                 }
             }
         }
