@@ -11,8 +11,8 @@
 namespace gdn {
 namespace tc {
 
-__device__ __forceinline__ void split2(float x, float &hi, float &lo);
 __device__ __forceinline__ uint32_t pack_bf16(float lo_elem, float hi_elem);
+__device__ __forceinline__ void split_pair(float x0, float x1, uint32_t &hi, uint32_t &lo);
 
 // Time limit of every mbarrier wait (ns of %globaltimer); on expiry the kernel
 // records where it gave up in the device error record and unwinds instead of
@@ -293,24 +293,32 @@ __device__ __forceinline__ void mma_chain_ta(uint32_t d_tmem, uint32_t a_tmem, u
 // Packs 32 fp32 values (pairs along K) into hi / lo bf16 pair words.
 __device__ __forceinline__ void split_pack32(const float *x, uint32_t (&hi)[32], uint32_t (&lo)[32]) {
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-        float h0, l0, h1, l1;
-        split2(x[2 * i], h0, l0);
-        split2(x[2 * i + 1], h1, l1);
-        hi[i] = pack_bf16(h0, h1);
-        lo[i] = pack_bf16(l0, l1);
-    }
+    for (int i = 0; i < 32; ++i) split_pair(x[2 * i], x[2 * i + 1], hi[i], lo[i]);
 }
 // Packs 16 fp32 values (pairs along K) into hi / lo bf16 pair words.
 __device__ __forceinline__ void split_pack16(const float *x, uint32_t (&hi)[16], uint32_t (&lo)[16]) {
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-        float h0, l0, h1, l1;
-        split2(x[2 * i], h0, l0);
-        split2(x[2 * i + 1], h1, l1);
-        hi[i] = pack_bf16(h0, h1);
-        lo[i] = pack_bf16(l0, l1);
+    for (int i = 0; i < 16; ++i) split_pair(x[2 * i], x[2 * i + 1], hi[i], lo[i]);
+}
+
+// 16 consecutive floats of shared memory (16-byte aligned) as four 16-byte loads.
+__device__ __forceinline__ void lds16f(const float *src, float (&x)[16]) {
+    const float4 *s4 = reinterpret_cast<const float4 *>(src);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const float4 w = s4[q];
+        x[4 * q] = w.x;
+        x[4 * q + 1] = w.y;
+        x[4 * q + 2] = w.z;
+        x[4 * q + 3] = w.w;
     }
+}
+
+// 8 consecutive floats of shared memory (16-byte aligned) as two 16-byte loads.
+__device__ __forceinline__ void lds8f(const float *src, float (&x)[8]) {
+    const float4 a = reinterpret_cast<const float4 *>(src)[0], b = reinterpret_cast<const float4 *>(src)[1];
+    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+    x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
 }
 
 // ------------------------------------------------------------------ swizzled tiles
@@ -328,21 +336,21 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo_elem, float hi_elem) {
     __nv_bfloat162 t = __floats2bfloat162_rn(lo_elem, hi_elem);
     return *reinterpret_cast<uint32_t *>(&t);
 }
-// hi = bf16(x), lo = bf16(x - hi): x ~= hi + lo to about 16 significant bits.
-__device__ __forceinline__ void split2(float x, float &hi, float &lo) {
-    hi = __bfloat162float(__float2bfloat16_rn(x));
-    lo = x - hi;
+// The pair (x0, x1) as a hi word {bf16(x0), bf16(x1)} and a lo word {bf16(x0 - hi0), bf16(x1 - hi1)}
+// (x0 in the low half of each word): x ~= hi + lo to about 16 significant bits.  One paired
+// conversion gives both hi values, which are read back from the word for the residuals.
+__device__ __forceinline__ void split_pair(float x0, float x1, uint32_t &hi, uint32_t &lo) {
+    hi = pack_bf16(x0, x1);
+    lo = pack_bf16(x0 - __uint_as_float(hi << 16), x1 - __uint_as_float(hi & 0xFFFF0000u));
 }
 // Writes 8 consecutive K elements of one row as hi and lo bf16 chunks.
 __device__ __forceinline__ void st_split_chunk(uint32_t hi_block, uint32_t lo_block, int row, int chunk,
                                                const float *x) {
-    float h[8], l[8];
+    uint32_t h[4], l[4];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) split2(x[i], h[i], l[i]);
-    st_shared_v4(sw128_addr(hi_block, row, chunk), pack_bf16(h[0], h[1]), pack_bf16(h[2], h[3]),
-                 pack_bf16(h[4], h[5]), pack_bf16(h[6], h[7]));
-    st_shared_v4(sw128_addr(lo_block, row, chunk), pack_bf16(l[0], l[1]), pack_bf16(l[2], l[3]),
-                 pack_bf16(l[4], l[5]), pack_bf16(l[6], l[7]));
+    for (int i = 0; i < 4; ++i) split_pair(x[2 * i], x[2 * i + 1], h[i], l[i]);
+    st_shared_v4(sw128_addr(hi_block, row, chunk), h[0], h[1], h[2], h[3]);
+    st_shared_v4(sw128_addr(lo_block, row, chunk), l[0], l[1], l[2], l[3]);
 }
 
 }  // namespace tc

@@ -385,6 +385,8 @@ k_tc_dscan(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
 #pragma unroll
             for (int hf = 0; hf < 2; ++hf) {
                 uint32_t kd16[16], pd16[16];
+                float ew[16];
+                lds16f(wv + 16 * hf, ew);
                 tmem_ld16x2(trow + TM_KD + 32 * hh + 16 * hf, kd16, trow + TM_PD + 32 * hh + 16 * hf, pd16);
 #pragma unroll
                 for (int q2 = 0; q2 < 2; ++q2) {
@@ -392,7 +394,7 @@ k_tc_dscan(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
 #pragma unroll
                     for (int e = 0; e < 8; ++e) {
                         const int i = 8 * q2 + e;
-                        x[e] = fmaf(p.scale, __uint_as_float(pd16[i]), wv[16 * hf + i] * __uint_as_float(kd16[i]));
+                        x[e] = fmaf(p.scale, __uint_as_float(pd16[i]), ew[i] * __uint_as_float(kd16[i]));
                     }
                     st_split_chunk(sb + SM_DD, sb + SM_DD + 16384, v, 4 * hh + 2 * hf + q2, x);
                 }
@@ -411,11 +413,16 @@ k_tc_dscan(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
             tc_fence_after();
             tmem_ld32(trow + TM_DR + 32 * hh, kd);
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-                float x[8];
+            for (int hf = 0; hf < 2; ++hf) {
+                float bw[16];
+                lds16f(wv + 32 + 16 * hf, bw);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) x[e] = wv[32 + 8 * q4 + e] * __uint_as_float(kd[8 * q4 + e]);
-                st_split_chunk(sb + SM_DD, sb + SM_DD + 16384, v, 4 * hh + q4, x);
+                for (int q2 = 0; q2 < 2; ++q2) {
+                    float x[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) x[e] = bw[8 * q2 + e] * __uint_as_float(kd[16 * hf + 8 * q2 + e]);
+                    st_split_chunk(sb + SM_DD, sb + SM_DD + 16384, v, 4 * hh + 2 * hf + q2, x);
+                }
             }
             tc_fence_before();
             fence_proxy_async_smem();

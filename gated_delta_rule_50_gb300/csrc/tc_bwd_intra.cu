@@ -335,22 +335,28 @@ k_tc_bwd_intra(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
             tmem_ld16x2(tmem + trow + C_KS + 16 * hh, ks, tmem + trow + C_QS + 16 * hh, qs);
             float part[16];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const int c = 16 * hh + i;
-                float vv = 0.f, dd = 0.f;
-                if (c < n) {
-                    vv = tile128_at(sm, S_DD, c, lrow);
-                    dd = tile128_at(sm, S_DO, c, lrow);
+            for (int q2 = 0; q2 < 2; ++q2) {
+                float g8[8];
+                lds8f(Gm + 16 * hh + 8 * q2, g8);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const int i = 8 * q2 + e, c = 16 * hh + i;
+                    float vv = 0.f, dd = 0.f;
+                    if (c < n) {
+                        vv = tile128_at(sm, S_DD, c, lrow);
+                        dd = tile128_at(sm, S_DO, c, lrow);
+                    }
+                    KSr[i] = __uint_as_float(ks[i]);
+                    Xr[i] = vv - g8[e] * KSr[i];
+                    part[i] = p.scale * g8[e] * dd * __uint_as_float(qs[i]);
                 }
-                KSr[i] = __uint_as_float(ks[i]);
-                Xr[i] = vv - Gm[c] * KSr[i];
-                part[i] = p.scale * Gm[c] * dd * __uint_as_float(qs[i]);
             }
 #pragma unroll
             for (int q2 = 0; q2 < 2; ++q2) {
-                float r8[8];
+                float r8[8], b8[8];
+                lds8f(bet + 16 * hh + 8 * q2, b8);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) r8[e] = bet[16 * hh + 8 * q2 + e] * Xr[8 * q2 + e];
+                for (int e = 0; e < 8; ++e) r8[e] = b8[e] * Xr[8 * q2 + e];
                 st_split_chunk(sb + S_DR + 16384, sb + S_DR + 49152, lrow, 2 * hh + q2, r8);
             }
             const float s = warp_transpose_sum16(part);
@@ -393,13 +399,14 @@ k_tc_bwd_intra(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
             float part[16];
 #pragma unroll
             for (int q2 = 0; q2 < 2; ++q2) {
-                float x8[8], d8[8];
+                float x8[8], d8[8], ev8[8];
+                lds8f(Ev + 16 * hh + 8 * q2, ev8);
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
-                    const int i = 8 * q2 + e, c = 16 * hh + i;
-                    x8[e] = fmaf(p.scale, __uint_as_float(pd[i]), Ev[c] * __uint_as_float(kd[i]));
+                    const int i = 8 * q2 + e;
+                    x8[e] = fmaf(p.scale, __uint_as_float(pd[i]), ev8[e] * __uint_as_float(kd[i]));
                     d8[e] = __uint_as_float(dl[i]);
-                    part[i] = Ev[c] * __uint_as_float(kd[i]) * d8[e];
+                    part[i] = ev8[e] * __uint_as_float(kd[i]) * d8[e];
                 }
                 st_split_chunk(sb + S_DD, sb + S_DD + 16384, lrow, 2 * hh + q2, x8);
                 st_split_chunk(sb + S_DR, sb + S_DR + 32768, lrow, 2 * hh + q2, d8);
@@ -436,20 +443,23 @@ k_tc_bwd_intra(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
             __nv_bfloat16 *dvs = reinterpret_cast<__nv_bfloat16 *>(sm + S_DD);  // dv staging [r][128]
 #pragma unroll
             for (int q2 = 0; q2 < 2; ++q2) {
-                float y8[8], s8[8];
+                float y8[8], s8[8], g8[8], b8[8], bg8[8];
+                lds8f(Gm + 16 * hh + 8 * q2, g8);
+                lds8f(bet + 16 * hh + 8 * q2, b8);
+                lds8f(bg + 16 * hh + 8 * q2, bg8);
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
                     const int i = 8 * q2 + e, c = 16 * hh + i;
                     const float drv = __uint_as_float(dr[i]);
-                    s8[e] = p.scale * Gm[c] * tile128_at(sm, S_DO, c, lrow);  // scale Gam dO (Gm = 0 past n)
+                    s8[e] = p.scale * g8[e] * tile128_at(sm, S_DO, c, lrow);  // scale Gam dO (Gm = 0 past n)
                     if (!F32OUT)
-                        dvs[c * DV + lrow] = __float2bfloat16_rn(bet[c] * drv);
+                        dvs[c * DV + lrow] = __float2bfloat16_rn(b8[e] * drv);
                     else if (c < n)  // checking mode: fp32 dv straight out (one 128-byte row segment per warp)
                         static_cast<float *>(a.dv)[(size_t)(tok0 + c) * p.Hv * DV + (size_t)hv * DV + lrow] =
-                            bet[c] * drv;
+                            b8[e] * drv;
                     pb[i] = drv * Xr[i];
-                    pg[i] = -bg[c] * drv * KSr[i];
-                    y8[e] = -bg[c] * drv;
+                    pg[i] = -bg8[e] * drv * KSr[i];
+                    y8[e] = -bg8[e] * drv;
                 }
                 // value-major tiles [v][i]: scale Gam dO and Y = -beta Gam dR side by side (N = 128 B operand)
                 st_split_chunk(sb + S_DR, sb + S_DR + 32768, lrow, 2 * hh + q2, s8);
@@ -547,9 +557,10 @@ k_tc_bwd_intra(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
             tmem_ld16(tmem + trow + C_DL + 16 * hh, dl);
 #pragma unroll
             for (int q2 = 0; q2 < 2; ++q2) {
-                float e8[8];
+                float e8[8], ev8[8];
+                lds8f(Ev + 16 * hh + 8 * q2, ev8);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) e8[e] = Ev[16 * hh + 8 * q2 + e] * __uint_as_float(dl[8 * q2 + e]);
+                for (int e = 0; e < 8; ++e) e8[e] = ev8[e] * __uint_as_float(dl[8 * q2 + e]);
                 st_split_chunk(sb + S_DD, sb + S_DD + 16384, lrow, 2 * hh + q2, e8);
             }
         }
@@ -559,13 +570,7 @@ k_tc_bwd_intra(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
             uint32_t z[16], hi[8], lo[8];
             tmem_ld16(tmem + trow + C_KS + 16 * hh, z);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                float h0, l0, h1, l1;
-                split2(__uint_as_float(z[2 * i]), h0, l0);
-                split2(__uint_as_float(z[2 * i + 1]), h1, l1);
-                hi[i] = pack_bf16(h0, h1);
-                lo[i] = pack_bf16(l0, l1);
-            }
+            for (int i = 0; i < 8; ++i) split_pair(__uint_as_float(z[2 * i]), __uint_as_float(z[2 * i + 1]), hi[i], lo[i]);
             tmem_st8x2(tmem + trow + C_QS + 8 * hh, hi, tmem + trow + C_QS + 32 + 8 * hh, lo);
         }
         pre_mma();

@@ -319,8 +319,7 @@ k_tc_fwd(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
             __nv_bfloat16 *stg = reinterpret_cast<__nv_bfloat16 *>(sm + SM_V + b * V_STAGE + 1024 * (warp - W_STATE0));
             uint32_t qs[16], oo[16];
             float gm[16];  // loaded before any store (generic pointers: no reordering across stores)
-#pragma unroll
-            for (int i = 0; i < 16; ++i) gm[i] = Gm[16 * hh + i];
+            lds16f(Gm + 16 * hh, gm);
             tmem_ld16x2(trow + TM_QS + 64 * b + 16 * hh, qs, trow + TM_O + 16 * hh, oo);
             tc_fence_before();
             mbar_arrive_warp(bar(B_EPIFREE0 + b));
@@ -385,13 +384,15 @@ k_tc_fwd(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
             const unsigned char *vt = sm + SM_V + (j & 1) * V_STAGE + (v >> 6) * 8192;
             // every operand is loaded before the first store (the stores are asm with a memory clobber,
             // which would otherwise order each load behind the previous store)
-            float R[16];
+            float R[16], bt[16], gg[16];
+            lds16f(bet + 16 * hh, bt);
+            lds16f(Gm + 16 * hh, gg);
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
                 const int c = 16 * hh + i;
                 const uint32_t vo = (uint32_t)c * 128u + ((uint32_t)(((v & 63) >> 3) ^ (c & 7)) << 4) + (uint32_t)(v & 7) * 2u;
                 const float vv = v_zero ? 0.f : __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(vt + vo));
-                R[i] = bet[c] * (vv - Gm[c] * __uint_as_float(raw[i]));
+                R[i] = bt[i] * (vv - gg[i] * __uint_as_float(raw[i]));
             }
 #pragma unroll
             for (int q = 0; q < 2; ++q) st_split_chunk(sb + SM_RT, sb + SM_RT + 16384, v, 2 * hh + q, R + 8 * q);
@@ -405,23 +406,18 @@ k_tc_fwd(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
             tc_fence_after();
             tmem_ld16(trow + TM_DL + 16 * hh, *reinterpret_cast<uint32_t(*)[16]>(raw));
             {
-                float ED[16], Dl[16];
+                float ED[16], Dl[16], ev[16];
+                lds16f(Ev + 16 * hh, ev);
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
                     Dl[i] = __uint_as_float(raw[i]);
-                    ED[i] = Ev[16 * hh + i] * Dl[i];
+                    ED[i] = ev[i] * Dl[i];
                 }
 #pragma unroll
                 for (int q = 0; q < 2; ++q) st_split_chunk(sb + SM_RT, sb + SM_RT + 16384, v, 2 * hh + q, Dl + 8 * q);
                 uint32_t ehi[8], elo[8];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    float h0, l0, h1, l1;
-                    split2(ED[2 * i], h0, l0);
-                    split2(ED[2 * i + 1], h1, l1);
-                    ehi[i] = pack_bf16(h0, h1);
-                    elo[i] = pack_bf16(l0, l1);
-                }
+                for (int i = 0; i < 8; ++i) split_pair(ED[2 * i], ED[2 * i + 1], ehi[i], elo[i]);
                 tmem_st8x2(trow + TM_EDH + 8 * hh, ehi, trow + TM_EDL + 8 * hh, elo);
             }
             tc_fence_before();

@@ -140,14 +140,12 @@ __device__ void blocked_inverse(float *Lm, float *Tb, int pt) {
 // 8 consecutive values of row r (chunk ch) of a 64-wide tile -> hi and lo 16-byte chunks of the image.
 __device__ __forceinline__ void put_split_chunk(unsigned char *hi_tile, unsigned char *lo_tile, int r, int ch,
                                                 const float *x) {
-    float h[8], l[8];
+    uint32_t h[4], l[4];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) split2(x[i], h[i], l[i]);
+    for (int i = 0; i < 4; ++i) split_pair(x[2 * i], x[2 * i + 1], h[i], l[i]);
     const uint32_t off = (uint32_t)r * 128u + ((uint32_t)(ch ^ (r & 7)) << 4);
-    *reinterpret_cast<uint4 *>(hi_tile + off) =
-        make_uint4(pack_bf16(h[0], h[1]), pack_bf16(h[2], h[3]), pack_bf16(h[4], h[5]), pack_bf16(h[6], h[7]));
-    *reinterpret_cast<uint4 *>(lo_tile + off) =
-        make_uint4(pack_bf16(l[0], l[1]), pack_bf16(l[2], l[3]), pack_bf16(l[4], l[5]), pack_bf16(l[6], l[7]));
+    *reinterpret_cast<uint4 *>(hi_tile + off) = make_uint4(h[0], h[1], h[2], h[3]);
+    *reinterpret_cast<uint4 *>(lo_tile + off) = make_uint4(l[0], l[1], l[2], l[3]);
 }
 
 __global__ void __launch_bounds__(NT, 6)
