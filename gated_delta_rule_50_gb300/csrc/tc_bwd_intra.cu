@@ -25,7 +25,9 @@
 // served by four warps, one per 16 chunk rows), one of them issues the MMAs of
 // a phase and all wait on one mbarrier before the next phase; work that needs
 // no result of the running MMAs (dv store-out, the (E Dl)^T tile, the dbeta / dg
-// reduction) runs meanwhile.  The k, q, dO and v chunk tiles arrive by TMA, the
+// reduction, and the next value head's h: copied in and staged in TMEM once the
+// h products of the dq / dk accumulation are done, while the rest of it runs)
+// proceeds meanwhile.  The k, q, dO and v chunk tiles arrive by TMA, the
 // A / P operand images and gate vectors by bulk copy, h and dSe by TMA as
 // 128-byte-swizzled fp32 boxes (value-major reads for the TMEM A operands) and
 // again by coalesced row loads transposed in shared memory (key-major, for the
@@ -58,7 +60,7 @@ constexpr uint32_t S_F = 180224;     // fp32 [64][65]: dA, then dL
 constexpr uint32_t S_F2 = S_F + 64 * 65 * 4;   // fp32 [64][65]: dQK staging
 constexpr uint32_t S_VEC = S_F2 + 64 * 65 * 4; // gam, Gam, E, beta, beta Gam (64 each); per-warp partial sums
 constexpr uint32_t S_BAR = S_VEC + (5 * 64 + 2 * NW * 64 + 2 * NW) * 4;
-constexpr uint32_t S_MISC = S_BAR + 32;
+constexpr uint32_t S_MISC = S_BAR + 40;
 constexpr uint32_t S_TOTAL = S_MISC + 16;
 constexpr uint32_t SMEM_BYTES = S_TOTAL + 1024;
 static_assert(SMEM_BYTES <= 232448, "shared memory");
@@ -117,14 +119,17 @@ __device__ __forceinline__ float tile128_at(const unsigned char *sm, uint32_t of
     return tile_at(sm, off + (uint32_t)(v >> 6) * 8192u, row, v & 63);
 }
 
-// dq^T, dk^T accumulation of one value head (issued by one thread).  A separate, non-inlined
-// function keeps the issue sequence compact and out of the kernel's register pressure.
-__device__ __noinline__ void issue_dq_dk(uint32_t sb, uint32_t tmem, uint32_t acc0) {
+// dq^T, dk^T accumulation of one value head (issued by one thread), in two groups with a commit to
+// bar_h_free between them: the products that read h (TMEM) and the value-major B tiles (S_DR) come
+// first, so that the next head's h can be copied in and staged while the rest run.  A separate,
+// non-inlined function keeps the issue sequence compact and out of the kernel's register pressure.
+__device__ __noinline__ void issue_dq_dk(uint32_t sb, uint32_t tmem, uint32_t acc0, uint32_t bar_h_free) {
         // [dq^T | dk^T] += h [scale Gam dO | Y]^T: one N = 128 product, the two value-major B tiles are
         // adjacent 64-wide blocks (hi at S_DR, lo at S_DR + 32 K)
         mma_chain_ta<8, 128>(tmem + C_DQ, tmem + C_HT, mdesc(sb + S_DR, 16384), ID_KM128, acc0);
         mma_chain_ta<8, 128>(tmem + C_DQ, tmem + C_HT + 64, mdesc(sb + S_DR, 16384), ID_KM128, 1);
         mma_chain_ta<8, 128>(tmem + C_DQ, tmem + C_HT, mdesc(sb + S_DR + 32768, 16384), ID_KM128, 1);
+        mma_commit(bar_h_free);
         for (int sp = 0; sp < 2; ++sp)  // dq^T += K^T dQK^T
             mma_chain<4, 128, 2>(tmem + C_DQ, mdesc(sb + S_KQ, 16384), kdesc(sb + S_DO + 8192 * sp), ID_MK, 1);
         // dk^T += dSe (E Dl)^T
@@ -167,14 +172,14 @@ __device__ __forceinline__ void key_rows(const float *__restrict__ src, uint32_t
                          __float_as_uint(w.z), __float_as_uint(w.w));
         }
         __syncwarp();
-        const int rr = lane & 15;
+        if ((lane >> 4) == hf) {  // the half-warp whose rows these are reads them (no selects)
+            const int rr = lane & 15;
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-            uint32_t v0, v1, v2, v3;
-            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                         : "=r"(v0), "=r"(v1), "=r"(v2), "=r"(v3)
-                         : "r"(tb + rr * 128 + ((c ^ (rr & 7)) << 4)));
-            if ((lane >> 4) == hf) {
+            for (int c = 0; c < 8; ++c) {
+                uint32_t v0, v1, v2, v3;
+                asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                             : "=r"(v0), "=r"(v1), "=r"(v2), "=r"(v3)
+                             : "r"(tb + rr * 128 + ((c ^ (rr & 7)) << 4)));
                 x[4 * c] = __uint_as_float(v0); x[4 * c + 1] = __uint_as_float(v1);
                 x[4 * c + 2] = __uint_as_float(v2); x[4 * c + 3] = __uint_as_float(v3);
             }
@@ -207,8 +212,9 @@ k_tc_bwd_intra(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     float *rdb = rdb_all + 64 * warp, *rdg = rdg_all + 64 * warp;
     float *Fa = reinterpret_cast<float *>(sm + S_F), *Fb = reinterpret_cast<float *>(sm + S_F2);
     const uint32_t bar_tma = sb + S_BAR, bar_mma = sb + S_BAR + 8;
-    // h (4 boxes) and dSe (2 + 2 boxes, two arrivals) of the current head, fp32 with the 128-byte swizzle
-    const uint32_t bar_h = sb + S_BAR + 16, bar_d = sb + S_BAR + 24;
+    // h (4 boxes) and dSe (2 + 2 boxes, two arrivals) of the current head, fp32 with the 128-byte swizzle;
+    // bar_hf: the current head's h products are done (S_DR and the h columns of TMEM are free)
+    const uint32_t bar_h = sb + S_BAR + 16, bar_d = sb + S_BAR + 24, bar_hf = sb + S_BAR + 32;
 
     const int gc = blockIdx.x, hq = blockIdx.y;
     const ChunkPos cp = chunk_pos(p, gc);
@@ -219,6 +225,7 @@ k_tc_bwd_intra(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         mbar_init(bar_mma, 1);
         mbar_init(bar_h, 1);
         mbar_init(bar_d, 2);
+        mbar_init(bar_hf, 1);
         misc[1] = 0;
         fence_mbar_init();
     }
@@ -227,7 +234,7 @@ k_tc_bwd_intra(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = misc[0];
-    uint32_t tma_ph = 0, mma_ph = 0, tma_issued = 0;
+    uint32_t tma_ph = 0, mma_ph = 0, tma_issued = 0, hf_ph = 0;
     // state loads: h phases issued / waited for, dSe arrivals (two per phase) / phases waited for
     uint32_t h_issued = 0, h_waited = 0, d_arrived = 0, d_waited = 0;
     bool ok = true;
@@ -260,6 +267,38 @@ k_tc_bwd_intra(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         ok = __syncthreads_and(w && ok) != 0;
     };
 
+    // h -> S_DR (4 boxes) and dSe boxes 0, 1 -> the fp32 scratch of value head hv_ (thread 0 issues;
+    // every thread counts).
+    auto issue_state = [&](int hv_) {
+        if (t == 0) {
+            const size_t unit = (size_t)gc * p.Hv + hv_;
+            mbar_arrive_expect_tx(bar_h, 65536);
+            for (int b = 0; b < 4; ++b)
+                tma_load_2d(sb + S_DR + 16384 * b, &tm_h, bar_h, 32 * b, (int)(unit * DK));
+            mbar_arrive_expect_tx(bar_d, 32768);
+            for (int b = 0; b < 2; ++b)
+                tma_load_2d(sb + S_F + 16384 * b, &tm_dse, bar_d, 32 * b, (int)(unit * DK));
+        }
+        ++h_issued;
+        ++d_arrived;
+    };
+    // h^T (lane v) from its boxes -> TMEM as the A operand of the KS / QS product: value v = lrow in
+    // box lq, keys 32 hh + i.  Returns false if the wait expired.
+    auto load_hT = [&]() -> bool {
+        bool w = true;
+        if (warp == 0) w = mbar_wait_warp(bar_h, h_waited & 1, abort_flag);
+        ok = __syncthreads_and(w && ok) != 0;
+        if (!ok) return false;
+        ++h_waited;
+        float xh[32];
+        state_col(sm + S_DR + 16384u * (uint32_t)lq, xh);
+        uint32_t hi[16], lo[16];
+        split_pack16(xh, hi, lo);
+        tmem_st16x2(tmem + trow + C_HT + 16 * hh, hi, tmem + trow + C_HT + 64 + 16 * hh, lo);
+        return true;
+    };
+
+    issue_state(hq * p.G);
     if (t == 0) {
         ++tma_issued;
         mbar_arrive_expect_tx(bar_tma, 32768);
@@ -276,13 +315,10 @@ k_tc_bwd_intra(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         const size_t st_off = ((size_t)gc * p.Hv + hv) * DK * DV;
         // ---------------------------------------------------------------- per-head vectors, dO / V tiles, A / P tiles
         ++tma_issued;
+        // (h and dSe boxes 0, 1 of this head were issued before the loop or during the previous
+        // head's dq / dk products)
         if (t == 0) {  // dO, V tiles; A / P operand images (S_A, S_P are adjacent); gate vectors
             const size_t unit = (size_t)gc * p.Hv + hv;
-            // h -> S_DR (4 boxes) first: it is needed first; dSe boxes 0, 1 -> the fp32 scratch
-            mbar_arrive_expect_tx(bar_h, 65536);
-            for (int b = 0; b < 4; ++b) tma_load_2d(sb + S_DR + 16384 * b, &tm_h, bar_h, 32 * b, (int)(unit * DK));
-            mbar_arrive_expect_tx(bar_d, 32768);
-            for (int b = 0; b < 2; ++b) tma_load_2d(sb + S_F + 16384 * b, &tm_dse, bar_d, 32 * b, (int)(unit * DK));
             mbar_arrive_expect_tx(bar_tma, 32768 + 32768 + 1024);
             bulk_load(sb + S_VEC, a.vecs + unit * 256, 1024, bar_tma);
             tma_load_3d(sb + S_DO, &tm_do, bar_tma, 0, hv, tok0);
@@ -291,23 +327,11 @@ k_tc_bwd_intra(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
             tma_load_3d(sb + S_DD + 8192, &tm_v, bar_tma, 64, hv, tok0);
             bulk_load(sb + S_A, a.tiles + unit * 32768, 32768, bar_tma);
         }
-        ++h_issued;
-        ++d_arrived;
         for (int o = t; o < 2 * NW * 64 + 2 * NW; o += NT) rdb_all[o] = 0.f;  // rdb, rdg, sH, sF
         // ---------------------------------------------------------------- P1: h^T (lane v) -> TMEM; KS, QS
-        {  // h^T from its boxes: value v = lrow in box lq, keys 32 hh + i
-            bool w = true;
-            if (warp == 0) w = mbar_wait_warp(bar_h, h_waited & 1, abort_flag);
-            ok = __syncthreads_and(w && ok) != 0;
-            if (!ok) break;
-            ++h_waited;
-            float xh[32];
-            state_col(sm + S_DR + 16384u * (uint32_t)lq, xh);
-            uint32_t hi[16], lo[16];
-            split_pack16(xh, hi, lo);
-            tmem_st16x2(tmem + trow + C_HT + 16 * hh, hi, tmem + trow + C_HT + 64 + 16 * hh, lo);
-        }
-        __syncthreads();  // vectors visible
+        // (for the later heads h^T was staged during the previous head's dq / dk products)
+        if (g == 0 && !load_hT()) break;
+        __syncthreads();  // partial sums zeroed
         pre_mma();
         ++d_arrived;
         if (t == 0) {
@@ -683,7 +707,7 @@ k_tc_bwd_intra(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         __syncthreads();
         // ---------------------------------------------------------------- P6: dq^T, dk^T accumulation
         pre_mma();
-        if (t == 0) issue_dq_dk(sb, tmem, g != 0);
+        if (t == 0) issue_dq_dk(sb, tmem, g != 0, bar_hf);
         // per-row results of this head (warp 1, while thread 0 issues the
         // dq / dk products below; lane holds rows lane and lane + 32): dbeta, and dg as
         // the reverse cumsum of dgam inside the chunk
@@ -726,6 +750,39 @@ k_tc_bwd_intra(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
                     a.dbeta[gi] = dbv[hf];
                 }
             }
+        }
+        // While the rest of the dq / dk products run: once the h products are done (S_DR and the h^T
+        // columns free), the next head's h and dSe boxes 0, 1 are copied in and each warp stages its share
+        // of the next h^T as soon as h has landed.  Thread 0 is still issuing, so warps 1..15 wait for the
+        // h products (named barrier) and warp 0 joins at the h wait.
+        if (g + 1 < p.G) {
+            bool w = true;
+            if (warp != 0) {
+                if (warp == 2) w = mbar_wait_warp(bar_hf, hf_ph & 1, abort_flag);
+                w = named_bar_and(1, NT - 32, w);
+                if (w && t == 64) {
+                    const size_t nu = (size_t)gc * p.Hv + hv + 1;
+                    mbar_arrive_expect_tx(bar_h, 65536);
+                    for (int b = 0; b < 4; ++b) tma_load_2d(sb + S_DR + 16384 * b, &tm_h, bar_h, 32 * b, (int)(nu * DK));
+                    mbar_arrive_expect_tx(bar_d, 32768);
+                    for (int b = 0; b < 2; ++b) tma_load_2d(sb + S_F + 16384 * b, &tm_dse, bar_d, 32 * b, (int)(nu * DK));
+                }
+            }
+            ++hf_ph;
+            ++h_issued;
+            ++d_arrived;
+            if (w) w = mbar_wait_warp(bar_h, h_waited & 1, abort_flag);
+            if (w) {
+                ++h_waited;
+                tc_fence_after();
+                float xh[32];
+                state_col(sm + S_DR + 16384u * (uint32_t)lq, xh);
+                uint32_t hi[16], lo[16];
+                split_pack16(xh, hi, lo);
+                tmem_st16x2(tmem + trow + C_HT + 16 * hh, hi, tmem + trow + C_HT + 64 + 16 * hh, lo);
+            }
+            ok = ok && w;
+            tc_fence_before();
         }
         mma_sync();
     }
