@@ -565,17 +565,24 @@ k_tc_bwd_intra(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
             mma_chain<4, 2, 2>(tmem + C_KS, kdesc(sb + S_A), kdesc(sb + S_P + 8192), ID_KK, 1);
             mma_chain<4, 2, 2>(tmem + C_KS, kdesc(sb + S_A + 8192), kdesc(sb + S_P), ID_KK, 1);
         }
-        // while Z runs: dv out, then (E Dl)^T into the staging region
-        if (!F32OUT) {  // dv out: 64 rows x 256 bytes from the staging tile, 16-byte stores
-            const uint4 *src = reinterpret_cast<const uint4 *>(sm + S_DD);
-            for (int o = t; o < 64 * 16; o += NT) {
-                const int r = o >> 4, c16 = o & 15;
-                if (r < n)
-                    *reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(a.dv) + (size_t)(tok0 + r) * p.Hv * DV +
-                                               (size_t)hv * DV + 8 * c16) = src[o];
+        // while Z runs: dv out, then (E Dl)^T into the staging region.  Warps 1..15 write dv out and
+        // signal it (barrier 2, arrive only) before syncing among themselves (barrier 3); warp 0, busy
+        // issuing, only waits at barrier 2 for the dv reads to be done before its share of the tile.
+        if (warp != 0) {
+            if (!F32OUT) {  // dv out: 64 rows x 256 bytes from the staging tile, 16-byte stores
+                const uint4 *src = reinterpret_cast<const uint4 *>(sm + S_DD);
+                for (int o = t - 32; o < 64 * 16; o += NT - 32) {
+                    const int r = o >> 4, c16 = o & 15;
+                    if (r < n)
+                        *reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(a.dv) +
+                                                   (size_t)(tok0 + r) * p.Hv * DV + (size_t)hv * DV + 8 * c16) = src[o];
+                }
             }
+            named_bar_arrive(2, NT);
+            named_bar(3, NT - 32);
+        } else {
+            named_bar(2, NT);
         }
-        __syncthreads();
         {  // (E Dl)^T -> value-major hi / lo tile [v][i] in the dDl region (the dv staging has been written out)
             uint32_t dl[16];
             tmem_ld16(tmem + trow + C_DL + 16 * hh, dl);
