@@ -331,8 +331,7 @@ k_tc_bwd_intra(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         // ---------------------------------------------------------------- P1: h^T (lane v) -> TMEM; KS, QS
         // (for the later heads h^T was staged during the previous head's dq / dk products)
         if (g == 0 && !load_hT()) break;
-        __syncthreads();  // partial sums zeroed
-        pre_mma();
+        pre_mma();  // (its barrier also orders the zeroed partial sums before their updates)
         ++d_arrived;
         if (t == 0) {
             // dSe boxes 2, 3 -> S_DR + 0, S_DR + 32 K (h read; the R^T tiles go to S_DR + 16 K, + 48 K)
@@ -619,8 +618,8 @@ k_tc_bwd_intra(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
 #pragma unroll
             for (int j = 0; j < 16; ++j) Fa[(16 * hh + j) * 65 + i] = -__uint_as_float(z[j]);
         }
-        __syncthreads();
-        // K K^T for the beta and gate terms of dL (lanes 0..63 of a [K; Q] K^T product)
+        // K K^T for the beta and gate terms of dL (lanes 0..63 of a [K; Q] K^T product); the barrier in
+        // pre_mma orders the dL loads above before it overwrites their columns
         pre_mma();
         if (t == 0)
             for (int blk = 0; blk < 2; ++blk)
@@ -711,7 +710,6 @@ k_tc_bwd_intra(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
                 tmem_st16x2(tmem + trow + C_KS + 16 * hh, hi, tmem + trow + C_KS + 64 + 16 * hh, lo);
             }
         }
-        __syncthreads();
         // ---------------------------------------------------------------- P6: dq^T, dk^T accumulation
         pre_mma();
         if (t == 0) issue_dq_dk(sb, tmem, g != 0, bar_hf);
