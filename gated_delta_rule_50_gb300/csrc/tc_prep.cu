@@ -42,7 +42,9 @@ constexpr uint32_t S_VEC = S_TB + 3 * 16 * 17 * 4;    // gam, Gam, E, beta (64 e
 constexpr uint32_t S_BAR = 32768;
 constexpr uint32_t S_MISC = S_BAR + 16;
 constexpr uint32_t SMEM_BYTES = S_MISC + 32 + 1024;
-static_assert(S_VEC + 4 * 64 * 4 <= S_BAR, "scratch fits in the k / q tile space");
+constexpr uint32_t S_GB = S_VEC + 4 * 64 * 4;        // g (or g_cum) and beta of up to 8 value heads x 64 rows
+constexpr int GB_HEADS = 8;
+static_assert(S_GB + 2 * GB_HEADS * 64 * 4 <= S_BAR, "scratch fits in the k / q tile space");
 
 constexpr uint32_t ID_N64 = idesc_bf16(128, 64, 0, 0);
 
@@ -178,6 +180,20 @@ k_tc_prep(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
     tc_fence_after();
     const uint32_t tmem = misc[0];
     bool ok = true;
+    // g (or g_cum) and beta of row t (threads 0..63) for every value head of the group (up to GB_HEADS;
+    // adjacent in memory), loaded now so that the loads overlap the k / q copy and the K K^T product and
+    // parked in shared memory once that space is free; rows past the chunk end hold the last value
+    const bool gb_staged = p.G <= GB_HEADS;
+    float gpre[GB_HEADS], bpre[GB_HEADS];
+    if (gb_staged && t < 64) {
+        const size_t row = (size_t)(tok0 + (t < n ? t : n - 1)) * p.Hv + (size_t)hq * p.G;
+#pragma unroll
+        for (int gg = 0; gg < GB_HEADS; ++gg)
+            if (gg < p.G) {
+                gpre[gg] = (a.g_is_cum || t < n) ? a.g[row + gg] : 0.f;
+                bpre[gg] = t < n ? a.beta[row + gg] : 0.f;
+            }
+    }
     // K K^T (lanes 0..63) and Q K^T (lanes 64..127) of this chunk: D1 = [K; Q] K^T
     if (t == 0) {
         mbar_arrive_expect_tx(bar_tma, 32768);
@@ -197,17 +213,30 @@ k_tc_prep(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
     if (ok && warp == 0) ok = mbar_wait_warp(bar_mma, 0, abort_flag);
     ok = __syncthreads_and(ok) != 0;  // the MMA has read the k / q tiles: their space is scratch from here
     tc_fence_after();
+    float *gst = reinterpret_cast<float *>(sm + S_GB), *bst = gst + GB_HEADS * 64;
+    if (gb_staged && t < 64) {  // each thread reads back only its own entries
+#pragma unroll
+        for (int gg = 0; gg < GB_HEADS; ++gg)
+            if (gg < p.G) {
+                gst[gg * 64 + t] = gpre[gg];
+                bst[gg * 64 + t] = bpre[gg];
+            }
+    }
     for (int g = 0; ok && g < p.G; ++g) {
         const int hv = hq * p.G + g;
         const size_t unit = (size_t)gc * p.Hv + hv;
         // gate cumsum over rows 0..63 (threads 0..63); rows past the chunk end hold the last value
         float x = 0.f, bv = 0.f;
         if (t < 64) {
-            const size_t gi = (size_t)(tok0 + (t < n ? t : n - 1)) * p.Hv + hv;
-            if (a.g_is_cum) {
-                x = a.g[gi];
+            if (gb_staged) {
+                x = gst[g * 64 + t];
+                bv = bst[g * 64 + t];
             } else {
-                x = t < n ? a.g[gi] : 0.f;
+                const size_t gi = (size_t)(tok0 + (t < n ? t : n - 1)) * p.Hv + hv;
+                x = (a.g_is_cum || t < n) ? a.g[gi] : 0.f;
+                bv = t < n ? a.beta[gi] : 0.f;
+            }
+            if (!a.g_is_cum) {
 #pragma unroll
                 for (int off = 1; off < 32; off <<= 1) {
                     const float y = __shfl_up_sync(0xffffffffu, x, off);
@@ -215,7 +244,6 @@ k_tc_prep(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                 }
                 if (t == 31) *wtot = x;
             }
-            bv = t < n ? a.beta[gi] : 0.f;
         }
         __syncthreads();
         if (t < 64) {
