@@ -22,6 +22,12 @@ constexpr uint64_t WAIT_NS = 1000000000ull;
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
+// The 1024-byte-aligned start of the dynamic shared memory, formed by pointer arithmetic on the shared
+// array itself so that the compiler keeps its address space: plain C++ loads and stores through it stay
+// shared-memory instructions (an integer round trip would make them generic ones).
+__device__ __forceinline__ unsigned char *smem_align1024(unsigned char *raw) {
+    return raw + ((1024u - (smem_u32(raw) & 1023u)) & 1023u);
+}
 
 // ------------------------------------------------------------------ mbarrier
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {

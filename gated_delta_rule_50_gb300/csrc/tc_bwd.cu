@@ -90,8 +90,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 k_tc_dscan(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_do, Plan p,
            DscanArgs a) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
-    unsigned char *sm = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                                          ~uintptr_t(1023));
+    unsigned char *sm = smem_align1024(smem_raw);
     const uint32_t sb = smem_u32(sm);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     uint32_t *misc = reinterpret_cast<uint32_t *>(sm + SM_MISC);

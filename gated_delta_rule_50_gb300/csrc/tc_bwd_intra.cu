@@ -195,8 +195,7 @@ k_tc_bwd_intra(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
                const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ CUtensorMap tm_dse, Plan p,
                IntraArgs a) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
-    unsigned char *sm = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                                          ~uintptr_t(1023));
+    unsigned char *sm = smem_align1024(smem_raw);
     const uint32_t sb = smem_u32(sm);
     const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
     const int lq = warp & 3, hh = warp >> 2;  // TMEM lane quarter; chunk rows 16 hh .. 16 hh + 15

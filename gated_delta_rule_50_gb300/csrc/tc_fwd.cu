@@ -105,6 +105,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 k_tc_fwd(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
          const __grid_constant__ CUtensorMap tm_v, Plan p, FwdArgs a) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
+    // (aligned through an integer round trip, so the state warps' shared-memory reads are generic loads:
+    // this kernel measured 5 % faster this way than with smem_align1024, unlike the other three)
     unsigned char *sm = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                           ~uintptr_t(1023));
     const uint32_t sb = smem_u32(sm);

@@ -153,8 +153,7 @@ __device__ __forceinline__ void put_split_chunk(unsigned char *hi_tile, unsigned
 __global__ void __launch_bounds__(NT, 6)
 k_tc_prep(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q, Plan p, PrepArgs a) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
-    unsigned char *sm = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                                          ~uintptr_t(1023));
+    unsigned char *sm = smem_align1024(smem_raw);
     const uint32_t sb = smem_u32(sm);
     const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
     uint32_t *misc = reinterpret_cast<uint32_t *>(sm + S_MISC);
