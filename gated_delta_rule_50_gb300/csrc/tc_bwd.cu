@@ -405,7 +405,7 @@ k_tc_dscan(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
             if (dSe_out) {  // while dR is computed: dS at this chunk's end -> workspace
                 float *dst = dSe_out + ((size_t)gc * p.Hv + hv) * DK * DV + (size_t)(64 * hh) * DV + v;
 #pragma unroll
-                for (int i = 0; i < 64; ++i) dst[(size_t)i * DV] = S[i];
+                for (int i = 0; i < 64; ++i) __stcs(dst + (size_t)i * DV, S[i]);
             }
             // (e) Y = -beta Gam o dR
             if (!(ok = wwait(B_DRDONE, t & 1, t))) break;

@@ -572,8 +572,9 @@ k_tc_bwd_intra(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
                 for (int o = t - 32; o < 64 * 16; o += NT - 32) {
                     const int r = o >> 4, c16 = o & 15;
                     if (r < n)
-                        *reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(a.dv) +
-                                                   (size_t)(tok0 + r) * p.Hv * DV + (size_t)hv * DV + 8 * c16) = src[o];
+                        __stcs(reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(a.dv) +
+                                                         (size_t)(tok0 + r) * p.Hv * DV + (size_t)hv * DV + 8 * c16),
+                               src[o]);
                 }
             }
             named_bar_arrive(2, NT);
@@ -814,7 +815,7 @@ k_tc_bwd_intra(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
             const int r = 16 * hh + j;
             if (r < n) {
                 __nv_bfloat16 b = __float2bfloat16_rn(__uint_as_float(d[j]));
-                dqp[(size_t)(tok0 + r) * rs] = *reinterpret_cast<uint16_t *>(&b);
+                __stcs(reinterpret_cast<unsigned short *>(dqp + (size_t)(tok0 + r) * rs), *reinterpret_cast<unsigned short *>(&b));
             }
         }
         tmem_ld16(tmem + trow + C_DK + 16 * hh, d);
@@ -823,7 +824,7 @@ k_tc_bwd_intra(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
             const int r = 16 * hh + j;
             if (r < n) {
                 __nv_bfloat16 b = __float2bfloat16_rn(__uint_as_float(d[j]));
-                dkp[(size_t)(tok0 + r) * rs] = *reinterpret_cast<uint16_t *>(&b);
+                __stcs(reinterpret_cast<unsigned short *>(dkp + (size_t)(tok0 + r) * rs), *reinterpret_cast<unsigned short *>(&b));
             }
         }
     } else if (t == 0) {

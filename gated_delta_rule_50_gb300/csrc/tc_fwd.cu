@@ -348,9 +348,10 @@ k_tc_fwd(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
                 const int ri = 8 * k2 + (lane >> 2), c = 16 * hh + ri;
                 const uint4 w = src[ri * 4 + (lane & 3)];
                 if (c < n)
-                    *reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(o_out) +
-                                               ((size_t)(tok0 + c) * p.Hv + hv) * DV + 32 * (warp & 3) +
-                                               8 * (lane & 3)) = w;
+                    __stcs(reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(o_out) +
+                                                     ((size_t)(tok0 + c) * p.Hv + hv) * DV + 32 * (warp & 3) +
+                                                     8 * (lane & 3)),
+                           w);
             }
             // the staging writes (generic proxy) are ordered before the next TMA write of this buffer
             fence_proxy_async_smem();
@@ -372,7 +373,7 @@ k_tc_fwd(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
             if (h_out) {  // while KS is computed: the chunk-entry state (backward recompute)
                 const size_t hb = ((size_t)(sr.c0 + j) * p.Hv + hv) * DK * DV;
 #pragma unroll
-                for (int i = 0; i < 32; ++i) h_out[hb + (size_t)(32 * hh + i) * DV + v] = S[i];
+                for (int i = 0; i < 32; ++i) __stcs(h_out + hb + (size_t)(32 * hh + i) * DV + v, S[i]);
             }
             // (c) R^T = beta (V - Gam K S)^T
             if (!(ok = wwait(B_VFULL0 + (j & 1), (j >> 1) & 1, j))) break;
