@@ -377,26 +377,31 @@ k_tc_fwd(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
             }
             // (c) R^T = beta (V - Gam K S)^T
             if (!(ok = wwait(B_VFULL0 + (j & 1), (j >> 1) & 1, j))) break;
+            const float *vj = vecs(j), *Gm = vj + 64, *Ev = vj + 128, *bet = vj + 192;
+            // the chunk's v values at (row c = 16 hh + i, column v), read while K S is still being computed;
+            // rows past the chunk end are finite (next tokens or zero fill) and meet beta = 0
+            float vv[16];
+            {
+                const unsigned char *vt = sm + SM_V + (j & 1) * V_STAGE + (v >> 6) * 8192;  // two 64-column boxes
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const int c = 16 * hh + i;
+                    const uint32_t vo = (uint32_t)c * 128u + ((uint32_t)(((v & 63) >> 3) ^ (c & 7)) << 4) +
+                                        (uint32_t)(v & 7) * 2u;
+                    vv[i] = v_zero ? 0.f : __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(vt + vo));
+                }
+            }
             if (!(ok = wwait(B_KSDONE, j & 1, j))) break;
             tc_fence_after();
-            const float *vj = vecs(j), *Gm = vj + 64, *Ev = vj + 128, *bet = vj + 192;
             uint32_t raw[32];
             tmem_ld16(trow + TM_KS + 16 * hh, *reinterpret_cast<uint32_t(*)[16]>(raw));
-            // v at (row c, column v) of the swizzled tile (two 64-column boxes); rows past the chunk end
-            // are finite (next tokens or zero fill) and meet beta = 0
-            const unsigned char *vt = sm + SM_V + (j & 1) * V_STAGE + (v >> 6) * 8192;
             // every operand is loaded before the first store (the stores are asm with a memory clobber,
             // which would otherwise order each load behind the previous store)
             float R[16], bt[16], gg[16];
             lds16f(bet + 16 * hh, bt);
             lds16f(Gm + 16 * hh, gg);
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const int c = 16 * hh + i;
-                const uint32_t vo = (uint32_t)c * 128u + ((uint32_t)(((v & 63) >> 3) ^ (c & 7)) << 4) + (uint32_t)(v & 7) * 2u;
-                const float vv = v_zero ? 0.f : __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(vt + vo));
-                R[i] = bt[i] * (vv - gg[i] * __uint_as_float(raw[i]));
-            }
+            for (int i = 0; i < 16; ++i) R[i] = bt[i] * (vv[i] - gg[i] * __uint_as_float(raw[i]));
 #pragma unroll
             for (int q = 0; q < 2; ++q) st_split_chunk(sb + SM_RT, sb + SM_RT + 16384, v, 2 * hh + q, R + 8 * q);
             tc_fence_before();
