@@ -347,6 +347,16 @@ k_tc_dscan(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
         bool ok = true;
         for (int t = 0; t < nck && ok; ++t) {
             const int j = nck - 1 - t, gc = sr.c0 + j, tok0 = chunk_tok0(t), n = min(C, sr.tok1 - tok0);
+            // gate values of this warp's chunk row c = 32 hh + lane, loaded first: their latency overlaps the
+            // dS split below
+            const int cg = 32 * hh + lane;
+            const float glast = a.g_cum[(size_t)(tok0 + n - 1) * p.Hv + hv];
+            float gcv = 0.f, btv = 0.f;
+            if (cg < n) {
+                const size_t gi = (size_t)(tok0 + cg) * p.Hv + hv;
+                gcv = a.g_cum[gi];
+                btv = a.beta[gi];
+            }
             // (a) dS^T -> TMEM (hi / lo bf16 pairs) for KdS; dS at this chunk's end -> workspace
 #pragma unroll
             for (int hf = 0; hf < 2; ++hf) {  // in halves: dS (64 registers) stays live throughout
@@ -356,15 +366,6 @@ k_tc_dscan(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
             }
             tc_fence_before();
             mbar_arrive_warp(bar(B_DSREADY));
-            // gate values of this warp's chunk row c = 32 hh + lane (loaded before the dSe stores below)
-            const int cg = 32 * hh + lane;
-            const float glast = a.g_cum[(size_t)(tok0 + n - 1) * p.Hv + hv];
-            float gcv = 0.f, btv = 0.f;
-            if (cg < n) {
-                const size_t gi = (size_t)(tok0 + cg) * p.Hv + hv;
-                gcv = a.g_cum[gi];
-                btv = a.beta[gi];
-            }
             // gate vectors of this warp's 32 chunk rows c = 32 hh + lane
             float gl_all;
             {

@@ -345,9 +345,17 @@ k_tc_bwd_intra(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
                     mma_chain_ta<4, 2>(tmem + C_KS, tmem + C_HT + 64 * sp + 32 * blk, kdesc(sb + S_KQ + 16384 * blk),
                                        ID_N128, (sp | blk) != 0);
         }
-        mma_sync();
-        if (!ok) break;
         tma_wait();  // dO, V, A, P and the gate vectors of this head
+        if (!ok) break;
+        // this thread's v and dO values (rows c = 16 hh + i, value lrow), read while K S / Q S run
+        float vv[16], dd[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const int c = 16 * hh + i;
+            vv[i] = c < n ? tile128_at(sm, S_DD, c, lrow) : 0.f;
+            dd[i] = c < n ? tile128_at(sm, S_DO, c, lrow) : 0.f;
+        }
+        mma_sync();
         if (!ok) break;
         if (t < 64) bg[t] = bet[t] * Gm[t];  // read after the next CTA barrier
         // ---------------------------------------------------------------- P2: R^T tile, dgam (scale Gam dO . QS)
@@ -362,15 +370,10 @@ k_tc_bwd_intra(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
                 lds8f(Gm + 16 * hh + 8 * q2, g8);
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
-                    const int i = 8 * q2 + e, c = 16 * hh + i;
-                    float vv = 0.f, dd = 0.f;
-                    if (c < n) {
-                        vv = tile128_at(sm, S_DD, c, lrow);
-                        dd = tile128_at(sm, S_DO, c, lrow);
-                    }
+                    const int i = 8 * q2 + e;
                     KSr[i] = __uint_as_float(ks[i]);
-                    Xr[i] = vv - g8[e] * KSr[i];
-                    part[i] = p.scale * g8[e] * dd * __uint_as_float(qs[i]);
+                    Xr[i] = vv[i] - g8[e] * KSr[i];
+                    part[i] = p.scale * g8[e] * dd[i] * __uint_as_float(qs[i]);
                 }
             }
 #pragma unroll
