@@ -246,6 +246,16 @@ __device__ __forceinline__ void tmem_ld16x2(uint32_t ta, uint32_t (&r)[16], uint
         : "r"(ta), "r"(tb)
         : "memory");
 }
+// Two 8-column loads, waited.
+__device__ __forceinline__ void tmem_ld8x2(uint32_t ta, uint32_t (&r)[8], uint32_t tb, uint32_t (&s)[8]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%16];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%8, %9, %10, %11, %12, %13, %14, %15}, [%17];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : GDN_R8(0), GDN_S8(0)
+        : "r"(ta), "r"(tb)
+        : "memory");
+}
 // Two 16-column stores (e.g. a hi / lo pair), waited.
 __device__ __forceinline__ void tmem_st16x2(uint32_t ta, const uint32_t (&a)[16], uint32_t tb,
                                             const uint32_t (&b)[16]) {

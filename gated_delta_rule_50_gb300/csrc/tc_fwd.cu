@@ -305,47 +305,54 @@ k_tc_fwd(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
         for (int i = 0; i < 32; ++i)
             S[i] = init ? init[(size_t)(32 * hh + i) * DV + v] : (init_identity && 32 * hh + i == v ? 1.f : 0.f);
 
-        // o of chunk jj: scale (Gam QS + O) -> bf16.  Each warp stages its 16 rows x 32 values in a private
-        // 1 KB part of the v buffer of chunk jj (consumed: every state thread is past R of jj) and writes
-        // them back as 64-byte row segments with 16-byte stores; no CTA-wide barrier is involved.
-        auto epilogue = [&](int jj) -> bool {
+        // o of chunk jj: scale (Gam QS + O) -> bf16, in two parts of 8 of the warp's 16 rows (part 0 while
+        // Dl of the next chunk is computed, part 1 while its U is).  Each warp stages its rows x 32 values in
+        // a private 1 KB part of the v buffer of chunk jj (consumed: every state thread is past R of jj) and
+        // writes them back as 64-byte row segments with 16-byte stores; no CTA-wide barrier is involved.
+        // QS / O and the v buffer are released after part 1.
+        auto epilogue = [&](int jj, int part) -> bool {
             const int tok0 = sr.tok0 + jj * C, n = min(C, sr.tok1 - tok0), b = jj & 1;
             const float *Gm = vecs(jj) + 64;
             if (!o_out) {  // nothing to write: release QS / O and the v buffer (this thread is past R of jj)
-                mbar_arrive_warp(bar(B_EPIFREE0 + b));
-                mbar_arrive_warp(bar(B_VEMPTY0 + b));
+                if (part == 1) {
+                    mbar_arrive_warp(bar(B_EPIFREE0 + b));
+                    mbar_arrive_warp(bar(B_VEMPTY0 + b));
+                }
                 return true;
             }
-            if (!wwait(B_ODONE, jj & 1, jj)) return false;
-            tc_fence_after();
+            if (part == 0) {
+                if (!wwait(B_ODONE, jj & 1, jj)) return false;
+                tc_fence_after();
+            }
             __nv_bfloat16 *stg = reinterpret_cast<__nv_bfloat16 *>(sm + SM_V + b * V_STAGE + 1024 * (warp - W_STATE0));
-            uint32_t qs[16], oo[16];
-            float gm[16];  // loaded before any store (generic pointers: no reordering across stores)
-            lds16f(Gm + 16 * hh, gm);
-            tmem_ld16x2(trow + TM_QS + 64 * b + 16 * hh, qs, trow + TM_O + 16 * hh, oo);
-            tc_fence_before();
-            mbar_arrive_warp(bar(B_EPIFREE0 + b));
+            uint32_t qs[8], oo[8];
+            float gm[8];  // loaded before any store (generic pointers: no reordering across stores)
+            lds8f(Gm + 16 * hh + 8 * part, gm);
+            tmem_ld8x2(trow + TM_QS + 64 * b + 16 * hh + 8 * part, qs, trow + TM_O + 16 * hh + 8 * part, oo);
+            if (part == 1) {
+                tc_fence_before();
+                mbar_arrive_warp(bar(B_EPIFREE0 + b));
+            }
             if (F32OUT) {  // checking mode: the fp32 value, one 128-byte row segment per warp and row
                 float *of = static_cast<float *>(o_out) + (size_t)tok0 * p.Hv * DV + (size_t)hv * DV + v;
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const int c = 16 * hh + i;
+                for (int i = 0; i < 8; ++i) {
+                    const int c = 16 * hh + 8 * part + i;
                     if (c < n)
                         of[(size_t)c * p.Hv * DV] =
                             p.scale * fmaf(gm[i], __uint_as_float(qs[i]), __uint_as_float(oo[i]));
                 }
-                mbar_arrive_warp(bar(B_VEMPTY0 + b));
+                if (part == 1) mbar_arrive_warp(bar(B_VEMPTY0 + b));
                 return true;
             }
 #pragma unroll
-            for (int i = 0; i < 16; ++i)  // row i of this warp's 16, column lane
-                stg[i * 32 + lane] =
+            for (int i = 0; i < 8; ++i)  // row 8 part + i of this warp's 16, column lane
+                stg[(8 * part + i) * 32 + lane] =
                     __float2bfloat16_rn(p.scale * fmaf(gm[i], __uint_as_float(qs[i]), __uint_as_float(oo[i])));
             __syncwarp();
-            const uint4 *src = reinterpret_cast<const uint4 *>(stg);
-#pragma unroll
-            for (int k2 = 0; k2 < 2; ++k2) {  // lane: row 8 k2 + lane / 4, 8 values at 8 (lane % 4)
-                const int ri = 8 * k2 + (lane >> 2), c = 16 * hh + ri;
+            {  // lane: row 8 part + lane / 4, 8 values at 8 (lane % 4)
+                const uint4 *src = reinterpret_cast<const uint4 *>(stg);
+                const int ri = 8 * part + (lane >> 2), c = 16 * hh + ri;
                 const uint4 w = src[ri * 4 + (lane & 3)];
                 if (c < n)
                     __stcs(reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(o_out) +
@@ -353,9 +360,11 @@ k_tc_fwd(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
                                                      8 * (lane & 3)),
                            w);
             }
-            // the staging writes (generic proxy) are ordered before the next TMA write of this buffer
-            fence_proxy_async_smem();
-            mbar_arrive_warp(bar(B_VEMPTY0 + b));
+            if (part == 1) {
+                // the staging writes (generic proxy) are ordered before the next TMA write of this buffer
+                fence_proxy_async_smem();
+                mbar_arrive_warp(bar(B_VEMPTY0 + b));
+            }
             return true;
         };
 
@@ -408,7 +417,7 @@ k_tc_fwd(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
             fence_proxy_async_smem();
             mbar_arrive_warp(bar(B_RTREADY));
             // while Dl is computed: o of chunk j - 1
-            if (j >= 1 && !(ok = epilogue(j - 1))) break;
+            if (j >= 1 && !(ok = epilogue(j - 1, 0))) break;
             // (e) Dl^T -> Dl^T tile (R region) and (E Dl)^T hi / lo pairs in TMEM
             if (!(ok = wwait(B_DLDONE, j & 1, j))) break;
             tc_fence_after();
@@ -431,6 +440,8 @@ k_tc_fwd(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
             tc_fence_before();
             fence_proxy_async_smem();
             mbar_arrive_warp(bar(B_EDREADY));
+            // while U is computed: the rest of the o of chunk j - 1
+            if (j >= 1 && !(ok = epilogue(j - 1, 1))) break;
             // (g) S^T <- Gam_last S^T + U^T
             if (!(ok = wwait(B_UPDDONE, j & 1, j))) break;
             tc_fence_after();
@@ -440,7 +451,8 @@ k_tc_fwd(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
             for (int i = 0; i < 32; ++i) S[i] = fmaf(gl, S[i], __uint_as_float(raw[i]));
             tc_fence_before();
         }
-        if (ok && nck > 0) ok = epilogue(nck - 1);
+        if (ok && nck > 0) ok = epilogue(nck - 1, 0);
+        if (ok && nck > 0) ok = epilogue(nck - 1, 1);
         if (ok && fin) {
 #pragma unroll
             for (int i = 0; i < 32; ++i) fin[(size_t)(32 * hh + i) * DV + v] = S[i];
