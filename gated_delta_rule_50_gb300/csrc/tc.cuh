@@ -120,10 +120,6 @@ __device__ __forceinline__ void tc_fence_after() {
 __device__ __forceinline__ void named_bar(uint32_t id, uint32_t nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
-// Arrival at a named barrier without waiting (the waiting threads use named_bar with the same count).
-__device__ __forceinline__ void named_bar_arrive(uint32_t id, uint32_t nthreads) {
-    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
-}
 // Named barrier that also ANDs a predicate over the participating threads, so a
 // group leaves a loop together (nobody is left waiting at the next bar.sync).
 __device__ __forceinline__ bool named_bar_and(uint32_t id, uint32_t nthreads, bool pred) {

@@ -24,8 +24,9 @@
 // The kernel is phase-sequential: 512 threads (each TMEM lane quarter is
 // served by four warps, one per 16 chunk rows), one of them issues the MMAs of
 // a phase and all wait on one mbarrier before the next phase; work that needs
-// no result of the running MMAs (dv store-out, the (E Dl)^T tile, the dbeta / dg
-// reduction, and the next value head's h: copied in and staged in TMEM once the
+// no result of the running MMAs (dv store-out beside Z = A dA~^T, the (E Dl)^T
+// tile beside A^T Z, the dbeta / dg reduction, and the next value head's h:
+// copied in and staged in TMEM once the
 // h products of the dq / dk accumulation are done, while the rest of it runs)
 // proceeds meanwhile.  The k, q, dO and v chunk tiles arrive by TMA, the
 // A / P operand images and gate vectors by bulk copy, h and dSe by TMA as
@@ -566,35 +567,15 @@ k_tc_bwd_intra(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
             mma_chain<4, 2, 2>(tmem + C_KS, kdesc(sb + S_A), kdesc(sb + S_P + 8192), ID_KK, 1);
             mma_chain<4, 2, 2>(tmem + C_KS, kdesc(sb + S_A + 8192), kdesc(sb + S_P), ID_KK, 1);
         }
-        // while Z runs: dv out, then (E Dl)^T into the staging region.  Warps 1..15 write dv out and
-        // signal it (barrier 2, arrive only) before syncing among themselves (barrier 3); warp 0, busy
-        // issuing, only waits at barrier 2 for the dv reads to be done before its share of the tile.
-        if (warp != 0) {
-            if (!F32OUT) {  // dv out: 64 rows x 256 bytes from the staging tile, 16-byte stores
-                const uint4 *src = reinterpret_cast<const uint4 *>(sm + S_DD);
-                for (int o = t - 32; o < 64 * 16; o += NT - 32) {
-                    const int r = o >> 4, c16 = o & 15;
-                    if (r < n)
-                        __stcs(reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(a.dv) +
-                                                         (size_t)(tok0 + r) * p.Hv * DV + (size_t)hv * DV + 8 * c16),
-                               src[o]);
-                }
-            }
-            named_bar_arrive(2, NT);
-            named_bar(3, NT - 32);
-        } else {
-            named_bar(2, NT);
-        }
-        {  // (E Dl)^T -> value-major hi / lo tile [v][i] in the dDl region (the dv staging has been written out)
-            uint32_t dl[16];
-            tmem_ld16(tmem + trow + C_DL + 16 * hh, dl);
-#pragma unroll
-            for (int q2 = 0; q2 < 2; ++q2) {
-                float e8[8], ev8[8];
-                lds8f(Ev + 16 * hh + 8 * q2, ev8);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) e8[e] = ev8[e] * __uint_as_float(dl[8 * q2 + e]);
-                st_split_chunk(sb + S_DD, sb + S_DD + 16384, lrow, 2 * hh + q2, e8);
+        // while Z runs (thread 0 issuing it): dv out by warps 1..15
+        if (warp != 0 && !F32OUT) {  // dv out: 64 rows x 256 bytes from the staging tile, 16-byte stores
+            const uint4 *src = reinterpret_cast<const uint4 *>(sm + S_DD);
+            for (int o = t - 32; o < 64 * 16; o += NT - 32) {
+                const int r = o >> 4, c16 = o & 15;
+                if (r < n)
+                    __stcs(reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(a.dv) +
+                                                     (size_t)(tok0 + r) * p.Hv * DV + (size_t)hv * DV + 8 * c16),
+                           src[o]);
             }
         }
         mma_sync();
@@ -611,6 +592,20 @@ k_tc_bwd_intra(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
             mma_chain_ta<4, 128>(tmem + C_KS, tmem + C_QS, mdesc(sb + S_A, 8192), ID_KM, 0);
             mma_chain_ta<4, 128>(tmem + C_KS, tmem + C_QS, mdesc(sb + S_A + 8192, 8192), ID_KM, 1);
             mma_chain_ta<4, 128>(tmem + C_KS, tmem + C_QS + 32, mdesc(sb + S_A, 8192), ID_KM, 1);
+        }
+        // while A^T Z runs: (E Dl)^T -> value-major hi / lo tile [v][i] in the dDl region (the dv staging
+        // has been written out; the tile's readers are the dq / dk products)
+        {
+            uint32_t dl[16];
+            tmem_ld16(tmem + trow + C_DL + 16 * hh, dl);
+#pragma unroll
+            for (int q2 = 0; q2 < 2; ++q2) {
+                float e8[8], ev8[8];
+                lds8f(Ev + 16 * hh + 8 * q2, ev8);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) e8[e] = ev8[e] * __uint_as_float(dl[8 * q2 + e]);
+                st_split_chunk(sb + S_DD, sb + S_DD + 16384, lrow, 2 * hh + q2, e8);
+            }
         }
         mma_sync();
         if (!ok) break;
