@@ -18,7 +18,10 @@
 // P lo, each a 64 x 64 bf16 tile in the 128-byte-swizzled K-major layout the
 // MMAs read (row r at r * 128, 16-byte chunk c at position c ^ (r & 7)) -- and a
 // 1 KB vector block {gam, exp(gam), exp(gam_last - gam), beta} x 64, ready for
-// plain bulk copies.  Optionally g_cum, A in the io dtype and fp32 A / P.
+// plain bulk copies.  Optionally g_cum, A in the io dtype and fp32 A / P.  Each
+// hi / lo pair is staged in shared memory and leaves by two 8 KB bulk copies (the
+// P pair while the inverse runs, the A pair while the next head starts): per-thread
+// 16-byte stores, each warp store touching 32 rows 128 bytes apart, cost 8 % more.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -37,14 +40,17 @@ constexpr int NT = 128;
 // The k / q tiles are dead once K K^T and Q K^T are in TMEM, so the fp32 scratch reuses their space.
 constexpr uint32_t S_KQ = 0;                          // [kb0: K 8K, Q 8K][kb1: K 8K, Q 8K]
 constexpr uint32_t S_LM = 0;                          // fp32 [64][65]: L, then A in place
-constexpr uint32_t S_TB = S_LM + 64 * 65 * 4;         // fp32 3 x [16][17]
-constexpr uint32_t S_VEC = S_TB + 3 * 16 * 17 * 4;    // gam, Gam, E, beta (64 each)
-constexpr uint32_t S_BAR = 32768;
+constexpr uint32_t S_VEC = S_LM + 64 * 65 * 4;        // gam, Gam, E, beta (64 each)
+constexpr int GB_HEADS = 4;
+constexpr uint32_t S_GB = S_VEC + 4 * 64 * 4;         // g (or g_cum) and beta of up to GB_HEADS value heads x 64 rows
+constexpr uint32_t S_IMG = S_GB + 2 * GB_HEADS * 64 * 4;  // staging of a hi / lo operand image pair (2 x 8 KB)
+// fp32 3 x [16][17], used only between the diagonal blocks and the end of the inverse, when no image is staged
+constexpr uint32_t S_TB = S_IMG;
+constexpr uint32_t S_BAR = S_IMG + 16384;
 constexpr uint32_t S_MISC = S_BAR + 16;
 constexpr uint32_t SMEM_BYTES = S_MISC + 32 + 1024;
-constexpr uint32_t S_GB = S_VEC + 4 * 64 * 4;        // g (or g_cum) and beta of up to 8 value heads x 64 rows
-constexpr int GB_HEADS = 8;
-static_assert(S_GB + 2 * GB_HEADS * 64 * 4 <= S_BAR, "scratch fits in the k / q tile space");
+static_assert(S_IMG % 16 == 0 && S_BAR >= 32768 && S_TB + 3 * 16 * 17 * 4 <= S_BAR, "shared memory map");
+static_assert(SMEM_BYTES + 1024 <= 233472 / 6, "six CTAs per SM");
 
 constexpr uint32_t ID_N64 = idesc_bf16(128, 64, 0, 0);
 
@@ -85,6 +91,7 @@ __device__ void blocked_inverse(float *Lm, float *Tb, int pt) {
 #pragma unroll
         for (int r = 0; r < 16; ++r) Lm[(base + r) * LS + base + jc] = x[r];
     }
+    if (pt == 0) bulk_wait_read_all();  // the P image has left the staging buffer, which takes A's next
     named_bar(1, 128);
     // Off-diagonal blocks, right to left.  Warp w computes block row I = J + 1 + w as register tiles: lane
     // (rq, cq) owns rows 2 rq, 2 rq + 1 and columns 4 cq .. 4 cq + 3 of the block (6 shared loads per 8
@@ -251,6 +258,7 @@ k_tc_prep(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
             bet[t] = bv;
             if (t < n && a.g_cum) a.g_cum[(size_t)(tok0 + t) * p.Hv + hv] = x;
         }
+        if (t == 0) bulk_wait_read_all();  // the previous head's A image has left the staging buffer
         __syncthreads();
         const float glast = gam[n - 1];
         if (t < 64) {
@@ -285,7 +293,7 @@ k_tc_prep(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                         const int i = 8 * ch + e;
                         pv[e] = (i <= r && r < n) ? __expf(gr - gam[i]) * __uint_as_float(raw[8 * cq + e]) : 0.f;
                     }
-                    put_split_chunk(img + 16384, img + 24576, r, ch, pv);
+                    put_split_chunk(sm + S_IMG, sm + S_IMG + 8192, r, ch, pv);
                     if (p32) {
                         reinterpret_cast<float4 *>(p32)[2 * ch] = make_float4(pv[0], pv[1], pv[2], pv[3]);
                         reinterpret_cast<float4 *>(p32)[2 * ch + 1] = make_float4(pv[4], pv[5], pv[6], pv[7]);
@@ -293,7 +301,13 @@ k_tc_prep(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                 }
             }
         }
+        if (t >= 64) fence_proxy_async_smem();  // staged P image -> bulk copy
         __syncthreads();
+        if (t == 0) {
+            bulk_store(img + 16384, sb + S_IMG, 8192);
+            bulk_store(img + 24576, sb + S_IMG + 8192, 8192);
+            bulk_commit();
+        }
         blocked_inverse(Lm, Tb, t);
         {  // A -> image, io-dtype output and fp32 copy: thread holds half a row
             const int r = t >> 1, hh = t & 1;
@@ -303,7 +317,7 @@ k_tc_prep(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                 float vals[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) vals[e] = Lm[r * 65 + 8 * ch + e];
-                put_split_chunk(img, img + 8192, r, ch, vals);
+                put_split_chunk(sm + S_IMG, sm + S_IMG + 8192, r, ch, vals);
                 if (a.A && r < n) {
                     const size_t ao = ((size_t)(tok0 + r) * p.Hv + hv) * C + 8 * ch;
                     if (p.out_f32) {
@@ -325,8 +339,15 @@ k_tc_prep(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
         }
         if (t < 64)  // vector block: 256 floats
             reinterpret_cast<float4 *>(a.vecs + unit * 256)[t] = reinterpret_cast<const float4 *>(gam)[t];
+        fence_proxy_async_smem();  // staged A image -> bulk copy
         __syncthreads();  // Lm, vectors reused by the next head
+        if (t == 0) {
+            bulk_store(img, sb + S_IMG, 8192);
+            bulk_store(img + 8192, sb + S_IMG + 8192, 8192);
+            bulk_commit();
+        }
     }
+    if (t == 0) bulk_wait_all();
     if (!ok && t == 0) {
         if (atomicCAS(p.err + 1, 0u, 301u) == 0u) {
             p.err[2] = (uint32_t)gc;

@@ -30,6 +30,8 @@ CASES = {
     "bf16_no_h0": lambda: small("prefill_b4_t4096", B=2, T=129, Hq=2, Hv=4, seed=15),
     "bf16_strong_decay": lambda: small("longseq_b1_t32k_h8", T=260, Hq=1, Hv=2, g_shift=4.0, seed=16),
     "bf16_dk64_v128": lambda: small("prefill_b4_t4096", B=1, T=100, Hq=1, Hv=2, K=64, V=128, seed=17),
+    # a GVA group of 12 value heads: the prep kernel prepares the gates in two groups (8 + 4)
+    "bf16_gva12": lambda: small("train_b2_t8192_h64", B=1, T=130, Hq=1, Hv=12, seed=28),
 }
 
 
