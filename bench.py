@@ -497,7 +497,9 @@ def _cpulist(text):
 def bind_near_gpu(dev):
     """Best effort: restricts this process to the CPUs local to the GPU (its PCI device's local_cpulist in
     sysfs), so that pinned host buffers allocated now sit in the GPU's nearest host memory.  Returns the
-    previous affinity (to restore) or None."""
+    previous affinity (to restore, or None) and what was found: "bound" (restricted now), "local" (every
+    allowed CPU is already local to the GPU), "none local" (no allowed CPU is) or "unknown" (no locality
+    information)."""
     try:
         bus = subprocess.run(["nvidia-smi", f"--id={dev.index}", "--query-gpu=pci.bus_id", "--format=csv,noheader"],
                              capture_output=True, text=True, timeout=20).stdout.strip()
@@ -505,12 +507,14 @@ def bind_near_gpu(dev):
         with open(f"/sys/bus/pci/devices/{int(dom, 16):04x}:{rest.lower()}/local_cpulist") as fh:
             near = _cpulist(fh.read())
         old = os.sched_getaffinity(0)
-        if near & old and near & old != old:
-            os.sched_setaffinity(0, near & old)
-            return old
     except Exception:
-        pass
-    return None
+        return None, "unknown"
+    if not near & old:
+        return None, "none local"
+    if near & old == old:
+        return None, "local"
+    os.sched_setaffinity(0, near & old)
+    return old, "bound"
 
 
 def copy_rates(host, dev):
@@ -540,7 +544,7 @@ def run_e2e(args, w, x, dev, gdn, world):
     stream) and step k-1's outputs read back (another stream) while step k computes, with two device
     input buffers."""
     names_in = ["q", "k", "v", "g", "beta", "h0", "do", "dht"]
-    old_affinity = bind_near_gpu(dev)  # restored once every pinned buffer exists (after the warm-up)
+    old_affinity, locality = bind_near_gpu(dev)  # restored once every pinned buffer exists (after the warm-up)
     host = {k: x[k].pin_memory() for k in names_in if x[k] is not None}
     cu_cpu = x["cu_seqlens"]
     h2d = sum(t.numel() * t.element_size() for t in host.values())
@@ -617,7 +621,7 @@ def run_e2e(args, w, x, dev, gdn, world):
     ms = max_over_ranks([e0.elapsed_time(e1) / args.steps], world, dev)[0]
     return {"value": round(job_rate(w.tokens, world, ms), 1), "unit": "tokens/s", "ms_per_step": round(ms, 4),
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-            "copy_gbs": {"h2d": h2d_gbs, "d2h": d2h_gbs, "host_buffers_near_gpu": old_affinity is not None},
+            "copy_gbs": {"h2d": h2d_gbs, "d2h": d2h_gbs, "host_cpus": locality},
             "pipelined": "each step's host-to-device inputs and device-to-host outputs are copied on their own "
                          "streams, overlapping the neighbouring steps' compute (two device input buffers)"}
 
