@@ -22,6 +22,8 @@
 // hi / lo pair is staged in shared memory and leaves by two 8 KB bulk copies (the
 // P pair while the inverse runs, the A pair while the next head starts): per-thread
 // 16-byte stores, each warp store touching 32 rows 128 bytes apart, cost 8 % more.
+// The fp32 L / A matrix has an even row stride so that the inverse's block products
+// and the L and A rows move pairs of values per shared-memory access.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -39,17 +41,18 @@ constexpr int NT = 128;
 
 // The k / q tiles are dead once K K^T and Q K^T are in TMEM, so the fp32 scratch reuses their space.
 constexpr uint32_t S_KQ = 0;                          // [kb0: K 8K, Q 8K][kb1: K 8K, Q 8K]
-constexpr uint32_t S_LM = 0;                          // fp32 [64][65]: L, then A in place
-constexpr uint32_t S_VEC = S_LM + 64 * 65 * 4;        // gam, Gam, E, beta (64 each)
+constexpr int LMS = 66;                               // row stride of Lm (even: 8-byte row pairs)
+constexpr uint32_t S_LM = 0;                          // fp32 [64][LMS]: L, then A in place
+constexpr uint32_t S_VEC = S_LM + 64 * LMS * 4;       // gam, Gam, E, beta (64 each)
 constexpr int GB_HEADS = 4;
 constexpr uint32_t S_GB = S_VEC + 4 * 64 * 4;         // g (or g_cum) and beta of up to GB_HEADS value heads x 64 rows
 constexpr uint32_t S_IMG = S_GB + 2 * GB_HEADS * 64 * 4;  // staging of a hi / lo operand image pair (2 x 8 KB)
-// fp32 3 x [16][17], used only between the diagonal blocks and the end of the inverse, when no image is staged
+// fp32 3 x [16][18], used only between the diagonal blocks and the end of the inverse, when no image is staged
 constexpr uint32_t S_TB = S_IMG;
 constexpr uint32_t S_BAR = S_IMG + 16384;
 constexpr uint32_t S_MISC = S_BAR + 16;
 constexpr uint32_t SMEM_BYTES = S_MISC + 32 + 1024;
-static_assert(S_IMG % 16 == 0 && S_BAR >= 32768 && S_TB + 3 * 16 * 17 * 4 <= S_BAR, "shared memory map");
+static_assert(S_IMG % 16 == 0 && S_BAR >= 32768 && S_TB + 3 * 16 * 18 * 4 <= S_BAR, "shared memory map");
 static_assert(SMEM_BYTES + 1024 <= 233472 / 6, "six CTAs per SM");
 
 constexpr uint32_t ID_N64 = idesc_bf16(128, 64, 0, 0);
@@ -67,13 +70,13 @@ struct PrepArgs {
 __device__ __forceinline__ uint64_t kdesc(uint32_t a) { return sdesc_sw128(a, 16, 1024); }
 
 // Blocked in-place inverse of the unit lower-triangular I + L held in Lm
-// ([64][65], strictly lower part = L, rest 0); afterwards Lm = (I + L)^{-1}.
+// ([64][LMS], strictly lower part = L, rest 0); afterwards Lm = (I + L)^{-1}.
 // Column blocks of 16 are processed right to left so that the inverted A_IK
 // (K > J) and the untouched L_KJ are both available:
 //     A_IJ = -(sum_{K=J+1}^{I} A_IK L_KJ) A_JJ.
 // Called by the 128 prep threads (named barrier 1).
 __device__ void blocked_inverse(float *Lm, float *Tb, int pt) {
-    constexpr int LS = 65, TS = 17;
+    constexpr int LS = LMS, TS = 18;
     float x[16];
     const int b = pt >> 4, jc = pt & 15, base = 16 * b;
     if (pt < 64) {  // diagonal blocks: forward substitution, one column per thread
@@ -94,10 +97,13 @@ __device__ void blocked_inverse(float *Lm, float *Tb, int pt) {
     if (pt == 0) bulk_wait_read_all();  // the P image has left the staging buffer, which takes A's next
     named_bar(1, 128);
     // Off-diagonal blocks, right to left.  Warp w computes block row I = J + 1 + w as register tiles: lane
-    // (rq, cq) owns rows 2 rq, 2 rq + 1 and columns 4 cq .. 4 cq + 3 of the block (6 shared loads per 8
-    // FMAs).  Each element is summed in the order K, then k, as the textbook block recursion writes it.
+    // (rq, cq) owns rows 2 rq, 2 rq + 1 and columns 4 cq .. 4 cq + 3 of the block, reading pairs of
+    // adjacent values with 8-byte shared loads (three per 8 FMAs).  Each element is summed in the order K,
+    // then k, as the textbook block recursion writes it.
     const int w = pt >> 5, ln = pt & 31, rq = ln >> 2, cq = ln & 3;
     float *Tw = Tb + w * 16 * TS;  // this warp's 16 x 16 T block
+    auto ld2 = [](const float *p) { return *reinterpret_cast<const float2 *>(p); };
+    auto st2 = [](float *p, float a, float b) { *reinterpret_cast<float2 *>(p) = make_float2(a, b); };
     for (int J = 2; J >= 0; --J) {
         const int I = J + 1 + w;
         if (I <= 3) {
@@ -106,20 +112,25 @@ __device__ void blocked_inverse(float *Lm, float *Tb, int pt) {
                 const float *arow = Lm + (16 * I + 2 * rq) * LS + 16 * K;
                 const float *lcol = Lm + (16 * K) * LS + 16 * J + 4 * cq;
 #pragma unroll
-                for (int k = 0; k < 16; ++k) {
-                    const float x0 = arow[k], x1 = arow[LS + k];
+                for (int k = 0; k < 16; k += 2) {
+                    const float2 xa = ld2(arow + k), xb = ld2(arow + LS + k);
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float y = lcol[k * LS + e];
-                        t0[e] = fmaf(x0, y, t0[e]);
-                        t1[e] = fmaf(x1, y, t1[e]);
+                    for (int kk = 0; kk < 2; ++kk) {
+                        const float x0 = kk ? xa.y : xa.x, x1 = kk ? xb.y : xb.x;
+                        const float2 ya = ld2(lcol + (k + kk) * LS), yb = ld2(lcol + (k + kk) * LS + 2);
+                        const float y[4] = {ya.x, ya.y, yb.x, yb.y};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            t0[e] = fmaf(x0, y[e], t0[e]);
+                            t1[e] = fmaf(x1, y[e], t1[e]);
+                        }
                     }
                 }
             }
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                Tw[(2 * rq) * TS + 4 * cq + e] = t0[e];
-                Tw[(2 * rq + 1) * TS + 4 * cq + e] = t1[e];
+            for (int e = 0; e < 4; e += 2) {
+                st2(Tw + (2 * rq) * TS + 4 * cq + e, t0[e], t0[e + 1]);
+                st2(Tw + (2 * rq + 1) * TS + 4 * cq + e, t1[e], t1[e + 1]);
             }
         }
         named_bar(1, 128);  // every L_KJ has been read before the A_IJ below overwrite them
@@ -127,19 +138,24 @@ __device__ void blocked_inverse(float *Lm, float *Tb, int pt) {
             float o0[4] = {0.f, 0.f, 0.f, 0.f}, o1[4] = {0.f, 0.f, 0.f, 0.f};  // A_IJ = -T_IJ A_JJ
             const float *acol = Lm + (16 * J) * LS + 16 * J + 4 * cq;
 #pragma unroll
-            for (int k = 0; k < 16; ++k) {
-                const float x0 = Tw[(2 * rq) * TS + k], x1 = Tw[(2 * rq + 1) * TS + k];
+            for (int k = 0; k < 16; k += 2) {
+                const float2 xa = ld2(Tw + (2 * rq) * TS + k), xb = ld2(Tw + (2 * rq + 1) * TS + k);
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float y = acol[k * LS + e];
-                    o0[e] = fmaf(x0, y, o0[e]);
-                    o1[e] = fmaf(x1, y, o1[e]);
+                for (int kk = 0; kk < 2; ++kk) {
+                    const float x0 = kk ? xa.y : xa.x, x1 = kk ? xb.y : xb.x;
+                    const float2 ya = ld2(acol + (k + kk) * LS), yb = ld2(acol + (k + kk) * LS + 2);
+                    const float y[4] = {ya.x, ya.y, yb.x, yb.y};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        o0[e] = fmaf(x0, y[e], o0[e]);
+                        o1[e] = fmaf(x1, y[e], o1[e]);
+                    }
                 }
             }
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                Lm[(16 * I + 2 * rq) * LS + 16 * J + 4 * cq + e] = -o0[e];
-                Lm[(16 * I + 2 * rq + 1) * LS + 16 * J + 4 * cq + e] = -o1[e];
+            for (int e = 0; e < 4; e += 2) {
+                st2(Lm + (16 * I + 2 * rq) * LS + 16 * J + 4 * cq + e, -o0[e], -o0[e + 1]);
+                st2(Lm + (16 * I + 2 * rq + 1) * LS + 16 * J + 4 * cq + e, -o1[e], -o1[e + 1]);
             }
         }
         named_bar(1, 128);
@@ -276,9 +292,12 @@ k_tc_prep(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                 const int r = t;
                 const float gr = gam[r], br = bet[r];
 #pragma unroll
-                for (int k = 0; k < 32; ++k) {
+                for (int k = 0; k < 32; k += 2) {  // pairs of entries: 8-byte stores
                     const int i = 32 * half + k;
-                    Lm[r * 65 + i] = (i < r && r < n) ? br * __expf(gr - gam[i]) * __uint_as_float(raw[k]) : 0.f;
+                    const float l0 = (i < r && r < n) ? br * __expf(gr - gam[i]) * __uint_as_float(raw[k]) : 0.f;
+                    const float l1 =
+                        (i + 1 < r && r < n) ? br * __expf(gr - gam[i + 1]) * __uint_as_float(raw[k + 1]) : 0.f;
+                    *reinterpret_cast<float2 *>(Lm + r * LMS + i) = make_float2(l0, l1);
                 }
             } else {  // P = D o Q K^T, lower incl. diagonal -> image (and fp32 copy)
                 const int r = t - 64;
@@ -316,7 +335,11 @@ k_tc_prep(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                 const int ch = 4 * hh + q;
                 float vals[8];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) vals[e] = Lm[r * 65 + 8 * ch + e];
+                for (int e = 0; e < 8; e += 2) {
+                    const float2 v2 = *reinterpret_cast<const float2 *>(Lm + r * LMS + 8 * ch + e);
+                    vals[e] = v2.x;
+                    vals[e + 1] = v2.y;
+                }
                 put_split_chunk(sm + S_IMG, sm + S_IMG + 8192, r, ch, vals);
                 if (a.A && r < n) {
                     const size_t ao = ((size_t)(tok0 + r) * p.Hv + hv) * C + 8 * ch;
