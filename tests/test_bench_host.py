@@ -1,6 +1,7 @@
-"""Host-side helpers of the benchmark that need no GPU: the sysfs CPU-list parser and the placement of
+"""Host-side parts of the benchmark that need no GPU: the sysfs CPU-list parser, the placement of
 the end-to-end leg's pinned buffers near the GPU (its four outcomes, with nvidia-smi, sysfs and the
-affinity calls replaced by fakes)."""
+affinity calls replaced by fakes), and the roofline accounting: the algorithmic work per token and value
+head, the kernels' shares of it, and the DRAM traffic figure tied to the kernel source it was taken on."""
 import io
 import types
 
@@ -59,3 +60,49 @@ def test_bind_unknown_without_locality(monkeypatch, fail):
     # nvidia-smi missing, or a bus id that does not parse
     f = _Fakes(monkeypatch, local="0-3", allowed=range(8), bus="garbage", fail=fail)
     assert bench.bind_near_gpu(DEV) == (None, "unknown") and f.set_calls == []
+
+
+# ---------------------------------------------------------------- roofline accounting
+def _train_workload():
+    from synth import workload
+    return workload("train_b2_t8192_h64")
+
+
+def test_algorithmic_per_token_head_figures():
+    """K = V = 128, C = 64, bf16, G = 4: forward 180,224 flops and 652 + 512 / G bytes, backward 507,904
+    flops and 912 + 1024 / G bytes per token and value head, plus the fp32 states per (sequence, head)."""
+    w = _train_workload()
+    assert (w.K, w.V, w.Hv // w.Hq) == (128, 128, 4)
+    alg = bench.algorithmic(w)
+    th = w.tokens * w.Hv
+    units, st = w.n_seqs * w.Hv, 4 * 128 * 128
+    assert alg["fwd_flops"] == th * 180224
+    assert alg["bwd_flops"] == th * 507904
+    assert alg["fwd_bytes"] == th * (652 + 512 / 4) + units * st * 2              # h0 in, final state out
+    assert alg["bwd_bytes"] == th * (912 + 1024 / 4) + units * st * 3             # h0, dht in, dh0 out
+
+
+def test_kernel_shares_add_up_to_the_passes():
+    w = _train_workload()
+    alg = bench.algorithmic(w)
+    kw = {n: bench.kernel_work(n, w) for n in ("fwd_prep_tc", "fwd_tc", "bwd_prep_tc", "bwd_state_tc",
+                                               "bwd_dscan_tc", "bwd_intra_tc")}
+    assert kw["fwd_prep_tc"][0] + kw["fwd_tc"][0] == alg["fwd_flops"]
+    assert kw["fwd_prep_tc"][1] + kw["fwd_tc"][1] == alg["fwd_bytes"]
+    assert sum(kw[n][0] for n in ("bwd_prep_tc", "bwd_state_tc", "bwd_dscan_tc", "bwd_intra_tc")) \
+        == alg["bwd_flops"]
+    # the gradient kernel's bytes: q, k, dq, dk once per group, v, do, dv, four fp32 vectors
+    th = w.tokens * w.Hv
+    assert kw["bwd_intra_tc"][1] == th * (4 * 128 * 2 / 4 + 3 * 128 * 2 + 16) == 1090519040
+    assert bench.kernel_work("no_such_kernel", w) is None
+
+
+def test_traffic_tied_to_the_kernel_source(monkeypatch):
+    name = "bwd_intra_tc"
+    value, sha = bench.TRAFFIC[name]
+    assert len(bench.source_sha16(name)) == 16
+    monkeypatch.setattr(bench, "source_sha16", lambda k: sha)      # the source the counters were taken on
+    assert bench.traffic_bytes(name) == value
+    monkeypatch.setattr(bench, "source_sha16", lambda k: "0" * 16)  # any other version: not reported
+    assert bench.traffic_bytes(name) is None
+    assert bench.traffic_bytes("fwd_tc") is None
